@@ -1,0 +1,36 @@
+"""CPU oracle for the DSpark draft/verify hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check of
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import
+anything here.  The product (the CUDA library and its Python binding) never
+imports, links or runs this package, and shares no code with it.
+
+Everything is plain numpy in float64 (integers exact), written step by step
+from the pages that define the method, each function citing its passage:
+
+  * "DSpark implementation and evaluation" (ggaaooppeenngg.github.io):
+    §2.2 Sequential Markov Sampling, §3 Markov Head structure, §4 draft step.
+  * "Speculative decoding: from zero to DSpark" (bittide.aicompass.dev):
+    §2 the loop and its lossless property, §6 scheduling by expected
+    throughput, §7 running in a real engine.
+
+Where the pages are silent (the random-number counter layout, the uniform
+mapping, the fixed-point resample, the objective's exact form) the oracle
+takes one plain reading; the same readings are implemented independently by
+the CUDA path.
+
+Pins: every function here is checked by ``tests/test_oracle_*.py`` against
+closed forms, library routines (cuRAND's host Philox generator, numpy/scipy),
+brute force on tiny inputs and statistical laws -- never against the CUDA path.
+"""
+from .philox import philox4x32_10, philox_words, uniform_from_word, gumbel_from_word
+from .draft import draft_logits, markov_sample, markov_bias
+from .verify import verify, acceptance_probability_exact
+from .schedule import schedule, survival_chain
+
+__all__ = [
+    "philox4x32_10", "philox_words", "uniform_from_word", "gumbel_from_word",
+    "draft_logits", "markov_sample", "markov_bias",
+    "verify", "acceptance_probability_exact",
+    "schedule", "survival_chain",
+]
