@@ -1,0 +1,421 @@
+"""Benchmark of the DSpark draft/verify hot path on GB300.
+
+One step = one pass of the whole hot path over one synthetic batch:
+    dspark_draft_logits -> dspark_markov_sample -> dspark_verify -> dspark_schedule
+Metric: draft tokens per second (B*N drafted tokens per step), plus the roofline
+fraction of the dominant kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gpu|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its own
+GPU (requests shard across GPUs with no data exchange: weak scaling); ranks meet
+only at the timing barriers.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import (DRAFT_CONFIGS, VERIFY_CONFIGS, SCHEDULE_CONFIGS, VerifyConfig,  # noqa: E402
+                       ScheduleConfig, draft_inputs, verify_inputs, schedule_inputs, markov_logits)
+
+METRIC = "draft tokens/sec (B·N per draft step) and % of roofline for logits+Markov sampling"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 * 1024 * 1024      # > 4x the 129 MB L2
+WORKLOAD_TEMPERATURE = {"qwen3_8b_single": 1.0, "batched_draft": 0.8, "tiny": 1.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen3_8b_single", choices=sorted(DRAFT_CONFIGS))
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workload construction (host, seeded)
+# ---------------------------------------------------------------------------
+def step_configs(name: str):
+    d = DRAFT_CONFIGS[name]
+    v = VerifyConfig(f"{name}_verify", B=d.B, gamma=d.N, V=d.V, target_std=3.0,
+                     draft_sigmas=(0.3, 1.0, 3.0), independent_draft=False,
+                     data_seed=d.data_seed + 4)
+    s = ScheduleConfig(f"{name}_schedule", B=d.B, N=d.N, K_in=-1,
+                       beta_mix=((9, 1), (5, 2), (2, 3)), sps_len=d.B * d.N,
+                       data_seed=d.data_seed + 5)
+    return d, v, s
+
+
+def host_inputs(name: str):
+    d, v, s = step_configs(name)
+    di = draft_inputs(d)
+    vi = verify_inputs(v)
+    si = schedule_inputs(s)
+    T = np.full(d.B, WORKLOAD_TEMPERATURE[name], np.float32)
+    return d, v, s, di, vi, si, T
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, p[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import draft_sampling_verification_tcgen05_gb300 as ds
+    from draft_sampling_verification_tcgen05_gb300 import _build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    ds.lib()
+
+    d, v, s, di, vi, si, T = host_inputs(args.workload)
+    B, N, V, H, r = d.B, d.N, d.V, d.H, d.r
+    M = B * N
+    # device-resident inputs and fixed output buffers
+    X = di["hidden"].to(dev)
+    W = di["lm_head"].to(dev)
+    w1 = di["w1"].to(dev)
+    w2 = di["w2"].to(dev)
+    anchor = torch.from_numpy(di["anchor"]).to(dev)
+    temp = torch.from_numpy(T).to(dev)
+    p_t = torch.from_numpy(vi["p_t"]).to(dev)
+    p_d = torch.from_numpy(vi["p_d"]).to(dev)
+    conf = torch.from_numpy(si["cond_accept"]).to(dev)
+    sps = torch.from_numpy(si["sps"]).to(dev)
+    L = torch.empty(M, V, dtype=torch.float32, device=dev)
+    tok = torch.empty(B, N, dtype=torch.int32, device=dev)
+    out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    surv = torch.empty(B, N, dtype=torch.float32, device=dev)
+    K_out = torch.empty(1, dtype=torch.int32, device=dev)
+    lens = torch.empty(B, dtype=torch.int32, device=dev)
+    sel = torch.empty(B * N, dtype=torch.int32, device=dev)
+    ws_g = ds.Workspace(ds.OP_DRAFT_LOGITS, device=dev)
+    ws_m = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
+    ws_v = ds.Workspace(ds.OP_VERIFY, device=dev)
+    ws_s = ds.Workspace(ds.OP_SCHEDULE, B, N, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+
+    def step(k=None):
+        e = ev[k] if k is not None else None
+        if e: e[0].record(stream)
+        ds.dspark_draft_logits(X, W, logits=L, workspace=ws_g)
+        if e: e[1].record(stream)
+        ds.dspark_markov_sample(L.view(B, N, V), anchor, w1, w2, temp, 0, 0, draft_tokens=tok,
+                                workspace=ws_m)
+        if e: e[2].record(stream)
+        ds.dspark_verify(p_t, p_d, tok, None, 2, 0, out_tokens=out, num_accepted=nacc, workspace=ws_v)
+        if e: e[3].record(stream)
+        ds.dspark_schedule(conf, sps, -1, survival=surv, K_out=K_out, lengths=lens, selected=sel,
+                           workspace=ws_s)
+        if e: e[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    for wsx in (ws_g, ws_m, ws_v, ws_s):
+        st, bits = ds.dspark_read_status(wsx)
+        if st not in (0,):
+            raise RuntimeError(f"device status {st} bits {bits:#x} after warm-up")
+
+    # ---------------- timed region (device-resident inputs) ----------------
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(float(k))                 # L2 flush between timed steps (not timed)
+            step(k)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    per = np.array([[ev[k][j].elapsed_time(ev[k][j + 1]) for j in range(4)] for k in range(args.steps)])
+    step_ms = float(per.sum(axis=1).mean())
+    kernel_ms = per.mean(axis=0)                  # draft_logits, markov, verify, schedule
+    if dist is not None:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * M / (step_ms / 1e3)
+
+    # ---------------- end to end through host buffers ----------------
+    e2e = None
+    if not args.skip_e2e:
+        h_X = di["hidden"].pin_memory()
+        h_anchor = torch.from_numpy(di["anchor"]).pin_memory()
+        h_T = torch.from_numpy(T).pin_memory()
+        h_pt = torch.from_numpy(vi["p_t"]).pin_memory()
+        h_pd = torch.from_numpy(vi["p_d"]).pin_memory()
+        h_c = torch.from_numpy(si["cond_accept"]).pin_memory()
+        h_sps = torch.from_numpy(si["sps"]).pin_memory()
+        h_out = torch.empty_like(out, device="cpu").pin_memory()
+        h_nacc = torch.empty_like(nacc, device="cpu").pin_memory()
+        h_tok = torch.empty_like(tok, device="cpu").pin_memory()
+        h_K = torch.empty_like(K_out, device="cpu").pin_memory()
+        h_lens = torch.empty_like(lens, device="cpu").pin_memory()
+        ins = [(X, h_X), (anchor, h_anchor), (temp, h_T), (p_t, h_pt), (p_d, h_pd), (conf, h_c), (sps, h_sps)]
+        outs = [(h_tok, tok), (h_out, out), (h_nacc, nacc), (h_K, K_out), (h_lens, lens)]
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
+        d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for k in range(args.warmup + args.steps):
+            timed = k >= args.warmup
+            flush.fill_(float(k))
+            if timed:
+                e0[k - args.warmup].record(stream)
+            for dst, src in ins:
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in outs:
+                dst.copy_(src, non_blocking=True)
+            if timed:
+                e1[k - args.warmup].record(stream)
+            stream.synchronize()
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(e0, e1)]))
+        if dist is not None:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * M / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    # ---------------- roofline of the dominant kernel ----------------
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    peak_src = "measured" if peaks else "fallback"
+    esize = 2 if d.dtype == "bf16" else 4
+    gemm_bytes = (V * H + M * H) * esize + M * V * 4
+    gemm_flops = 2.0 * M * H * V
+    markov_bytes = M * V * 4 + V * r * esize + B * N * r * esize
+    t_gemm = kernel_ms[0] / 1e3
+    gemm_bound = "hbm" if gemm_bytes / (hbm_peak * 1e9) >= gemm_flops / (bf16_peak * 1e12) else "tensor"
+    if gemm_bound == "hbm":
+        ach = gemm_bytes / t_gemm / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak}
+    else:
+        ach = gemm_flops / t_gemm / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s", "frac": ach / bf16_peak}
+    roof["kernel"] = "dspark_draft_logits"
+    roof["peak_source"] = peak_src
+    roof["traffic"] = None
+
+    if dist is not None and rank != 0:
+        dist.barrier()
+        dist.destroy_process_group()
+        return
+
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": d.dtype, "data": "synthetic",
+        "config": {"workload": f"{d.name}: B={B} N={N} H={H} V={V} r={r} {d.dtype} "
+                               f"T={WORKLOAD_TEMPERATURE[args.workload]}, verify gamma={N}, "
+                               f"schedule over B*N={M} candidates",
+                   "global_batch_requests": B * world, "draft_tokens_per_step": M * world,
+                   "parallelism": f"replicas x{world} (requests sharded, no collective)",
+                   "l2": "flushed (512 MB write) between timed steps"},
+        "kernel_ms": {"draft_logits": kernel_ms[0], "markov_sample": kernel_ms[1],
+                      "verify": kernel_ms[2], "schedule": kernel_ms[3]},
+        "roofline": roof,
+        "markov_roofline": {"bound": "hbm", "algorithmic_bytes": markov_bytes,
+                            "achieved": markov_bytes / (kernel_ms[1] / 1e3) / 1e9, "peak": hbm_peak,
+                            "unit": "GB/s", "frac": markov_bytes / (kernel_ms[1] / 1e3) / 1e9 / hbm_peak},
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if not args.skip_cpu_baseline and rank == 0:
+        res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, (d, v, s, di, vi, si, T))
+    print(json.dumps(res))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_step(name, inputs, req):
+    """The whole hot path on the CPU oracle for the requests `req` of one batch."""
+    import oracle
+    d, v, s, di, vi, si, T = inputs
+    rows = (req[:, None] * d.N + np.arange(d.N)[None, :]).reshape(-1)
+    Lr = oracle.draft_logits(di["hidden_f32"][rows], di["lm_head_f32"]).reshape(len(req), d.N, d.V)
+    tok, _, _ = oracle.markov_sample(Lr, di["anchor"][req], di["w1_f32"], di["w2_f32"], T[req], 0, 0,
+                                     req_ids=req)
+    oracle.verify(vi["p_t"][req], vi["p_d"][req], tok, None, 2, 0, req_ids=req)
+    oracle.schedule(si["cond_accept"][req], si["sps"][: len(req) * d.N], -1)
+    return len(req) * d.N
+
+
+def cpu_baseline(name, budget_s, inputs):
+    d = inputs[0]
+    t0 = time.perf_counter()
+    tokens = 0
+    b = 0
+    while True:
+        tokens += oracle_step(name, inputs, np.array([b % d.B]))
+        b += 1
+        if time.perf_counter() - t0 >= budget_s or b >= 64:
+            break
+    el = time.perf_counter() - t0
+    return {"value": tokens / el, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"{b} request(s) of {d.name} through the whole path on the CPU oracle "
+                      f"(fp64 numpy): {tokens} draft tokens in {el:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    d, v, s, di, vi, si, T = host_inputs(args.workload)
+    inputs = (d, v, s, di, vi, si, T)
+    per_step_budget = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_step(args.workload, inputs, np.array([0]))
+    times, toks = [], 0
+    for k in range(args.steps):
+        t0 = time.perf_counter()
+        n = 0
+        b = k
+        while True:
+            n += oracle_step(args.workload, inputs, np.array([b % d.B]))
+            b += args.steps
+            if time.perf_counter() - t0 >= per_step_budget or n >= d.B * d.N:
+                break
+        times.append(time.perf_counter() - t0)
+        toks += n
+    value = toks / sum(times)
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": f"{d.name}: B={d.B} N={d.N} H={d.H} V={d.V} r={d.r} {d.dtype}",
+                      "note": "CPU oracle, each step a bounded sample of requests of the workload"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                            "sample": f"{toks} draft tokens over {args.steps} steps"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,424 @@
+// Sequential Markov-biased Gumbel-max sampling of N draft tokens per request.
+//
+// "DSpark implementation and evaluation" §2.2 (_sample_sequential): for
+// i = 0..N-1, bias = markov_w2 . markov_w1[prev] is added to base_logits[:, i],
+// a token is Gumbel-sampled and becomes prev; §3: markov_w1 is an
+// Embedding(V, r), markov_w2 a bias-free r -> V linear.
+//
+// One persistent cooperative kernel runs all N steps.  Block c owns a
+// contiguous vocabulary slice [v_lo, v_hi) for the whole call; per step:
+//   1. prev_b (the anchor, or the previous step's winner) -> w1 row gather
+//      into shared memory (E[b, :])
+//   2. pass 1: z = (base + w2 . E[b]) / T_b for every v of the slice, kept in
+//      shared memory; the block's argmax of z is perturbed with its own Gumbel
+//      noise, giving a real candidate value y*, published as a lower bound
+//      LB[i][b] (atomicMax) and as a candidate key
+//   3. pass 2: Gumbel noise only for elements that can still win:
+//      z + G_max >= LB (G_max bounds every variate), each candidate (value,
+//      index) folded into a 64-bit key; block reduction, then one atomicMax
+//      per (block, b) into the step's slot -- the two-level argmax
+//   4. grid barrier; every block reads the B winners as the next prev.
+// Rows of z never leave the block: no [B, V] array is written to memory.
+// Ties go to the lowest index through the key encoding; the result does not
+// depend on which elements were skipped, because a skipped element is
+// strictly below the bound, which is itself a value some element reaches.
+#include "device_common.cuh"
+#include "host_common.h"
+
+#include <algorithm>
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxGrid = 1024;                         // workspace is sized for this many blocks
+constexpr size_t kW2CacheBytes = 144 * 1024;           // w2 slice kept in shared memory when it fits
+constexpr size_t kZStoreBytes = 32 * 1024;             // z rows kept in shared memory when they fit
+constexpr int kMaxEFloats = 16384;                     // B * r limit of the shared E matrix
+constexpr uint32_t kWaitStep = 0x200;                  // + step index
+
+struct MarkovLayout {
+    unsigned long long* slots;   // [N][B] argmax keys
+    uint32_t* lb;                // [N][B] order bits of the published lower bound
+    float2* lse_part;            // [2][kMaxGrid][B] (max, sum) partials
+};
+
+__host__ __device__ inline MarkovLayout markov_layout(void* ws, int B, int N) {
+    uint8_t* p = static_cast<uint8_t*>(ws) + sizeof(WsHeader);
+    MarkovLayout L;
+    L.slots = reinterpret_cast<unsigned long long*>(p);
+    p += sizeof(unsigned long long) * static_cast<size_t>(N) * B;
+    L.lb = reinterpret_cast<uint32_t*>(p);
+    p += sizeof(uint32_t) * static_cast<size_t>(N) * B;
+    p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15));
+    L.lse_part = reinterpret_cast<float2*>(p);
+    return L;
+}
+
+struct MarkovArgs {
+    const float* base;          // [B, N, V]
+    const int32_t* anchor;      // [B]
+    const void* w1;             // [V, r]
+    const void* w2;             // [V, r]
+    const float* temperature;   // [B]
+    int32_t* tokens;            // [B, N]
+    float* lse;                 // [B, N] or null
+    WsHeader* ws;
+    MarkovLayout lay;
+    uint64_t seed;
+    uint32_t offset;
+    int B, N, V, r;
+    int slice;                  // vocabulary entries per block
+    int w2_cached;              // w2 slice lives in shared memory
+    int w2_pitch;               // bytes per cached w2 row (padded)
+    int z_stored;               // z rows live in shared memory
+    long long timeout_ns;
+};
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// dot(w2 row, E row) over r, fp32 accumulation in k order.
+template <typename WT>
+__device__ __forceinline__ float bias_dot(const uint8_t* row, const float* e, int r) {
+    float acc = 0.f;
+    if constexpr (sizeof(WT) == 2) {
+        int k = 0;
+        if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+            for (; k + 8 <= r; k += 8) {
+                const uint4 q = *reinterpret_cast<const uint4*>(row + 2 * k);
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __bfloat1622float2(h[j]);
+                    acc = fmaf(f.x, e[k + 2 * j], acc);
+                    acc = fmaf(f.y, e[k + 2 * j + 1], acc);
+                }
+            }
+        }
+        for (; k < r; ++k)
+            acc = fmaf(__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(row)[k]), e[k], acc);
+    } else {
+        int k = 0;
+        if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+            for (; k + 4 <= r; k += 4) {
+                const float4 q = *reinterpret_cast<const float4*>(row + 4 * k);
+                acc = fmaf(q.x, e[k], acc);
+                acc = fmaf(q.y, e[k + 1], acc);
+                acc = fmaf(q.z, e[k + 2], acc);
+                acc = fmaf(q.w, e[k + 3], acc);
+            }
+        }
+        for (; k < r; ++k) acc = fmaf(reinterpret_cast<const float*>(row)[k], e[k], acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ float gumbel_at(const MarkovArgs& a, int b, int i, int v) {
+    const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(b),
+                              kStreamGumbel, static_cast<uint32_t>(i));
+    const uint32_t sel = static_cast<uint32_t>(v) & 3u;
+    const uint32_t word = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
+    return gumbel_from_word(word);
+}
+
+__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long k, unsigned long long* red) {
+    k = warp_max_u64(k);
+    __syncthreads();
+    if (lane_id() == 0) red[warp_id()] = k;
+    __syncthreads();
+    unsigned long long m = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) m = red[w] > m ? red[w] : m;
+    return m;
+}
+
+__device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
+    if (a.y == 0.f) return b;
+    if (b.y == 0.f) return a;
+    const float m = fmaxf(a.x, b.x);
+    return make_float2(m, a.y * __expf(a.x - m) + b.y * __expf(b.x - m));
+}
+
+__device__ __forceinline__ float2 block_lse(float2 v, float2* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float2 other;
+        other.x = __shfl_xor_sync(0xFFFFFFFFu, v.x, o);
+        other.y = __shfl_xor_sync(0xFFFFFFFFu, v.y, o);
+        v = lse_merge(v, other);
+    }
+    __syncthreads();
+    if (lane_id() == 0) red[warp_id()] = v;
+    __syncthreads();
+    float2 m = make_float2(0.f, 0.f);
+    for (int w = 0; w < kWarps; ++w) m = lse_merge(m, red[w]);
+    return m;
+}
+
+// Reads a token from a step slot; key 0 means no finite candidate existed.
+__device__ __forceinline__ int slot_token(const MarkovArgs& a, int i, int b) {
+    const unsigned long long k = __ldcg(a.lay.slots + static_cast<size_t>(i) * a.B + b);
+    if (k == 0ull) {
+        set_status(a.ws, DSPARK_STATUS_NUMERIC);
+        return 0;
+    }
+    return static_cast<int>(key_index(k));
+}
+
+// Combine the lse partials of step i for the requests this block finalises.
+__device__ void finish_lse(const MarkovArgs& a, int i) {
+    if (a.lse == nullptr) return;
+    const float2* part = a.lay.lse_part + static_cast<size_t>(i & 1) * kMaxGrid * a.B;
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.B; b += gridDim.x * blockDim.x) {
+        float2 m = make_float2(0.f, 0.f);
+        for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
+            const float2 p = __ldcg(part + static_cast<size_t>(c) * a.B + b);
+            m = lse_merge(m, p);
+        }
+        a.lse[static_cast<size_t>(b) * a.N + i] = m.y > 0.f ? m.x + logf(m.y) : -INFINITY;
+    }
+}
+
+template <typename WT>
+__global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sp = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
+    __shared__ unsigned long long s_red[kWarps];
+    __shared__ float2 s_red2[kWarps];
+    __shared__ float s_bcast[2];
+
+    const int v_lo = blockIdx.x * a.slice;
+    const int v_hi = min(a.V, v_lo + a.slice);
+    const int n_local = max(0, v_hi - v_lo);
+    const int tid = threadIdx.x;
+
+    // shared-memory carve-up: [w2 cache][z store][E][prev]
+    uint8_t* w2s = sp;
+    sp += a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
+    float* zs = reinterpret_cast<float*>(sp);
+    sp += a.z_stored ? sizeof(float) * static_cast<size_t>(a.slice) * a.B : 0;
+    float* E = reinterpret_cast<float*>(sp);
+    sp += sizeof(float) * static_cast<size_t>(a.B) * a.r;
+    int* prev = reinterpret_cast<int*>(sp);
+
+    const size_t row_bytes = sizeof(WT) * static_cast<size_t>(a.r);
+    if (a.w2_cached) {
+        // load this block's w2 rows once; rows padded to w2_pitch bytes
+        const uint8_t* src = static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v_lo) * row_bytes;
+        const int chunks = static_cast<int>(row_bytes / 16);
+        for (int idx = tid; idx < n_local * chunks; idx += kThreads) {
+            const int v = idx / chunks, c = idx % chunks;
+            *reinterpret_cast<uint4*>(w2s + static_cast<size_t>(v) * a.w2_pitch + 16 * c) =
+                __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(v) * row_bytes + 16 * c));
+        }
+    }
+
+    bool alive = true;
+    for (int i = 0; i < a.N && alive; ++i) {
+        // ---- 1. previous tokens and the Markov embedding E[b] = w1[prev_b] ----
+        for (int b = tid; b < a.B; b += kThreads) {
+            int p;
+            if (i == 0) {
+                p = a.anchor[b];
+                if (p < 0 || p >= a.V) {
+                    set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+                    p = 0;
+                }
+            } else {
+                p = slot_token(a, i - 1, b);
+            }
+            prev[b] = p;
+        }
+        if (i > 0) finish_lse(a, i - 1);
+        __syncthreads();
+        for (int idx = tid; idx < a.B * a.r; idx += kThreads) {
+            const int b = idx / a.r, k = idx % a.r;
+            E[idx] = to_f<WT>(static_cast<const WT*>(a.w1)[static_cast<size_t>(prev[b]) * a.r + k]);
+        }
+        __syncthreads();
+
+        unsigned long long* slot = a.lay.slots + static_cast<size_t>(i) * a.B;
+        uint32_t* lbs = a.lay.lb + static_cast<size_t>(i) * a.B;
+        float2* lse_part = a.lay.lse_part + static_cast<size_t>(i & 1) * kMaxGrid * a.B;
+
+        for (int b = 0; b < a.B; ++b) {
+            float T = __ldg(a.temperature + b);
+            if (!(T >= 0.f) || isinf(T)) {
+                if (tid == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+                T = 0.f;
+            }
+            const bool hot = T > 0.f;
+            const float invT = hot ? __frcp_rn(T) : 1.f;
+            const float* lrow = a.base + (static_cast<size_t>(b) * a.N + i) * a.V;
+            const float* e = E + static_cast<size_t>(b) * a.r;
+
+            // ---- 2. pass 1: z for the slice, block argmax of z ----
+            unsigned long long best = 0ull;
+            float2 ls = make_float2(0.f, 0.f);
+            bool bad = false;
+            for (int t = tid; t < n_local; t += kThreads) {
+                const int v = v_lo + t;
+                const uint8_t* wrow = a.w2_cached ? w2s + static_cast<size_t>(t) * a.w2_pitch
+                                                  : static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v) * row_bytes;
+                const float bias = bias_dot<WT>(wrow, e, a.r);
+                const float s = __fadd_rn(__ldcs(lrow + v), bias);
+                const float z = hot ? __fmul_rn(s, invT) : s;
+                if (a.z_stored) zs[static_cast<size_t>(b) * a.slice + t] = z;
+                if (z != z) { bad = true; continue; }
+                const unsigned long long k = argmax_key(z, static_cast<uint32_t>(v));
+                best = k > best ? k : best;
+                if (a.lse != nullptr && z > -INFINITY) ls = lse_merge(ls, make_float2(z, 1.f));
+            }
+            if (bad) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+            best = block_max_u64(best, s_red);
+            if (a.lse != nullptr) {
+                ls = block_lse(ls, s_red2);
+                if (tid == 0) lse_part[static_cast<size_t>(blockIdx.x) * a.B + b] = ls;
+            }
+            if (tid == 0 && best != 0ull) {
+                const uint32_t vb = key_index(best);
+                if (hot) {
+                    const float zb = float_from_order_bits(static_cast<uint32_t>(best >> 32));
+                    const float y = __fadd_rn(zb, gumbel_at(a, b, i, static_cast<int>(vb)));
+                    atomicMax(lbs + b, float_order_bits(y));
+                    atomicMax(slot + b, argmax_key(y, vb));
+                } else {
+                    atomicMax(slot + b, best);
+                }
+            }
+            if (!hot) continue;
+
+            // ---- 3. pass 2: Gumbel noise where the element can still win ----
+            __syncthreads();
+            if (tid == 0) s_bcast[0] = float_from_order_bits(__ldcg(lbs + b));
+            __syncthreads();
+            const float lb = s_bcast[0];
+            best = 0ull;
+            for (int t = tid; t < n_local; t += kThreads) {
+                const int v = v_lo + t;
+                float z;
+                if (a.z_stored) {
+                    z = zs[static_cast<size_t>(b) * a.slice + t];
+                } else {
+                    const uint8_t* wrow = a.w2_cached ? w2s + static_cast<size_t>(t) * a.w2_pitch
+                                                      : static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v) * row_bytes;
+                    z = __fmul_rn(__fadd_rn(__ldg(lrow + v), bias_dot<WT>(wrow, e, a.r)), invT);
+                }
+                if (!(__fadd_rn(z, kGumbelMax) >= lb)) continue;      // cannot win (or NaN)
+                const float y = __fadd_rn(z, gumbel_at(a, b, i, v));
+                if (y != y) continue;
+                const unsigned long long k = argmax_key(y, static_cast<uint32_t>(v));
+                best = k > best ? k : best;
+            }
+            best = block_max_u64(best, s_red);
+            if (tid == 0 && best != 0ull) atomicMax(slot + b, best);
+        }
+
+        // ---- 4. all blocks agree on the step's winners ----
+        alive = grid_barrier(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i);
+    }
+    if (!alive) return;
+    __threadfence();
+    finish_lse(a, a.N - 1);
+    if (blockIdx.x == 0) {
+        for (int idx = tid; idx < a.B * a.N; idx += kThreads) {
+            const int b = idx / a.N, i = idx % a.N;
+            a.tokens[idx] = slot_token(a, i, b);
+        }
+    }
+}
+
+template <typename WT>
+dspark_status run_generic(MarkovArgs& a, cudaStream_t stream, const DeviceInfo& dev) {
+    // one block per SM; each block owns ceil(V / grid) vocabulary entries (multiple of 32)
+    int grid = std::min(dev.sm_count, (a.V + 255) / 256);
+    grid = std::max(1, std::min(grid, kMaxGrid));
+    a.slice = ((a.V + grid - 1) / grid + 31) & ~31;
+    grid = (a.V + a.slice - 1) / a.slice;
+    const size_t row_bytes = sizeof(WT) * static_cast<size_t>(a.r);
+    a.w2_pitch = static_cast<int>(row_bytes + 16);
+    a.w2_cached = (row_bytes % 16 == 0) && static_cast<size_t>(a.slice) * a.w2_pitch <= kW2CacheBytes;
+    a.z_stored = sizeof(float) * static_cast<size_t>(a.slice) * a.B <= kZStoreBytes;
+    if (static_cast<size_t>(a.B) * a.r > static_cast<size_t>(kMaxEFloats)) {
+        set_error("markov_sample: B*r = %d exceeds the %d the sampler holds on chip", a.B * a.r, kMaxEFloats);
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    size_t smem = 16;
+    smem += a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
+    smem += a.z_stored ? sizeof(float) * static_cast<size_t>(a.slice) * a.B : 0;
+    smem += sizeof(float) * static_cast<size_t>(a.B) * a.r + sizeof(int) * static_cast<size_t>(a.B);
+    if (smem > dev.smem_optin) {
+        set_error("markov_sample: needs %zu bytes of shared memory", smem);
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    auto kernel = markov_generic_kernel<WT>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(markov_sample)");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    if (e != cudaSuccess) return cuda_error(e, "occupancy(markov_sample)");
+    if (per_sm * dev.sm_count < grid) {
+        set_error("markov_sample: %d blocks cannot be co-resident", grid);
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, a);
+    if (e != cudaSuccess) return cuda_error(e, "launch(markov_sample)");
+    return DSPARK_OK;
+}
+
+}  // namespace
+
+size_t markov_workspace_bytes(int B, int N) {
+    const size_t nb = static_cast<size_t>(B) * N;
+    size_t bytes = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t);
+    bytes = (bytes + 15) & ~static_cast<size_t>(15);
+    bytes += 2 * static_cast<size_t>(kMaxGrid) * B * sizeof(float2);
+    return bytes;
+}
+
+dspark_status launch_markov_sample(const float* base_logits, const int32_t* anchor, const void* w1,
+                                   const void* w2, dspark_dtype wdtype, const float* temperature,
+                                   uint64_t seed, uint32_t offset, int B, int N, int V, int r,
+                                   int32_t* draft_tokens, float* lse, void* ws, cudaStream_t stream,
+                                   const DeviceInfo& dev) {
+    // clear header, slots and bounds (the lse partials need no clearing)
+    const size_t nb = static_cast<size_t>(B) * N;
+    const size_t clear = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t);
+    dspark_status st = clear_workspace(ws, clear, stream);
+    if (st != DSPARK_OK) return st;
+    MarkovArgs a = {};
+    a.base = base_logits;
+    a.anchor = anchor;
+    a.w1 = w1;
+    a.w2 = w2;
+    a.temperature = temperature;
+    a.tokens = draft_tokens;
+    a.lse = lse;
+    a.ws = static_cast<WsHeader*>(ws);
+    a.lay = markov_layout(ws, B, N);
+    a.seed = seed;
+    a.offset = offset;
+    a.B = B;
+    a.N = N;
+    a.V = V;
+    a.r = r;
+    a.timeout_ns = kDefaultTimeoutNs;
+    if (wdtype == DSPARK_BF16) return run_generic<__nv_bfloat16>(a, stream, dev);
+    return run_generic<float>(a, stream, dev);
+}
+
+}  // namespace dspark

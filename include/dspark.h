@@ -1,0 +1,243 @@
+/*
+ * dspark.h -- C ABI of the DSpark draft-sampling / verification hot path on one
+ * GB300 (sm_103a).
+ *
+ * Four operations, each one or two kernel launches on the caller's stream:
+ *
+ *   dspark_draft_logits   base logits of the draft LM head (tcgen05 GEMM)
+ *   dspark_markov_sample  N-step Markov-biased Gumbel-max sampling (one
+ *                         persistent kernel)
+ *   dspark_verify         lossless speculative rejection sampling
+ *   dspark_schedule       confidence-scheduled admission (survival chain,
+ *                         global radix sort, throughput-optimal K, fill)
+ *
+ * Conventions shared by every call
+ *   - All array arguments are DEVICE pointers on the current CUDA device,
+ *     contiguous and row-major, owned by the caller.  The library never
+ *     allocates, frees or synchronises inside these calls, so every call can
+ *     be captured in a CUDA graph (the caller keeps the buffers at fixed
+ *     addresses, as the draft step of "DSpark implementation and evaluation"
+ *     §6 does).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).
+ *   - Host-side argument errors return DSPARK_ERR_INVALID_ARG or
+ *     DSPARK_ERR_UNSUPPORTED synchronously and launch nothing.  A failed
+ *     launch returns DSPARK_ERR_CUDA (see dspark_last_error()).
+ *   - Errors found on the device (a wait that timed out, non-finite or
+ *     out-of-range inputs) set bits in the status word at the start of the
+ *     caller's workspace; dspark_read_status() reads it.  Each call clears
+ *     the status word of the workspace it is given before launching.
+ *   - Random numbers: a counter-based Philox4x32-10 generator keyed by
+ *     `seed`; `offset` (< 2^32) selects an independent stream, so the caller
+ *     advances it per decode step.  Outputs are a pure function of the inputs
+ *     and (seed, offset).
+ *   - Workspace: device memory of at least dspark_workspace_size() bytes,
+ *     256-byte aligned, used by one call at a time (calls that overlap on the
+ *     GPU must use different workspaces).
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or workspace  */
+    DSPARK_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle  */
+    DSPARK_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed       */
+    DSPARK_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out         */
+    DSPARK_ERR_NUMERIC = 5,       /* non-finite input or a distribution with no mass */
+    DSPARK_ERR_INPUT_RANGE = 6    /* a token id, length or probability out of range  */
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+typedef enum {
+    DSPARK_OP_DRAFT_LOGITS = 0,
+    DSPARK_OP_MARKOV_SAMPLE = 1,
+    DSPARK_OP_VERIFY = 2,
+    DSPARK_OP_SCHEDULE = 3
+} dspark_op;
+
+/* Device status-word bits (OR-ed by kernels; read with dspark_read_status). */
+#define DSPARK_STATUS_TIMEOUT      0x1u
+#define DSPARK_STATUS_NUMERIC      0x2u
+#define DSPARK_STATUS_INPUT_RANGE  0x4u
+#define DSPARK_STATUS_INTERNAL     0x8u
+
+/*
+ * Bytes of workspace an operation needs.  op is a dspark_op; for
+ * DSPARK_OP_DRAFT_LOGITS and DSPARK_OP_VERIFY only the status word is needed
+ * (256 bytes); for DSPARK_OP_MARKOV_SAMPLE it grows with B*N and B; for
+ * DSPARK_OP_SCHEDULE with B*N.  Arguments an op does not use are ignored.
+ * Returns 0 for an unknown op or negative sizes.
+ */
+DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);
+
+/*
+ * Base logits of the draft LM head:  logits[m, v] = sum_h hidden[m, h] * lm_head[v, h].
+ *
+ * "DSpark implementation and evaluation" §2.2 (compute_draft_logits: all N
+ * positions of every request through the LM head at once, giving [B, N, V]) and
+ * §4 (the draft step).  Here M = B*N rows.
+ *
+ *   hidden   [M, H]  dtype (bf16 or fp32), device
+ *   lm_head  [V, H]  dtype, device
+ *   logits   [M, V]  fp32, device (output)
+ * bf16 inputs are multiplied exactly and accumulated in fp32 on the tensor
+ * cores (tcgen05 kind::f16); fp32 inputs run as tf32 (kind::tf32).
+ * Requirements: 1 <= M, 1 <= V < 2^31, 1 <= H, H*sizeof(dtype) a multiple of
+ * 16 bytes, hidden/lm_head 16-byte aligned, logits 4-byte aligned.
+ * workspace: >= dspark_workspace_size(DSPARK_OP_DRAFT_LOGITS, ...) bytes.
+ */
+DSPARK_API dspark_status dspark_draft_logits(const void* hidden, const void* lm_head, dspark_dtype dtype,
+                                  int M, int H, int V, float* logits,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Sequential Markov-biased Gumbel-max sampling of N draft tokens per request.
+ *
+ * "DSpark implementation and evaluation" §2.2 (_sample_sequential) and §3
+ * (the low-rank Markov head).  For each request b, prev = anchor[b]; for
+ * i = 0..N-1:
+ *     bias[v] = sum_k w2[v, k] * w1[prev, k]
+ *     z[v]    = (base_logits[b, i, v] + bias[v]) / T_b          (T_b > 0)
+ *     x       = argmax_v (z[v] + g[v])   ties to the lowest v
+ *     draft_tokens[b, i] = x;  prev = x
+ * with g the stream-0 Gumbel noise of counter (v >> 2, b, i, offset), word
+ * v & 3.  T_b = 0 means greedy: x = argmax_v (base + bias), no noise.
+ * The [B, V] row of z is never written to device memory.
+ *
+ *   base_logits  [B, N, V] fp32, device (row (b, i) contiguous over v)
+ *   anchor       [B] int32, device, each in [0, V)
+ *   w1, w2       [V, r] wdtype (bf16 or fp32), device (markov_w1 embedding and
+ *                markov_w2 projection, both stored [V, r])
+ *   temperature  [B] fp32, device, each >= 0 and finite
+ *   draft_tokens [B, N] int32, device (output)
+ *   lse          [B, N] fp32 device output or NULL: log-sum-exp over v of z
+ *                (of base + bias when T_b = 0), so that
+ *                p_d(x) = exp(z[x] - lse) downstream.
+ * Requirements: B, N >= 1, N <= 65535, 2 <= V < 2^31, 1 <= r <= 1024,
+ * offset < 2^32.  Device-side: an anchor outside [0, V) sets INPUT_RANGE and
+ * is read as 0; a negative or non-finite temperature sets NUMERIC and is read
+ * as 0 (greedy); non-finite logits are skipped by the argmax and set NUMERIC.
+ * workspace: >= dspark_workspace_size(DSPARK_OP_MARKOV_SAMPLE, B, N, V, r).
+ */
+DSPARK_API dspark_status dspark_markov_sample(const float* base_logits, const int32_t* anchor,
+                                   const void* w1, const void* w2, dspark_dtype wdtype,
+                                   const float* temperature, uint64_t seed, uint64_t offset,
+                                   int B, int N, int V, int r,
+                                   int32_t* draft_tokens, float* lse,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Lossless speculative verification (rejection sampling) of a block of gamma
+ * draft tokens per request.
+ *
+ * "Speculative decoding: from zero to DSpark" §2: draft token x_k is accepted
+ * with probability min(1, p_t(x_k) / p_d(x_k)), decided as
+ * fl32(u_k * p_d[b,k,x_k]) < p_t[b,k,x_k] with u_k the stream-1 uniform of
+ * counter (0, b, k, offset); the first rejected position k* draws a correction
+ * from norm(max(0, p_t[k*] - p_d[k*])); if all L_b tested tokens are accepted
+ * a bonus token is drawn from p_t[b, L_b].  The draw is an inverse CDF over
+ * q_v = floor(w_v * 2^40) with t = floor(R * Q / 2^64), R the stream-2 word
+ * pair of counter (0, b, position, offset), Q = sum q_v; the token is the
+ * smallest v whose inclusive prefix sum exceeds t.  A residual with no mass
+ * falls back to p_t[k*]; a p_t row with no mass gives argmax p_t and sets
+ * NUMERIC.
+ *
+ *   p_target     [B, gamma+1, V] fp32 probabilities, device
+ *   p_draft      [B, gamma, V]   fp32 probabilities, device
+ *   draft_tokens [B, gamma] int32, device, each in [0, V)
+ *   lengths      [B] int32 in [0, gamma], device, or NULL (= gamma): the
+ *                scheduler's per-request verify length
+ *   out_tokens   [B, gamma+1] int32 output: accepted prefix, then the
+ *                correction or bonus token, then -1
+ *   num_accepted [B] int32 output
+ * Requirements: B >= 1, 1 <= gamma <= 65535, 1 <= V <= 2^24 (keeps Q < 2^64),
+ * offset < 2^32; p_target/p_draft 16-byte aligned.
+ * Device-side: a token or length out of range sets INPUT_RANGE (the request
+ * outputs num_accepted 0 and -1 tokens).
+ * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY, ...) bytes.
+ */
+DSPARK_API dspark_status dspark_verify(const float* p_target, const float* p_draft,
+                            const int32_t* draft_tokens, const int32_t* lengths,
+                            uint64_t seed, uint64_t offset, int B, int gamma, int V,
+                            int32_t* out_tokens, int32_t* num_accepted,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Confidence-scheduled admission of draft tokens for the next verify batch.
+ *
+ * "Speculative decoding: from zero to DSpark" §6 and §7:
+ *   survival[b, 0] = c[b, 0],  survival[b, k] = fl32(survival[b, k-1] * c[b, k])
+ *   candidates (b, k) sorted by survival descending, ties by b*N+k ascending
+ *   (a stable device radix sort of all B*N candidates);
+ *   if K_in < 0: K = smallest argmax over K in [1, min(B*N, S)] of
+ *       f(K) = float64(B * 2^32 + sum_{j<K} floor(s_(j) * 2^32)) * sps[K-1]
+ *     (expected tokens of the batch in 32.32 fixed point, times the
+ *      steps-per-second table at batch size K; every K is evaluated);
+ *   else K = min(K_in, B*N) (capacity fixed ahead of time, §7).
+ *   The top K candidates are admitted; lengths[b] counts request b's admitted
+ *   candidates, which are always a prefix 0..lengths[b]-1.  The call reads no
+ *   token values, so admission of token k never depends on token k's value.
+ *
+ *   cond_accept [B, N] fp32 in [0, 1], device (values outside are clamped,
+ *               NaN read as 0, and INPUT_RANGE is set)
+ *   sps         [S] fp64, device, or NULL when K_in >= 0
+ *   survival    [B, N] fp32 output
+ *   K_out       [1] int32 output
+ *   lengths     [B] int32 output
+ *   selected    [B*N] int32 output: flat index b*N+k of the admitted
+ *               candidates in rank order, then -1
+ * Requirements: B, N >= 1, B*N <= 2^20, S >= 1 when K_in < 0.
+ * workspace: >= dspark_workspace_size(DSPARK_OP_SCHEDULE, B, N, 0, 0) bytes.
+ */
+DSPARK_API dspark_status dspark_schedule(const float* cond_accept, const double* sps, int S,
+                              int B, int N, int K_in,
+                              float* survival, int32_t* K_out, int32_t* lengths,
+                              int32_t* selected,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, reads the status word of `workspace` written by the
+ * last call that used it, stores the raw DSPARK_STATUS_* bits in *bits (if
+ * bits != NULL) and returns the most severe matching dspark_status
+ * (TIMEOUT > NUMERIC > INPUT_RANGE > OK; INTERNAL maps to DSPARK_ERR_CUDA).
+ * For tests and debugging: it blocks the host.
+ */
+DSPARK_API dspark_status dspark_read_status(const void* workspace, uint32_t* bits, void* stream);
+
+/* Static description of a status code. */
+DSPARK_API const char* dspark_status_string(dspark_status s);
+
+/* Text of the last host-side error of the calling thread ("" if none). */
+DSPARK_API const char* dspark_last_error(void);
+
+/*
+ * Self-test of the bounded device-side wait used by every kernel: launches
+ * one block that waits on a flag in `workspace` that nothing sets, for at most
+ * timeout_ns nanoseconds (1e3 .. 1e10), then records DSPARK_STATUS_TIMEOUT in
+ * the workspace status word and returns.  Lets a test show that a wait that
+ * runs out ends with an error status and leaves the context usable.
+ * workspace: >= 256 bytes.
+ */
+DSPARK_API dspark_status dspark_selftest_wait_timeout(void* workspace, size_t ws_bytes,
+                                           long long timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

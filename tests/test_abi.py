@@ -1,0 +1,67 @@
+"""The C-ABI library builds, loads and exports every entry point declared in
+include/dspark.h; host-side validation rejects bad arguments before any CUDA call
+(runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from draft_sampling_verification_tcgen05_gb300 import _build
+    _build.build()
+    import draft_sampling_verification_tcgen05_gb300 as ds
+    return ds.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "dspark.h")).read()
+    return re.findall(r"DSPARK_API\s+[\w\s\*]+?\b(dspark_\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule"):
+        assert op in names
+
+
+def test_workspace_sizes(L):
+    assert L.dspark_workspace_size(0, 0, 0, 0, 0) == 256
+    assert L.dspark_workspace_size(2, 256, 8, 151936, 0) == 256
+    m = L.dspark_workspace_size(1, 64, 16, 151936, 256)
+    assert m >= 256 + 64 * 16 * 12
+    assert L.dspark_workspace_size(3, 1024, 16, 0, 0) == 256 + 2 * 8 * 1024 * 16
+    assert L.dspark_workspace_size(9, 1, 1, 1, 1) == 0
+
+
+def test_host_validation_without_gpu(L):
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(4096)        # never dereferenced: validation fails first
+    assert L.dspark_draft_logits(null, fake, 1, 8, 64, 100, fake, fake, 256, null) == 1
+    assert L.dspark_draft_logits(fake, fake, 1, 8, 60, 100, fake, fake, 256, null) == 1   # H*2 % 16
+    assert L.dspark_draft_logits(fake, fake, 7, 8, 64, 100, fake, fake, 256, null) == 1   # dtype
+    assert L.dspark_draft_logits(fake, fake, 1, 8, 64, 100, fake, fake, 16, null) == 1    # workspace
+    assert L.dspark_markov_sample(fake, fake, fake, fake, 1, fake, 0, 2 ** 32, 1, 8, 100, 64,
+                                  fake, null, fake, 1 << 20, null) == 1                   # offset
+    assert L.dspark_markov_sample(fake, fake, fake, fake, 1, fake, 0, 0, 1, 0, 100, 64,
+                                  fake, null, fake, 1 << 20, null) == 1                   # N = 0
+    assert L.dspark_verify(fake, fake, fake, null, 0, 0, 1, 0, 10, fake, fake, fake, 256, null) == 1
+    assert L.dspark_schedule(fake, null, 0, 4, 4, -1, fake, fake, fake, fake, fake, 1024, null) == 1
+    assert L.dspark_schedule(fake, null, 0, 2048, 1024, 5, fake, fake, fake, fake, fake, 1 << 30, null) == 1
+    assert b"SPS" in L.dspark_last_error() or len(L.dspark_last_error()) > 0
+    assert L.dspark_status_string(4) == b"device wait timed out"
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import draft_sampling_verification_tcgen05_gb300 as ds
+    monkeypatch.setattr(ds, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(ds, "_lib", None)
+    with pytest.raises(RuntimeError):
+        ds.lib()
