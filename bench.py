@@ -40,8 +40,8 @@ WORKLOAD_TEMPERATURE = {"qwen3_8b_single": 1.0, "batched_draft": 0.8, "tiny": 1.
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="qwen3_8b_single", choices=sorted(DRAFT_CONFIGS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--skip-e2e", action="store_true")
@@ -100,7 +100,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -113,7 +116,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "window", (-1e30, 1e30))
+        inside = [ln for t, ln in self.lines if t0 - 0.25 <= t <= t1 + 0.25]
+        for ln in inside or [ln for _, ln in self.lines]:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -128,7 +133,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_timed_region": len(inside)}
 
 
 # ---------------------------------------------------------------------------
@@ -213,12 +218,16 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.5)                           # let the sampler start before the timed region
         wall0 = time.perf_counter()
         for k in range(args.steps):
             flush.fill_(float(k))                 # L2 flush between timed steps (not timed)
             step(k)
         torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
+        wall1 = time.perf_counter()
+        wall = wall1 - wall0
+        clk.mark(wall0, wall1)
+        time.sleep(0.3)
     if dist is not None:
         dist.barrier()
     per = np.array([[ev[k][j].elapsed_time(ev[k][j + 1]) for j in range(4)] for k in range(args.steps)])
