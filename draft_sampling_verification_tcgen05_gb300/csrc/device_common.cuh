@@ -88,6 +88,43 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* ws, uint32_t phase, long 
     return s_ok != 0;
 }
 
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// Grid barrier among a subset of every block's threads: the `nthreads`
+// participants of named barrier `bar_id` (a multiple of 32), of which exactly
+// one has `leader` set.  Same bounded spin and abort rules as grid_barrier.
+__device__ __forceinline__ bool grid_barrier_named(WsHeader* ws, uint32_t phase, long long timeout_ns,
+                                                   uint32_t where, uint32_t bar_id, uint32_t nthreads,
+                                                   bool leader, volatile int* s_ok) {
+    named_bar_sync(bar_id, nthreads);
+    if (leader) {
+        int ok = 1;
+        const uint32_t target = (phase + 1u) * gridDim.x;
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(&ws->barrier) : "memory");
+        const long long t0 = global_ns();
+        uint32_t spins = 0;
+        while (ld_acquire_u32(&ws->barrier) < target) {
+            if ((++spins & 63u) == 0) {
+                if (aborted(ws)) { ok = 0; break; }
+                if (global_ns() - t0 > timeout_ns) {
+                    atomicOr(&ws->status, DSPARK_STATUS_TIMEOUT);
+                    atomicExch(&ws->detail, where);
+                    ok = 0;
+                    break;
+                }
+            }
+            __nanosleep(32);
+        }
+        __threadfence();
+        *s_ok = ok;
+    }
+    named_bar_sync(bar_id, nthreads);
+    return *s_ok != 0;
+}
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
 // as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplications on counter

@@ -1,0 +1,100 @@
+// Shared pieces of the two Markov-sampler kernels (CUDA-core and tensor-core
+// paths): workspace layout, arguments, Gumbel variate of an element, step
+// slots and the log-sum-exp partials.
+#pragma once
+
+#include "device_common.cuh"
+#include "host_common.h"
+
+namespace dspark {
+namespace markov {
+
+constexpr int kMaxGrid = 1024;                         // workspace is sized for this many blocks
+constexpr uint32_t kWaitStep = 0x200;                  // + step index (grid barrier)
+
+struct MarkovLayout {
+    unsigned long long* slots;   // [N][B] argmax keys
+    uint32_t* lb;                // [N][B] order bits of the published lower bound
+    float2* lse_part;            // [2][kMaxGrid][B] (max, sum) partials
+};
+
+__host__ __device__ inline MarkovLayout markov_layout(void* ws, int B, int N) {
+    uint8_t* p = static_cast<uint8_t*>(ws) + sizeof(WsHeader);
+    MarkovLayout L;
+    L.slots = reinterpret_cast<unsigned long long*>(p);
+    p += sizeof(unsigned long long) * static_cast<size_t>(N) * B;
+    L.lb = reinterpret_cast<uint32_t*>(p);
+    p += sizeof(uint32_t) * static_cast<size_t>(N) * B;
+    p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15));
+    L.lse_part = reinterpret_cast<float2*>(p);
+    return L;
+}
+
+struct MarkovArgs {
+    const float* base;          // [B, N, V]
+    const int32_t* anchor;      // [B]
+    const void* w1;             // [V, r]
+    const void* w2;             // [V, r]
+    const float* temperature;   // [B]
+    int32_t* tokens;            // [B, N]
+    float* lse;                 // [B, N] or null
+    WsHeader* ws;
+    MarkovLayout lay;
+    uint64_t seed;
+    uint32_t offset;
+    int B, N, V, r;
+    int slice;                  // vocabulary entries per block
+    int w2_cached;              // w2 slice lives in shared memory
+    int w2_pitch;               // bytes per cached w2 row (padded)
+    int z_stored;               // z rows live in shared memory
+    long long timeout_ns;
+};
+
+__device__ __forceinline__ float gumbel_at(const MarkovArgs& a, int b, int i, int v) {
+    const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(b),
+                              kStreamGumbel, static_cast<uint32_t>(i));
+    const uint32_t sel = static_cast<uint32_t>(v) & 3u;
+    const uint32_t word = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
+    return gumbel_from_word(word);
+}
+
+__device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
+    if (a.y == 0.f) return b;
+    if (b.y == 0.f) return a;
+    const float m = fmaxf(a.x, b.x);
+    return make_float2(m, a.y * __expf(a.x - m) + b.y * __expf(b.x - m));
+}
+
+// Reads a token from a step slot; key 0 means no finite candidate existed.
+__device__ __forceinline__ int slot_token(const MarkovArgs& a, int i, int b) {
+    const unsigned long long k = __ldcg(a.lay.slots + static_cast<size_t>(i) * a.B + b);
+    if (k == 0ull) {
+        set_status(a.ws, DSPARK_STATUS_NUMERIC);
+        return 0;
+    }
+    return static_cast<int>(key_index(k));
+}
+
+// Combine the lse partials of step i for the requests this block finalises.
+// `tid`/`nthreads`: this thread's index among the block's participating threads.
+__device__ inline void finish_lse(const MarkovArgs& a, int i, int tid, int nthreads) {
+    if (a.lse == nullptr) return;
+    const float2* part = a.lay.lse_part + static_cast<size_t>(i & 1) * kMaxGrid * a.B;
+    for (int b = blockIdx.x * nthreads + tid; b < a.B; b += gridDim.x * nthreads) {
+        float2 m = make_float2(0.f, 0.f);
+        for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
+            const float2 p = __ldcg(part + static_cast<size_t>(c) * a.B + b);
+            m = lse_merge(m, p);
+        }
+        a.lse[static_cast<size_t>(b) * a.N + i] = m.y > 0.f ? m.x + logf(m.y) : -INFINITY;
+    }
+}
+
+}  // namespace markov
+
+// Tensor-core path (csrc/markov_tc.cu): bf16 Markov head, 16 <= B <= 256.
+bool markov_tc_eligible(int B, int N, int V, int r, dspark_dtype wdtype, const float* base, const float* lse,
+                        int sm_count);
+dspark_status launch_markov_tc(const markov::MarkovArgs& a, cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace dspark

@@ -24,57 +24,22 @@
 // strictly below the bound, which is itself a value some element reaches.
 #include "device_common.cuh"
 #include "host_common.h"
+#include "markov_common.cuh"
 
 #include <algorithm>
 
 namespace dspark {
 namespace {
 
+using namespace markov;
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxGrid = 1024;                         // workspace is sized for this many blocks
 constexpr size_t kW2CacheBytes = 144 * 1024;           // w2 slice kept in shared memory when it fits
 constexpr size_t kZStoreBytes = 32 * 1024;             // z rows kept in shared memory when they fit
 constexpr int kMaxEFloats = 16384;                     // B * r limit of the shared E matrix
-constexpr uint32_t kWaitStep = 0x200;                  // + step index
 
-struct MarkovLayout {
-    unsigned long long* slots;   // [N][B] argmax keys
-    uint32_t* lb;                // [N][B] order bits of the published lower bound
-    float2* lse_part;            // [2][kMaxGrid][B] (max, sum) partials
-};
 
-__host__ __device__ inline MarkovLayout markov_layout(void* ws, int B, int N) {
-    uint8_t* p = static_cast<uint8_t*>(ws) + sizeof(WsHeader);
-    MarkovLayout L;
-    L.slots = reinterpret_cast<unsigned long long*>(p);
-    p += sizeof(unsigned long long) * static_cast<size_t>(N) * B;
-    L.lb = reinterpret_cast<uint32_t*>(p);
-    p += sizeof(uint32_t) * static_cast<size_t>(N) * B;
-    p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15));
-    L.lse_part = reinterpret_cast<float2*>(p);
-    return L;
-}
-
-struct MarkovArgs {
-    const float* base;          // [B, N, V]
-    const int32_t* anchor;      // [B]
-    const void* w1;             // [V, r]
-    const void* w2;             // [V, r]
-    const float* temperature;   // [B]
-    int32_t* tokens;            // [B, N]
-    float* lse;                 // [B, N] or null
-    WsHeader* ws;
-    MarkovLayout lay;
-    uint64_t seed;
-    uint32_t offset;
-    int B, N, V, r;
-    int slice;                  // vocabulary entries per block
-    int w2_cached;              // w2 slice lives in shared memory
-    int w2_pitch;               // bytes per cached w2 row (padded)
-    int z_stored;               // z rows live in shared memory
-    long long timeout_ns;
-};
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
@@ -116,13 +81,6 @@ __device__ __forceinline__ float bias_dot(const uint8_t* row, const float* e, in
     return acc;
 }
 
-__device__ __forceinline__ float gumbel_at(const MarkovArgs& a, int b, int i, int v) {
-    const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(b),
-                              kStreamGumbel, static_cast<uint32_t>(i));
-    const uint32_t sel = static_cast<uint32_t>(v) & 3u;
-    const uint32_t word = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
-    return gumbel_from_word(word);
-}
 
 __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long k, unsigned long long* red) {
     k = warp_max_u64(k);
@@ -135,12 +93,6 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long k
     return m;
 }
 
-__device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {
-    if (a.y == 0.f) return b;
-    if (b.y == 0.f) return a;
-    const float m = fmaxf(a.x, b.x);
-    return make_float2(m, a.y * __expf(a.x - m) + b.y * __expf(b.x - m));
-}
 
 __device__ __forceinline__ float2 block_lse(float2 v, float2* red) {
 #pragma unroll
@@ -158,29 +110,6 @@ __device__ __forceinline__ float2 block_lse(float2 v, float2* red) {
     return m;
 }
 
-// Reads a token from a step slot; key 0 means no finite candidate existed.
-__device__ __forceinline__ int slot_token(const MarkovArgs& a, int i, int b) {
-    const unsigned long long k = __ldcg(a.lay.slots + static_cast<size_t>(i) * a.B + b);
-    if (k == 0ull) {
-        set_status(a.ws, DSPARK_STATUS_NUMERIC);
-        return 0;
-    }
-    return static_cast<int>(key_index(k));
-}
-
-// Combine the lse partials of step i for the requests this block finalises.
-__device__ void finish_lse(const MarkovArgs& a, int i) {
-    if (a.lse == nullptr) return;
-    const float2* part = a.lay.lse_part + static_cast<size_t>(i & 1) * kMaxGrid * a.B;
-    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.B; b += gridDim.x * blockDim.x) {
-        float2 m = make_float2(0.f, 0.f);
-        for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
-            const float2 p = __ldcg(part + static_cast<size_t>(c) * a.B + b);
-            m = lse_merge(m, p);
-        }
-        a.lse[static_cast<size_t>(b) * a.N + i] = m.y > 0.f ? m.x + logf(m.y) : -INFINITY;
-    }
-}
 
 template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs a) {
@@ -232,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             }
             prev[b] = p;
         }
-        if (i > 0) finish_lse(a, i - 1);
+        if (i > 0) finish_lse(a, i - 1, tid, kThreads);
         __syncthreads();
         for (int idx = tid; idx < a.B * a.r; idx += kThreads) {
             const int b = idx / a.r, k = idx % a.r;
@@ -322,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     }
     if (!alive) return;
     __threadfence();
-    finish_lse(a, a.N - 1);
+    finish_lse(a, a.N - 1, tid, kThreads);
     if (blockIdx.x == 0) {
         for (int idx = tid; idx < a.B * a.N; idx += kThreads) {
             const int b = idx / a.N, i = idx % a.N;
@@ -417,6 +346,8 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
     a.V = V;
     a.r = r;
     a.timeout_ns = kDefaultTimeoutNs;
+    if (markov_tc_eligible(B, N, V, r, wdtype, base_logits, lse, dev.sm_count))
+        return launch_markov_tc(a, stream, dev);
     if (wdtype == DSPARK_BF16) return run_generic<__nv_bfloat16>(a, stream, dev);
     return run_generic<float>(a, stream, dev);
 }

@@ -1,0 +1,470 @@
+// Tensor-core path of the sequential Markov sampler (bf16 Markov head,
+// 16 <= B <= 256 requests): the per-step bias markov_w2 . markov_w1[prev]
+// ("DSpark implementation and evaluation" §2.2, §3) is a [V, r] x [r, B]
+// product of 2*V*r*B FLOP per step -- 5 GFLOP at V=151936, r=256, B=64 --
+// which belongs on the 5th-generation tensor cores.
+//
+// One persistent cooperative kernel for all N steps.  Block c owns vocabulary
+// tiles [tile_lo, tile_hi) of 128 entries for the whole call.
+//   warp 0        one thread streams, ahead of use and across steps, the w2
+//                 tiles of the block (TMA, 128-byte swizzle, kept in L2 with
+//                 evict_last) and the base-logit tiles [16 requests x 128 v]
+//                 (3-D TMA, evict_first) into shared-memory rings
+//   warp 1        allocates tensor memory; per step one thread issues, for
+//                 every local tile, tcgen05.mma (M=128 vocab rows, N=B rounded
+//                 to 16, K=16) with A = w2 tile and B = E = w1[prev] (gathered
+//                 by the block into a swizzled shared-memory operand), into its
+//                 own TMEM columns
+//   warps 2..9    epilogue in two groups of four warps (one per TMEM lane
+//                 quadrant); group g handles request chunks g, g+2, ...:
+//                 pass 1   bias (tcgen05.ld) + base logit -> z = (base + bias)/T,
+//                          written back in place (tcgen05.st): TMEM holds the
+//                          block's whole [tiles x 128, B] slab of z for the step;
+//                          per-request argmax of z -> one real perturbed value
+//                          published as the lower bound LB (atomicMax)
+//                 pass 2   z from TMEM; Gumbel noise only where z + G_max >= LB;
+//                          block argmax -> one atomicMax per (block, request)
+//   then a grid barrier among warps 1..9; the producer keeps streaming.
+// No [B, V] row is written to device memory.
+#include "device_common.cuh"
+#include "host_common.h"
+#include "markov_common.cuh"
+
+#include <algorithm>
+
+namespace dspark {
+namespace {
+
+using namespace markov;
+
+constexpr int kGroups = 2;
+constexpr int kEpiWarps = 4 * kGroups;
+constexpr int kThreadsTC = 32 * (2 + kEpiWarps);
+constexpr uint32_t kStepThreads = 32 * (1 + kEpiWarps);
+constexpr int kW2Stages = 4;
+constexpr int kLStages = 5;                      // per epilogue group
+constexpr int kTileV = 128;
+constexpr int kChunk = 16;                       // requests per epilogue chunk
+constexpr int kMaxLocalTiles = 32;
+constexpr uint32_t kW2StageBytes = kTileV * 128;             // 128 rows x 64 bf16
+constexpr uint32_t kLStageBytes = kTileV * kChunk * 4;       // 16 requests x 128 fp32
+constexpr uint32_t kBarStep = 1;
+constexpr uint32_t kBarGroup0 = 2;
+constexpr uint32_t kWaitProducer = 0x301, kWaitMma = 0x302, kWaitEpi = 0x303;
+constexpr size_t kEMaxBytes = 64 * 1024;
+
+struct TcArgs {
+    int B_pad;            // B rounded up to 16 (MMA N)
+    int n_tiles;          // ceil(V / 128)
+    uint32_t tmem_cols;   // power of two >= max tiles per block * B_pad
+};
+
+__device__ __forceinline__ void tile_range(const TcArgs& t, int& lo, int& hi) {
+    lo = static_cast<int>((static_cast<long long>(blockIdx.x) * t.n_tiles) / gridDim.x);
+    hi = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * t.n_tiles) / gridDim.x);
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmL,
+                 MarkovArgs a, TcArgs t) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* w2s = base;
+    uint8_t* Ls = w2s + kW2Stages * kW2StageBytes;
+    uint8_t* Es = Ls + kGroups * kLStages * kLStageBytes;
+
+    __shared__ uint64_t bar_w2_full[kW2Stages], bar_w2_empty[kW2Stages];
+    __shared__ uint64_t bar_L_full[kGroups][kLStages], bar_L_empty[kGroups][kLStages];
+    __shared__ uint64_t bar_tile[kMaxLocalTiles];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_prev[256];
+    __shared__ float s_invT[256];
+    __shared__ float s_lb[kGroups][kChunk];
+    __shared__ unsigned long long s_part[kGroups][4][kChunk];
+    __shared__ int s_ok;
+
+    const uint32_t warp = warp_id(), lane = lane_id();
+    const int Bp = t.B_pad;
+    const int n_chunks = Bp / kChunk;
+    const int rounds = (n_chunks + kGroups - 1) / kGroups;
+    const int kblocks = a.r / 64;
+    const uint32_t e_kb_bytes = static_cast<uint32_t>(Bp) * 128u;
+    int tile_lo, tile_hi;
+    tile_range(t, tile_lo, tile_hi);
+    const int nt = tile_hi - tile_lo;
+
+    // ---------------- set-up ----------------
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kW2Stages; ++s) {
+            mbar_init(&bar_w2_full[s], 1);
+            mbar_init(&bar_w2_empty[s], 1);
+        }
+        for (int g = 0; g < kGroups; ++g)
+            for (int s = 0; s < kLStages; ++s) {
+                mbar_init(&bar_L_full[g][s], 1);
+                mbar_init(&bar_L_empty[g][s], 128);
+            }
+        for (int i = 0; i < kMaxLocalTiles; ++i) mbar_init(&bar_tile[i], 1);
+        fence_mbarrier_init();
+        prefetch_tensormap(&tmW2);
+        prefetch_tensormap(&tmL);
+    }
+    bool bad_t = false;
+    for (int b = threadIdx.x; b < 256; b += kThreadsTC) {
+        float inv = 0.f;
+        if (b < a.B) {
+            float T = a.temperature[b];
+            if (!(T >= 0.f) || isinf(T)) {
+                bad_t = true;
+                T = 0.f;
+            }
+            inv = T > 0.f ? __frcp_rn(T) : 0.f;          // 0 marks a greedy request
+        }
+        s_invT[b] = inv;
+    }
+    if (bad_t) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+    {   // zero E once: padding rows (b >= B) stay zero for the whole call
+        uint4* e4 = reinterpret_cast<uint4*>(Es);
+        const int n16 = Bp * a.r * 2 / 16;
+        for (int k = threadIdx.x; k < n16; k += kThreadsTC) e4[k] = make_uint4(0, 0, 0, 0);
+    }
+    if (warp == 1) {
+        tmem_alloc(&s_tmem, t.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer: w2 and base-logit tiles for every step ----------------
+            const uint64_t pol_keep = l2_policy_evict_last();
+            const uint64_t pol_stream = l2_policy_evict_first();
+            int ws = 0, ls[kGroups];
+            uint32_t wph = 0, lph[kGroups];
+            for (int g = 0; g < kGroups; ++g) { ls[g] = 0; lph[g] = 0; }
+            bool ok = true;
+            for (int i = 0; i < a.N && ok; ++i) {
+                for (int ro = 0; ro < rounds && ok; ++ro) {
+                    for (int tl = 0; tl < nt && ok; ++tl) {
+                        const int v0 = (tile_lo + tl) * kTileV;
+                        if (ro == 0) {
+                            for (int kb = 0; kb < kblocks; ++kb) {
+                                if (!mbar_wait(&bar_w2_empty[ws], wph ^ 1u, a.ws, a.timeout_ns, kWaitProducer)) {
+                                    ok = false;
+                                    break;
+                                }
+                                mbar_arrive_expect_tx(&bar_w2_full[ws], kW2StageBytes);
+                                tma_load_2d(w2s + ws * kW2StageBytes, &tmW2, kb * 64, v0, &bar_w2_full[ws], pol_keep);
+                                if (++ws == kW2Stages) { ws = 0; wph ^= 1u; }
+                            }
+                        }
+                        for (int g = 0; g < kGroups && ok; ++g) {
+                            const int c = ro * kGroups + g;
+                            if (c >= n_chunks) continue;
+                            if (!mbar_wait(&bar_L_empty[g][ls[g]], lph[g] ^ 1u, a.ws, a.timeout_ns, kWaitProducer)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&bar_L_full[g][ls[g]], kLStageBytes);
+                            tma_load_3d(Ls + (g * kLStages + ls[g]) * kLStageBytes, &tmL, v0, i, c * kChunk,
+                                        &bar_L_full[g][ls[g]], pol_stream);
+                            if (++ls[g] == kLStages) { ls[g] = 0; lph[g] ^= 1u; }
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the block exits: stages before the
+                // ring position were last filled in the current phase, the rest one phase
+                // earlier (or never, which reads as complete)
+                const long long t0 = global_ns();
+                for (int s = 0; s < kW2Stages; ++s)
+                    while (!mbar_try_wait(&bar_w2_full[s], s < ws ? wph : (wph ^ 1u)) &&
+                           global_ns() - t0 < a.timeout_ns) {
+                    }
+                for (int g = 0; g < kGroups; ++g)
+                    for (int s = 0; s < kLStages; ++s)
+                        while (!mbar_try_wait(&bar_L_full[g][s], s < ls[g] ? lph[g] : (lph[g] ^ 1u)) &&
+                               global_ns() - t0 < a.timeout_ns) {
+                        }
+            }
+        }
+    } else {
+        // ---------------- MMA warp + epilogue warps: the N sequential steps ----------------
+        const int stid = static_cast<int>(threadIdx.x) - 32;
+        const bool is_mma = warp == 1;
+        const int epi = static_cast<int>(warp) - 2;
+        const int grp = epi >= 0 ? epi / 4 : 0;
+        const uint32_t quad = warp & 3u;
+        const bool grp_lead = epi >= 0 && (epi % 4) == 0;
+        int w2st = 0, lsg = 0;
+        uint32_t w2ph = 0, lphg = 0;
+        bool alive = true, dead = false, nan_seen = false;
+        const uint32_t idesc = mma_idesc(128, Bp, false);
+        const int chunks16 = a.r / 8;                         // 16-byte pieces of a w1 row
+
+        for (int i = 0; i < a.N && alive; ++i) {
+            // ---- previous tokens, then E = w1[prev] in the swizzled K-major operand layout ----
+            for (int b = stid; b < a.B; b += kStepThreads) {
+                int p;
+                if (i == 0) {
+                    p = a.anchor[b];
+                    if (p < 0 || p >= a.V) {
+                        set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+                        p = 0;
+                    }
+                } else {
+                    p = slot_token(a, i - 1, b);
+                }
+                s_prev[b] = p;
+            }
+            named_bar_sync(kBarStep, kStepThreads);
+            for (int idx = stid; idx < a.B * chunks16; idx += kStepThreads) {
+                const int b = idx / chunks16, c16 = idx % chunks16;
+                const int kb = c16 >> 3, cc = c16 & 7;
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                    static_cast<const uint8_t*>(a.w1) + (static_cast<size_t>(s_prev[b]) * a.r + c16 * 8) * 2));
+                uint8_t* dst = Es + kb * e_kb_bytes + (b >> 3) * 1024 + (b & 7) * 128 + ((cc ^ (b & 7)) << 4);
+                *reinterpret_cast<uint4*>(dst) = v;
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(kBarStep, kStepThreads);
+
+            if (is_mma) {
+                // ---- bias for every local tile: D[tile] = w2_tile (128 x r) . E^T (r x Bp) ----
+                if (lane == 0 && !dead) {
+                    tc_fence_after();
+                    for (int tl = 0; tl < nt && !dead; ++tl) {
+                        const uint32_t d = tmem + static_cast<uint32_t>(tl * Bp);
+                        for (int kb = 0; kb < kblocks; ++kb) {
+                            if (!mbar_wait(&bar_w2_full[w2st], w2ph, a.ws, a.timeout_ns, kWaitMma)) {
+                                dead = true;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t a_addr = smem_u32(w2s + w2st * kW2StageBytes);
+                            const uint32_t b_addr = smem_u32(Es + kb * e_kb_bytes);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_issue<false>(d, sw128_kmajor_desc(a_addr + 32 * k),
+                                                 sw128_kmajor_desc(b_addr + 32 * k), idesc, (kb | k) != 0 ? 1u : 0u);
+                            mma_commit(&bar_w2_empty[w2st]);
+                            if (++w2st == kW2Stages) { w2st = 0; w2ph ^= 1u; }
+                        }
+                        if (!dead) mma_commit(&bar_tile[tl]);
+                    }
+                }
+                __syncwarp();
+            } else {
+                unsigned long long* slot = a.lay.slots + static_cast<size_t>(i) * a.B;
+                uint32_t* lbs = a.lay.lb + static_cast<size_t>(i) * a.B;
+                for (int ro = 0; ro < rounds; ++ro) {
+                    const int c = ro * kGroups + grp;
+                    if (c >= n_chunks) continue;                       // uniform over the group
+                    // ---- pass 1: z = (base + bias) / T into TMEM, argmax of z ----
+                    float bz[kChunk];
+                    int bv[kChunk];
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) { bz[j] = -INFINITY; bv[j] = -1; }
+                    for (int tl = 0; tl < nt; ++tl) {
+                        const int v = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32 + lane);
+                        bool okw = !dead;
+                        if (okw) okw = mbar_wait(&bar_tile[tl], static_cast<uint32_t>(i & 1), a.ws, a.timeout_ns, kWaitEpi);
+                        if (okw) okw = mbar_wait(&bar_L_full[grp][lsg], lphg, a.ws, a.timeout_ns, kWaitEpi);
+                        dead = !__all_sync(0xFFFFFFFFu, okw);
+                        if (!dead) {
+                            tc_fence_after();
+                            const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
+                            uint32_t r[kChunk];
+                            tmem_ld16(taddr, r);
+                            tmem_wait_ld();
+                            const float* Lt = reinterpret_cast<const float*>(Ls + (grp * kLStages + lsg) * kLStageBytes);
+#pragma unroll
+                            for (int j = 0; j < kChunk; ++j) {
+                                const float s = __fadd_rn(Lt[j * kTileV + quad * 32 + lane], __uint_as_float(r[j]));
+                                const float inv = s_invT[c * kChunk + j];
+                                const float z = inv > 0.f ? __fmul_rn(s, inv) : s;
+                                r[j] = __float_as_uint(z);
+                                if (z != z) nan_seen = true;
+                                if (v < a.V && z > bz[j]) { bz[j] = z; bv[j] = v; }
+                            }
+                            tmem_st16(taddr, r);
+                        }
+                        mbar_arrive(&bar_L_empty[grp][lsg]);
+                        if (++lsg == kLStages) { lsg = 0; lphg ^= 1u; }
+                    }
+                    if (!dead) tmem_wait_st();
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        const unsigned long long k = warp_max_u64(bv[j] >= 0 ? argmax_key(bz[j], static_cast<uint32_t>(bv[j])) : 0ull);
+                        if (lane == 0) s_part[grp][quad][j] = k;
+                    }
+                    named_bar_sync(kBarGroup0 + grp, 128);
+                    if (grp_lead && lane < kChunk) {
+                        const int b = c * kChunk + static_cast<int>(lane);
+                        unsigned long long k = 0;
+                        for (int q = 0; q < 4; ++q) k = s_part[grp][q][lane] > k ? s_part[grp][q][lane] : k;
+                        float lbv = INFINITY;                          // nothing to sample
+                        if (b < a.B && k != 0ull) {
+                            const uint32_t vb = key_index(k);
+                            if (s_invT[b] > 0.f) {
+                                const float zb = float_from_order_bits(static_cast<uint32_t>(k >> 32));
+                                const float y = __fadd_rn(zb, gumbel_at(a, b, i, static_cast<int>(vb)));
+                                atomicMax(lbs + b, float_order_bits(y));
+                                atomicMax(slot + b, argmax_key(y, vb));
+                                lbv = float_from_order_bits(__ldcg(lbs + b));
+                            } else {
+                                atomicMax(slot + b, k);                 // greedy: argmax of z is the token
+                            }
+                        }
+                        s_lb[grp][lane] = lbv;
+                    }
+                    named_bar_sync(kBarGroup0 + grp, 128);
+                    // ---- pass 2: Gumbel noise only where z can still beat the bound ----
+                    float lb[kChunk], by[kChunk];
+                    int bv2[kChunk];
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) { lb[j] = s_lb[grp][j]; by[j] = -INFINITY; bv2[j] = -1; }
+                    bool any = false;
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) any |= lb[j] < INFINITY;
+                    if (any && !dead) {
+                        for (int tl = 0; tl < nt; ++tl) {
+                            const int v = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32 + lane);
+                            const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
+                            uint32_t r[kChunk];
+                            tmem_ld16(taddr, r);
+                            tmem_wait_ld();
+                            if (v < a.V) {
+#pragma unroll
+                                for (int j = 0; j < kChunk; ++j) {
+                                    const float z = __uint_as_float(r[j]);
+                                    if (__fadd_rn(z, kGumbelMax) >= lb[j]) {
+                                        const float y = __fadd_rn(z, gumbel_at(a, c * kChunk + j, i, v));
+                                        if (y > by[j]) { by[j] = y; bv2[j] = v; }
+                                    }
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        const unsigned long long k = warp_max_u64(bv2[j] >= 0 ? argmax_key(by[j], static_cast<uint32_t>(bv2[j])) : 0ull);
+                        if (lane == 0) s_part[grp][quad][j] = k;
+                    }
+                    named_bar_sync(kBarGroup0 + grp, 128);
+                    if (grp_lead && lane < kChunk) {
+                        const int b = c * kChunk + static_cast<int>(lane);
+                        unsigned long long k = 0;
+                        for (int q = 0; q < 4; ++q) k = s_part[grp][q][lane] > k ? s_part[grp][q][lane] : k;
+                        if (b < a.B && k != 0ull) atomicMax(slot + b, k);
+                    }
+                    named_bar_sync(kBarGroup0 + grp, 128);
+                }
+            }
+            // ---- every block agrees on the step's winners ----
+            tc_fence_before();
+            alive = grid_barrier_named(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i, kBarStep,
+                                       kStepThreads, threadIdx.x == 32, &s_ok);
+            tc_fence_after();
+        }
+        if (nan_seen) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+        if (alive && blockIdx.x == 0) {
+            for (int idx = stid; idx < a.B * a.N; idx += kStepThreads) {
+                const int b = idx / a.N, i = idx % a.N;
+                a.tokens[idx] = slot_token(a, i, b);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, t.tmem_cols);
+    }
+}
+
+size_t tc_smem_bytes(int B_pad, int r) {
+    return 1024 + kW2Stages * kW2StageBytes + kGroups * kLStages * kLStageBytes +
+           static_cast<size_t>(B_pad) * r * 2;
+}
+
+}  // namespace
+
+bool markov_tc_eligible(int B, int N, int V, int r, dspark_dtype wdtype, const float* base, const float* lse,
+                        int sm_count) {
+    if (wdtype != DSPARK_BF16 || lse != nullptr) return false;
+    if (B < 16 || B > 256 || r % 64 != 0 || r > 256 || V % 4 != 0 || V < kTileV) return false;
+    if (N > 65535 || !aligned(base, 16)) return false;
+    const int B_pad = (B + 15) & ~15;
+    if (static_cast<size_t>(B_pad) * r * 2 > kEMaxBytes) return false;
+    const int n_tiles = (V + kTileV - 1) / kTileV;
+    const int grid = std::min(sm_count, n_tiles);
+    const int max_local = (n_tiles + grid - 1) / grid;
+    return max_local <= kMaxLocalTiles && max_local * B_pad <= 512;
+}
+
+dspark_status launch_markov_tc(const MarkovArgs& a, cudaStream_t stream, const DeviceInfo& dev) {
+    TcArgs t;
+    t.B_pad = (a.B + 15) & ~15;
+    t.n_tiles = (a.V + kTileV - 1) / kTileV;
+    const int grid = std::min(dev.sm_count, t.n_tiles);
+    const int max_local = (t.n_tiles + grid - 1) / grid;
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(max_local * t.B_pad)) cols *= 2;
+    t.tmem_cols = cols;
+
+    CUtensorMap tmW2, tmL;
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.r), static_cast<uint64_t>(a.V)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.r) * 2};
+        const uint32_t box[2] = {64, static_cast<uint32_t>(kTileV)};
+        if (!make_tensor_map(&tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.w2, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+            return DSPARK_ERR_UNSUPPORTED;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(a.V), static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.B)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(a.V) * 4, static_cast<uint64_t>(a.N) * a.V * 4};
+        const uint32_t box[3] = {static_cast<uint32_t>(kTileV), 1, static_cast<uint32_t>(kChunk)};
+        if (!make_tensor_map(&tmL, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.base, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            return DSPARK_ERR_UNSUPPORTED;
+    }
+    const size_t smem = tc_smem_bytes(t.B_pad, a.r);
+    if (smem > dev.smem_optin) {
+        set_error("markov_sample (tensor path): needs %zu bytes of shared memory", smem);
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    cudaError_t e = cudaFuncSetAttribute(markov_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(markov_tc)");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, markov_tc_kernel, kThreadsTC, smem);
+    if (e != cudaSuccess) return cuda_error(e, "occupancy(markov_tc)");
+    if (per_sm < 1 || per_sm * dev.sm_count < grid) {
+        set_error("markov_sample (tensor path): %d blocks cannot be co-resident", grid);
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, markov_tc_kernel, tmW2, tmL, a, t);
+    if (e != cudaSuccess) return cuda_error(e, "launch(markov_tc)");
+    return DSPARK_OK;
+}
+
+}  // namespace dspark
