@@ -183,7 +183,7 @@ def run_gpu(args):
     sel = torch.empty(B * N, dtype=torch.int32, device=dev)
     ws_g = ds.Workspace(ds.OP_DRAFT_LOGITS, device=dev)
     ws_m = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
-    ws_v = ds.Workspace(ds.OP_VERIFY, device=dev)
+    ws_v = ds.Workspace(ds.OP_VERIFY, B, N, V, device=dev)
     ws_s = ds.Workspace(ds.OP_SCHEDULE, B, N, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)

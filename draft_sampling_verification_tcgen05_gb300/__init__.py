@@ -190,7 +190,7 @@ def dspark_verify(p_target, p_draft, draft_tokens, lengths, seed: int, offset: i
         out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=p_target.device)
     if num_accepted is None:
         num_accepted = torch.empty(B, dtype=torch.int32, device=p_target.device)
-    ws = _ws(workspace, OP_VERIFY, device=p_target.device)
+    ws = _ws(workspace, OP_VERIFY, B, gamma, V, 0, p_target.device)
     _check(lib().dspark_verify(_ptr(p_target), _ptr(p_draft), _ptr(draft_tokens), _ptr(lengths),
                                seed, offset, B, gamma, V, _ptr(out_tokens), _ptr(num_accepted),
                                ws.ptr, ws.nbytes, _stream(stream)), "dspark_verify")

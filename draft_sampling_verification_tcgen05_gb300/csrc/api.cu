@@ -161,13 +161,13 @@ bool bad_ws(const void* ws, size_t ws_bytes, size_t need) {
 extern "C" {
 
 size_t dspark_workspace_size(int op, int B, int N, int V, int r) {
-    (void)V;
     (void)r;
     if (B < 0 || N < 0) return 0;
     switch (op) {
         case DSPARK_OP_DRAFT_LOGITS:
-        case DSPARK_OP_VERIFY:
             return sizeof(WsHeader);
+        case DSPARK_OP_VERIFY:
+            return V < 0 ? 0 : verify_workspace_bytes(B, V);
         case DSPARK_OP_MARKOV_SAMPLE:
             return markov_workspace_bytes(B, N);
         case DSPARK_OP_SCHEDULE:

@@ -51,6 +51,7 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
                                    int32_t* draft_tokens, float* lse, void* ws,
                                    cudaStream_t stream, const DeviceInfo& dev);
 
+size_t verify_workspace_bytes(int B, int V);
 dspark_status launch_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,
                             const int32_t* lengths, uint64_t seed, uint32_t offset, int B, int gamma,
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,

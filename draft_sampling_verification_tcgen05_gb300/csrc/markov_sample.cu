@@ -138,11 +138,14 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         // load this block's w2 rows once; rows padded to w2_pitch bytes
         const uint8_t* src = static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v_lo) * row_bytes;
         const int chunks = static_cast<int>(row_bytes / 16);
+        // asynchronous 16-byte copies (many in flight); completed before step 0's first pass
         for (int idx = tid; idx < n_local * chunks; idx += kThreads) {
             const int v = idx / chunks, c = idx % chunks;
-            *reinterpret_cast<uint4*>(w2s + static_cast<size_t>(v) * a.w2_pitch + 16 * c) =
-                __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(v) * row_bytes + 16 * c));
+            const uint32_t dst = smem_u32(w2s + static_cast<size_t>(v) * a.w2_pitch + 16 * c);
+            const uint8_t* g = src + static_cast<size_t>(v) * row_bytes + 16 * c;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(g) : "memory");
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
 
     bool alive = true;
@@ -167,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             const int b = idx / a.r, k = idx % a.r;
             E[idx] = to_f<WT>(static_cast<const WT*>(a.w1)[static_cast<size_t>(prev[b]) * a.r + k]);
         }
+        if (i == 0 && a.w2_cached) asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
 
         unsigned long long* slot = a.lay.slots + static_cast<size_t>(i) * a.B;

@@ -64,6 +64,15 @@ __device__ __forceinline__ void tile_range(const TcArgs& t, int& lo, int& hi) {
     hi = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * t.n_tiles) / gridDim.x);
 }
 
+// One queued candidate: request c*16 + j, vocabulary entry v, scaled logit z.
+__device__ __forceinline__ void drain_candidate(const MarkovArgs& a, uint32_t e, float z, int c, int i,
+                                                unsigned long long* best) {
+    const int j = static_cast<int>(e >> 27);
+    const int v = static_cast<int>(e & 0x7FFFFFFu);
+    const float y = __fadd_rn(z, gumbel_at(a, c * kChunk + j, i, v));
+    if (y == y) atomicMax(best + j, argmax_key(y, static_cast<uint32_t>(v)));
+}
+
 __global__ void __launch_bounds__(kThreadsTC, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmL,
                  MarkovArgs a, TcArgs t) {
@@ -82,6 +91,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ float s_invT[256];
     __shared__ float s_lb[kGroups][kChunk];
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
+    __shared__ unsigned long long s_best[kGroups][kChunk];
+    __shared__ uint32_t s_qv[kEpiWarps][64];
+    __shared__ float s_qz[kEpiWarps][64];
     __shared__ int s_ok;
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -322,45 +334,63 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             }
                         }
                         s_lb[grp][lane] = lbv;
+                        s_best[grp][lane] = 0ull;
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
-                    // ---- pass 2: Gumbel noise only where z can still beat the bound ----
-                    float lb[kChunk], by[kChunk];
-                    int bv2[kChunk];
+                    // ---- pass 2: Gumbel noise only where z can still beat the bound; the
+                    //      surviving (request, v) pairs are compacted into a per-warp queue so
+                    //      that Philox and the two logarithms run 32 lanes wide ----
+                    float lb[kChunk];
 #pragma unroll
-                    for (int j = 0; j < kChunk; ++j) { lb[j] = s_lb[grp][j]; by[j] = -INFINITY; bv2[j] = -1; }
+                    for (int j = 0; j < kChunk; ++j) lb[j] = s_lb[grp][j];
                     bool any = false;
 #pragma unroll
                     for (int j = 0; j < kChunk; ++j) any |= lb[j] < INFINITY;
                     if (any && !dead) {
+                        uint32_t* qv = s_qv[epi];
+                        float* qz = s_qz[epi];
+                        unsigned long long* best = s_best[grp];
+                        int qn = 0;
                         for (int tl = 0; tl < nt; ++tl) {
                             const int v = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32 + lane);
                             const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
                             uint32_t r[kChunk];
                             tmem_ld16(taddr, r);
                             tmem_wait_ld();
-                            if (v < a.V) {
 #pragma unroll
-                                for (int j = 0; j < kChunk; ++j) {
-                                    const float z = __uint_as_float(r[j]);
-                                    if (__fadd_rn(z, kGumbelMax) >= lb[j]) {
-                                        const float y = __fadd_rn(z, gumbel_at(a, c * kChunk + j, i, v));
-                                        if (y > by[j]) { by[j] = y; bv2[j] = v; }
-                                    }
+                            for (int j = 0; j < kChunk; ++j) {
+                                const float z = __uint_as_float(r[j]);
+                                const bool pred = v < a.V && __fadd_rn(z, kGumbelMax) >= lb[j];
+                                const uint32_t mask = __ballot_sync(0xFFFFFFFFu, pred);
+                                if (mask == 0u) continue;
+                                if (pred) {
+                                    const int pos = qn + __popc(mask & ((1u << lane) - 1u));
+                                    qv[pos] = (static_cast<uint32_t>(j) << 27) | static_cast<uint32_t>(v);
+                                    qz[pos] = z;
+                                }
+                                qn += __popc(mask);
+                                if (qn >= 32) {
+                                    __syncwarp();
+                                    const uint32_t e = qv[lane];
+                                    const float ze = qz[lane];
+                                    const bool mv = static_cast<int>(lane) < qn - 32;
+                                    uint32_t e2 = 0;
+                                    float z2 = 0.f;
+                                    if (mv) { e2 = qv[32 + lane]; z2 = qz[32 + lane]; }
+                                    __syncwarp();
+                                    if (mv) { qv[lane] = e2; qz[lane] = z2; }
+                                    qn -= 32;
+                                    drain_candidate(a, e, ze, c, i, best);
                                 }
                             }
                         }
-                    }
-#pragma unroll
-                    for (int j = 0; j < kChunk; ++j) {
-                        const unsigned long long k = warp_max_u64(bv2[j] >= 0 ? argmax_key(by[j], static_cast<uint32_t>(bv2[j])) : 0ull);
-                        if (lane == 0) s_part[grp][quad][j] = k;
+                        __syncwarp();
+                        if (static_cast<int>(lane) < qn) drain_candidate(a, qv[lane], qz[lane], c, i, best);
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
                     if (grp_lead && lane < kChunk) {
                         const int b = c * kChunk + static_cast<int>(lane);
-                        unsigned long long k = 0;
-                        for (int q = 0; q < 4; ++q) k = s_part[grp][q][lane] > k ? s_part[grp][q][lane] : k;
+                        const unsigned long long k = s_best[grp][lane];
                         if (b < a.B && k != 0ull) atomicMax(slot + b, k);
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
@@ -400,7 +430,8 @@ size_t tc_smem_bytes(int B_pad, int r) {
 bool markov_tc_eligible(int B, int N, int V, int r, dspark_dtype wdtype, const float* base, const float* lse,
                         int sm_count) {
     if (wdtype != DSPARK_BF16 || lse != nullptr) return false;
-    if (B < 16 || B > 256 || r % 64 != 0 || r > 256 || V % 4 != 0 || V < kTileV) return false;
+    if (B < 16 || B > 256 || r % 64 != 0 || r > 256 || V % 4 != 0 || V < kTileV || V >= (1 << 27))
+        return false;
     if (N > 65535 || !aligned(base, 16)) return false;
     const int B_pad = (B + 15) & ~15;
     if (static_cast<size_t>(B_pad) * r * 2 > kEMaxBytes) return false;

@@ -107,10 +107,24 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
     for (int i = tid; i < kWarps * kRadix; i += kThreads) (&s_cnt[0][0])[i] = 0;
     __syncthreads();
 
-    // ---- 2. stable LSD radix sort on the upper 32 bits ----
+    // ---- 2. sort: keys are unique (the index is part of the key) ----
     unsigned long long* src = a.keys0;
     unsigned long long* dst = a.keys1;
-    for (int pass = 0; pass < 4; ++pass) {
+    if (n <= kThreads) {
+        // small pools: rank of each key = number of smaller keys (one key per thread)
+        unsigned long long* sk = reinterpret_cast<unsigned long long*>(&s_cnt[0][0]);
+        const unsigned long long mine = tid < n ? src[tid] : 0ull;
+        if (tid < n) sk[tid] = mine;
+        __syncthreads();
+        if (tid < n) {
+            int rank = 0;
+            for (int j = 0; j < n; ++j) rank += sk[j] < mine ? 1 : 0;
+            dst[rank] = mine;
+        }
+        __syncthreads();
+        src = dst;
+    }
+    for (int pass = 0; pass < (n <= kThreads ? 0 : 4); ++pass) {
         const int shift = 32 + 8 * pass;
         if (tid < kRadix) s_base[tid] = 0;
         __syncthreads();
@@ -164,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
         src = dst;
         dst = t;
     }
-    // after 4 passes the sorted keys are back in keys0 (== src)
+    // sorted keys are in src (keys0 after the 4 radix passes, keys1 after the rank sort)
 
     // ---- 3. capacity K ----
     if (a.K_in >= 0) {

@@ -1,19 +1,22 @@
-// Lossless speculative verification, one block per request.
+// Lossless speculative verification.
 //
 // "Speculative decoding: from zero to DSpark" §2: draft token x_k is accepted
 // with probability min(1, p_t(x_k)/p_d(x_k)); the first rejection k* draws a
 // correction from norm(max(0, p_t - p_d)); if all tested tokens pass, a bonus
 // token is drawn from p_t at the position after the block.
 //
-// Per request (block):
-//   1. all tested positions k < L_b are checked at once (one thread each):
-//      fl32(u_k * p_d[x_k]) < p_t[x_k]; k* = the smallest failing k (shared atomicMin)
-//   2. one streaming pass over the residual (or bonus) row: each warp turns 128
+// S blocks per request (S = 1 when the batch alone fills the GPU, more when it
+// does not, so a single request still streams its 1-2 vocabulary rows at full
+// bandwidth).  Every block of request b:
+//   1. checks all tested positions k < L_b at once (one thread each):
+//      fl32(u_k * p_d[x_k]) < p_t[x_k]; k* = the smallest failing k
+//   2. streams its share of the residual (or bonus) row: each warp turns 128
 //      consecutive entries into integer masses q_v = floor(w_v * 2^40) and
-//      stores their sum; Q = sum over the row
-//   3. t = floor(R * Q / 2^64); a block-wide exclusive scan over the 128-entry
-//      sums finds the segment holding t; one warp re-reads that segment and an
-//      inclusive warp scan picks the token.
+//      writes their sum to the workspace
+// The last block of the request to finish (an atomic counter) then
+//   3. sums the segment masses, t = floor(R * Q / 2^64), finds the segment
+//      holding t with a block-wide exclusive scan, re-reads that segment with
+//      one warp and picks the token with an inclusive warp scan.
 // Integer masses make the result independent of the summation order, so the
 // token equals the CPU reference bit for bit.
 #include "device_common.cuh"
@@ -27,7 +30,6 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSeg = 128;                        // entries per warp segment (4 per lane)
-constexpr int kMaxSegs = (1 << 24) / kSeg;       // V <= 2^24
 
 struct VerifyArgs {
     const float* p_t;
@@ -37,9 +39,11 @@ struct VerifyArgs {
     int32_t* out;
     int32_t* n_acc;
     WsHeader* ws;
+    uint32_t* done;              // [B] blocks finished per request
+    unsigned long long* seg;     // [B][n_seg] segment masses
     uint64_t seed;
     uint32_t offset;
-    int B, gamma, V;
+    int B, gamma, V, n_seg, splits;
 };
 
 // Four consecutive entries starting at e (a multiple of 4), zero past the end.
@@ -91,36 +95,37 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
     return x;
 }
 
-// Pass over the row: per-segment sums into seg[] and the total.
-__device__ unsigned long long segment_sums(const float* rt, const float* rd, int V, bool vec,
-                                           unsigned long long* seg, unsigned long long* red) {
-    const int n_seg = (V + kSeg - 1) / kSeg;
+// Masses of segments [s0, s1) of the row into dst[segment].
+__device__ void segment_sums(const float* rt, const float* rd, int V, bool vec, int s0, int s1,
+                             unsigned long long* dst) {
     const uint32_t warp = warp_id(), lane = lane_id();
-    unsigned long long total = 0;
-    for (int sgi = warp; sgi < n_seg; sgi += kWarps) {
+    for (int sgi = s0 + static_cast<int>(warp); sgi < s1; sgi += kWarps) {
         unsigned long long q[4];
         masses4(rt, rd, sgi * kSeg + 4 * static_cast<int>(lane), V, vec, q);
         const unsigned long long s = warp_sum_u64(q[0] + q[1] + q[2] + q[3]);
-        if (lane == 0) seg[sgi] = s;
-        total += s;
+        if (lane == 0) dst[sgi] = s;
     }
+}
+
+__device__ unsigned long long block_sum_u64(unsigned long long x, unsigned long long* red) {
+    x = warp_sum_u64(x);
     __syncthreads();
-    if (lane == 0) red[warp] = total;
+    if (lane_id() == 0) red[warp_id()] = x;
     __syncthreads();
-    unsigned long long Q = 0;
-    for (int w = 0; w < kWarps; ++w) Q += red[w];
-    __syncthreads();
-    return Q;
+    unsigned long long s = 0;
+    for (int w = 0; w < kWarps; ++w) s += red[w];
+    return s;
 }
 
 __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
-    extern __shared__ unsigned long long seg[];           // [n_seg] segment sums
+    extern __shared__ unsigned long long s_seg[];         // [n_seg] (last block only)
     __shared__ unsigned long long s_red[kWarps];
     __shared__ unsigned long long s_scan[kWarps];
-    __shared__ int s_kstar, s_bad, s_pick;
+    __shared__ int s_kstar, s_bad, s_pick, s_last;
     __shared__ unsigned long long s_tloc;
 
-    const int b = blockIdx.x;
+    const int b = blockIdx.x / a.splits;
+    const int split = blockIdx.x % a.splits;
     const int tid = threadIdx.x;
     const int V = a.V, g = a.gamma;
     int32_t* out = a.out + static_cast<size_t>(b) * (g + 1);
@@ -150,22 +155,49 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
     }
     __syncthreads();
     if (s_bad) {
-        if (tid == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
-        for (int k = tid; k <= g; k += kThreads) out[k] = -1;
-        if (tid == 0) a.n_acc[b] = 0;
+        if (split == 0) {
+            if (tid == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+            for (int k = tid; k <= g; k += kThreads) out[k] = -1;
+            if (tid == 0) a.n_acc[b] = 0;
+        }
         return;
     }
     const int kstar = s_kstar;
     const bool rej = kstar < Lb;
 
-    // ---- 2. residual (or bonus) row -> segment masses ----
+    // ---- 2. this block's share of the residual (or bonus) row ----
     const float* rt = a.p_t + (static_cast<size_t>(b) * (g + 1) + kstar) * V;
     const float* rd = rej ? a.p_d + (static_cast<size_t>(b) * g + kstar) * V : nullptr;
     const bool vec = (V & 3) == 0;
-    unsigned long long Q = segment_sums(rt, rd, V, vec, seg, s_red);
+    const int n_seg = a.n_seg;
+    unsigned long long* seg = a.seg + static_cast<size_t>(b) * n_seg;
+    const int s0 = static_cast<int>((static_cast<long long>(split) * n_seg) / a.splits);
+    const int s1 = static_cast<int>((static_cast<long long>(split + 1) * n_seg) / a.splits);
+    segment_sums(rt, rd, V, vec, s0, s1, seg);
+
+    // ---- the last block of the request finishes it ----
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(a.done + b, 1u) == static_cast<uint32_t>(a.splits - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    unsigned long long mine = 0;
+    for (int s = tid; s < n_seg; s += kThreads) {
+        const unsigned long long v = __ldcg(seg + s);
+        s_seg[s] = v;
+        mine += v;
+    }
+    unsigned long long Q = block_sum_u64(mine, s_red);
     if (Q == 0 && rd != nullptr) {                 // residual without mass: use the p_t row
         rd = nullptr;
-        Q = segment_sums(rt, rd, V, vec, seg, s_red);
+        __syncthreads();
+        segment_sums(rt, rd, V, vec, 0, n_seg, s_seg);
+        __syncthreads();
+        mine = 0;
+        for (int s = tid; s < n_seg; s += kThreads) mine += s_seg[s];
+        Q = block_sum_u64(mine, s_red);
     }
 
     int y;
@@ -177,6 +209,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
             best = k > best ? k : best;
         }
         best = warp_max_u64(best);
+        __syncthreads();
         if (lane_id() == 0) s_red[warp_id()] = best;
         __syncthreads();
         unsigned long long m = 0;
@@ -189,19 +222,18 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
                                   static_cast<uint32_t>(kstar));
         const unsigned long long R = (static_cast<unsigned long long>(w.x) << 32) | w.y;
         const unsigned long long t = __umul64hi(R, Q);
-        // block-wide exclusive scan over segment sums, each thread owning a run of segments
-        const int n_seg = (V + kSeg - 1) / kSeg;
+        // block-wide exclusive scan over segment masses, each thread owning a run of segments
         const int per = (n_seg + kThreads - 1) / kThreads;
-        const int s0 = tid * per, s1 = min(n_seg, s0 + per);
-        unsigned long long mine = 0;
-        for (int s = s0; s < s1; ++s) mine += seg[s];
-        const unsigned long long incl = warp_incl_scan_u64(mine);
+        const int r0 = tid * per, r1 = min(n_seg, r0 + per);
+        unsigned long long run = 0;
+        for (int s = r0; s < r1; ++s) run += s_seg[s];
+        const unsigned long long incl = warp_incl_scan_u64(run);
         if (lane_id() == 31) s_scan[warp_id()] = incl;
         __syncthreads();
-        unsigned long long before = incl - mine;
+        unsigned long long before = incl - run;
         for (int w2 = 0; w2 < static_cast<int>(warp_id()); ++w2) before += s_scan[w2];
-        for (int s = s0; s < s1; ++s) {
-            const unsigned long long sv = seg[s];
+        for (int s = r0; s < r1; ++s) {
+            const unsigned long long sv = s_seg[s];
             if (before <= t && t < before + sv) {   // exactly one segment holds t
                 s_pick = s;
                 s_tloc = t - before;
@@ -216,11 +248,11 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
             masses4(rt, rd, s * kSeg + 4 * static_cast<int>(lane_id()), V, vec, q);
             const unsigned long long lane_sum = q[0] + q[1] + q[2] + q[3];
             const unsigned long long incl_l = warp_incl_scan_u64(lane_sum);
-            unsigned long long run = incl_l - lane_sum;
+            unsigned long long acc = incl_l - lane_sum;
             int pick = -1;
             for (int j = 0; j < 4; ++j) {
-                run += q[j];
-                if (pick < 0 && run > tl) pick = j;
+                acc += q[j];
+                if (pick < 0 && acc > tl) pick = j;
             }
             const bool has = (incl_l - lane_sum <= tl) && (tl < incl_l);
             const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, has);
@@ -246,24 +278,28 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
     if (tid == 0) a.n_acc[b] = kstar;
 }
 
+int n_segments(int V) { return (V + kSeg - 1) / kSeg; }
+
+size_t done_bytes(int B) { return (sizeof(uint32_t) * static_cast<size_t>(B) + 15) & ~static_cast<size_t>(15); }
+
 }  // namespace
+
+size_t verify_workspace_bytes(int B, int V) {
+    return sizeof(WsHeader) + done_bytes(B) + sizeof(unsigned long long) * static_cast<size_t>(B) * n_segments(V);
+}
 
 dspark_status launch_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,
                             const int32_t* lengths, uint64_t seed, uint32_t offset, int B, int gamma,
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
                             cudaStream_t stream, const DeviceInfo& dev) {
-    dspark_status st = clear_workspace(ws, sizeof(WsHeader), stream);
-    if (st != DSPARK_OK) return st;
-    const int n_seg = (V + kSeg - 1) / kSeg;
-    if (n_seg > kMaxSegs) {
-        set_error("verify: V=%d too large", V);
-        return DSPARK_ERR_UNSUPPORTED;
-    }
+    const int n_seg = n_segments(V);
     const size_t smem = sizeof(unsigned long long) * static_cast<size_t>(n_seg);
     if (smem > dev.smem_optin) {
         set_error("verify: V=%d needs %zu bytes of shared memory", V, smem);
         return DSPARK_ERR_UNSUPPORTED;
     }
+    dspark_status st = clear_workspace(ws, sizeof(WsHeader) + done_bytes(B), stream);
+    if (st != DSPARK_OK) return st;
     cudaError_t e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(verify)");
@@ -275,12 +311,22 @@ dspark_status launch_verify(const float* p_target, const float* p_draft, const i
     a.out = out_tokens;
     a.n_acc = num_accepted;
     a.ws = static_cast<WsHeader*>(ws);
+    a.done = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader));
+    a.seg = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader) + done_bytes(B));
     a.seed = seed;
     a.offset = offset;
     a.B = B;
     a.gamma = gamma;
     a.V = V;
-    verify_kernel<<<B, kThreads, smem, stream>>>(a);
+    a.n_seg = n_seg;
+    // enough blocks to cover the GPU twice, but at least 8 segments (1024 entries) per block
+    a.splits = B >= dev.sm_count ? 1 : std::max(1, std::min((2 * dev.sm_count + B - 1) / B, n_seg / 8));
+    const long long grid = static_cast<long long>(B) * a.splits;
+    if (grid > 0x7FFFFFFFLL) {
+        set_error("verify: too many requests (%d)", B);
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    verify_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "launch(verify)");
     return DSPARK_OK;

@@ -77,10 +77,12 @@ typedef enum {
 #define DSPARK_STATUS_INTERNAL     0x8u
 
 /*
- * Bytes of workspace an operation needs.  op is a dspark_op; for
- * DSPARK_OP_DRAFT_LOGITS and DSPARK_OP_VERIFY only the status word is needed
- * (256 bytes); for DSPARK_OP_MARKOV_SAMPLE it grows with B*N and B; for
- * DSPARK_OP_SCHEDULE with B*N.  Arguments an op does not use are ignored.
+ * Bytes of workspace an operation needs.  op is a dspark_op; arguments an op
+ * does not use are ignored:
+ *   DSPARK_OP_DRAFT_LOGITS  256 (the status word)
+ *   DSPARK_OP_MARKOV_SAMPLE grows with B*N and B (argmax slots, bounds, lse partials)
+ *   DSPARK_OP_VERIFY        grows with B*V/128 (per-128-entry integer masses); N = gamma
+ *   DSPARK_OP_SCHEDULE      grows with B*N (radix-sort key buffers)
  * Returns 0 for an unknown op or negative sizes.
  */
 DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);

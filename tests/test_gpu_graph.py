@@ -33,7 +33,7 @@ def test_capture_and_replay_whole_step(cuda_lib):
     sel = torch.empty(8, dtype=torch.int32, device="cuda")
     ws_g = ds.Workspace(ds.OP_DRAFT_LOGITS)
     ws_m = ds.Workspace(ds.OP_MARKOV_SAMPLE, cfg.B, cfg.N, cfg.V, cfg.r)
-    ws_v = ds.Workspace(ds.OP_VERIFY)
+    ws_v = ds.Workspace(ds.OP_VERIFY, 1, 8, cfg.V)
     ws_s = ds.Workspace(ds.OP_SCHEDULE, 1, 8)
 
     def step():

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _gpu(ds, p_t, p_d, x, lengths, seed, offset):
-    ws = ds.Workspace(ds.OP_VERIFY)
+    ws = ds.Workspace(ds.OP_VERIFY, p_t.shape[0], p_t.shape[1] - 1, p_t.shape[2])
     out, nacc = ds.dspark_verify(to_dev(p_t), to_dev(p_d), to_dev(np.asarray(x, np.int32)),
                                  None if lengths is None else to_dev(np.asarray(lengths, np.int32)),
                                  seed, offset, workspace=ws)
