@@ -15,6 +15,7 @@ constexpr uint32_t kWaitStep = 0x200;                  // + step index (grid bar
 struct MarkovLayout {
     unsigned long long* slots;   // [N][B] argmax keys
     uint32_t* lb;                // [N][B] order bits of the published lower bound
+    uint32_t* pub;               // [N] blocks that have published their bounds (tensor path)
     float2* lse_part;            // [2][kMaxGrid][B] (max, sum) partials
 };
 
@@ -25,6 +26,8 @@ __host__ __device__ inline MarkovLayout markov_layout(void* ws, int B, int N) {
     p += sizeof(unsigned long long) * static_cast<size_t>(N) * B;
     L.lb = reinterpret_cast<uint32_t*>(p);
     p += sizeof(uint32_t) * static_cast<size_t>(N) * B;
+    L.pub = reinterpret_cast<uint32_t*>(p);
+    p += sizeof(uint32_t) * static_cast<size_t>(N);
     p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15));
     L.lse_part = reinterpret_cast<float2*>(p);
     return L;
@@ -47,6 +50,7 @@ struct MarkovArgs {
     int w2_cached;              // w2 slice lives in shared memory
     int w2_pitch;               // bytes per cached w2 row (padded)
     int z_stored;               // z rows live in shared memory
+    int single_pass;            // noise on every element in one pass (few elements per block)
     long long timeout_ns;
 };
 

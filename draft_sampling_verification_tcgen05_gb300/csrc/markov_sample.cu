@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     int* prev = reinterpret_cast<int*>(sp);
 
     const size_t row_bytes = sizeof(WT) * static_cast<size_t>(a.r);
+    const size_t row_bytes_w1 = row_bytes;
     if (a.w2_cached) {
         // load this block's w2 rows once; rows padded to w2_pitch bytes
         const uint8_t* src = static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v_lo) * row_bytes;
@@ -201,9 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 const float z = hot ? __fmul_rn(s, invT) : s;
                 if (a.z_stored) zs[static_cast<size_t>(b) * a.slice + t] = z;
                 if (z != z) { bad = true; continue; }
-                const unsigned long long k = argmax_key(z, static_cast<uint32_t>(v));
-                best = k > best ? k : best;
                 if (a.lse != nullptr && z > -INFINITY) ls = lse_merge(ls, make_float2(z, 1.f));
+                // single pass (few elements per block): perturb every element right away
+                const float key_val = (hot && a.single_pass) ? __fadd_rn(z, gumbel_at(a, b, i, v)) : z;
+                if (key_val != key_val) continue;
+                const unsigned long long k = argmax_key(key_val, static_cast<uint32_t>(v));
+                best = k > best ? k : best;
             }
             if (bad) set_status(a.ws, DSPARK_STATUS_NUMERIC);
             best = block_max_u64(best, s_red);
@@ -213,7 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             }
             if (tid == 0 && best != 0ull) {
                 const uint32_t vb = key_index(best);
-                if (hot) {
+                // the next step may gather this row: bring it into L2 now
+                for (size_t l = 0; l < row_bytes_w1; l += 128)
+                    prefetch_l2(static_cast<const uint8_t*>(a.w1) + static_cast<size_t>(vb) * row_bytes_w1 + l);
+                if (hot && !a.single_pass) {
                     const float zb = float_from_order_bits(static_cast<uint32_t>(best >> 32));
                     const float y = __fadd_rn(zb, gumbel_at(a, b, i, static_cast<int>(vb)));
                     atomicMax(lbs + b, float_order_bits(y));
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                     atomicMax(slot + b, best);
                 }
             }
-            if (!hot) continue;
+            if (!hot || a.single_pass) continue;
 
             // ---- 3. pass 2: Gumbel noise where the element can still win ----
             __syncthreads();
@@ -275,6 +282,9 @@ dspark_status run_generic(MarkovArgs& a, cudaStream_t stream, const DeviceInfo& 
     a.w2_pitch = static_cast<int>(row_bytes + 16);
     a.w2_cached = (row_bytes % 16 == 0) && static_cast<size_t>(a.slice) * a.w2_pitch <= kW2CacheBytes;
     a.z_stored = sizeof(float) * static_cast<size_t>(a.slice) * a.B <= kZStoreBytes;
+    // at most 8 elements per thread and step: one pass with noise on every element is
+    // cheaper than publishing a bound and making a second pass
+    a.single_pass = static_cast<size_t>(a.slice) * a.B <= static_cast<size_t>(8 * kThreads);
     if (static_cast<size_t>(a.B) * a.r > static_cast<size_t>(kMaxEFloats)) {
         set_error("markov_sample: B*r = %d exceeds the %d the sampler holds on chip", a.B * a.r, kMaxEFloats);
         return DSPARK_ERR_UNSUPPORTED;
@@ -317,7 +327,8 @@ dspark_status run_generic(MarkovArgs& a, cudaStream_t stream, const DeviceInfo& 
 
 size_t markov_workspace_bytes(int B, int N) {
     const size_t nb = static_cast<size_t>(B) * N;
-    size_t bytes = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t);
+    size_t bytes = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t) +
+                   sizeof(uint32_t) * static_cast<size_t>(N);
     bytes = (bytes + 15) & ~static_cast<size_t>(15);
     bytes += 2 * static_cast<size_t>(kMaxGrid) * B * sizeof(float2);
     return bytes;
@@ -330,7 +341,8 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
                                    const DeviceInfo& dev) {
     // clear header, slots and bounds (the lse partials need no clearing)
     const size_t nb = static_cast<size_t>(B) * N;
-    const size_t clear = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t);
+    const size_t clear = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t) +
+                         sizeof(uint32_t) * static_cast<size_t>(N);
     dspark_status st = clear_workspace(ws, clear, stream);
     if (st != DSPARK_OK) return st;
     MarkovArgs a = {};

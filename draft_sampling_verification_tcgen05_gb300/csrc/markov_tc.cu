@@ -41,8 +41,8 @@ constexpr int kGroups = 2;
 constexpr int kEpiWarps = 4 * kGroups;
 constexpr int kThreadsTC = 32 * (2 + kEpiWarps);
 constexpr uint32_t kStepThreads = 32 * (1 + kEpiWarps);
-constexpr int kW2Stages = 4;
-constexpr int kLStages = 5;                      // per epilogue group
+constexpr int kW2Stages = 8;                    // upper bound; the launcher picks 4 or 8
+constexpr int kLStages = 5;                      // upper bound per epilogue group; the launcher picks 3 or 5
 constexpr int kTileV = 128;
 constexpr int kChunk = 16;                       // requests per epilogue chunk
 constexpr int kMaxLocalTiles = 32;
@@ -50,10 +50,13 @@ constexpr uint32_t kW2StageBytes = kTileV * 128;             // 128 rows x 64 bf
 constexpr uint32_t kLStageBytes = kTileV * kChunk * 4;       // 16 requests x 128 fp32
 constexpr uint32_t kBarStep = 1;
 constexpr uint32_t kBarGroup0 = 2;
+constexpr uint32_t kBarEpi = kBarGroup0 + kGroups;   // all epilogue warps
 constexpr uint32_t kWaitProducer = 0x301, kWaitMma = 0x302, kWaitEpi = 0x303;
 constexpr size_t kEMaxBytes = 64 * 1024;
 
 struct TcArgs {
+    int w2_stages;        // depth of the w2 ring
+    int l_stages;         // depth of each base-logit ring
     int B_pad;            // B rounded up to 16 (MMA N)
     int n_tiles;          // ceil(V / 128)
     uint32_t tmem_cols;   // power of two >= max tiles per block * B_pad
@@ -80,8 +83,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* w2s = base;
-    uint8_t* Ls = w2s + kW2Stages * kW2StageBytes;
-    uint8_t* Es = Ls + kGroups * kLStages * kLStageBytes;
+    uint8_t* Ls = w2s + t.w2_stages * kW2StageBytes;
+    uint8_t* Es = Ls + kGroups * t.l_stages * kLStageBytes;
 
     __shared__ uint64_t bar_w2_full[kW2Stages], bar_w2_empty[kW2Stages];
     __shared__ uint64_t bar_L_full[kGroups][kLStages], bar_L_empty[kGroups][kLStages];
@@ -171,7 +174,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 }
                                 mbar_arrive_expect_tx(&bar_w2_full[ws], kW2StageBytes);
                                 tma_load_2d(w2s + ws * kW2StageBytes, &tmW2, kb * 64, v0, &bar_w2_full[ws], pol_keep);
-                                if (++ws == kW2Stages) { ws = 0; wph ^= 1u; }
+                                if (++ws == t.w2_stages) { ws = 0; wph ^= 1u; }
                             }
                         }
                         for (int g = 0; g < kGroups && ok; ++g) {
@@ -182,9 +185,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 break;
                             }
                             mbar_arrive_expect_tx(&bar_L_full[g][ls[g]], kLStageBytes);
-                            tma_load_3d(Ls + (g * kLStages + ls[g]) * kLStageBytes, &tmL, v0, i, c * kChunk,
+                            tma_load_3d(Ls + (g * t.l_stages + ls[g]) * kLStageBytes, &tmL, v0, i, c * kChunk,
                                         &bar_L_full[g][ls[g]], pol_stream);
-                            if (++ls[g] == kLStages) { ls[g] = 0; lph[g] ^= 1u; }
+                            if (++ls[g] == t.l_stages) { ls[g] = 0; lph[g] ^= 1u; }
                         }
                     }
                 }
@@ -194,12 +197,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 // ring position were last filled in the current phase, the rest one phase
                 // earlier (or never, which reads as complete)
                 const long long t0 = global_ns();
-                for (int s = 0; s < kW2Stages; ++s)
+                for (int s = 0; s < t.w2_stages; ++s)
                     while (!mbar_try_wait(&bar_w2_full[s], s < ws ? wph : (wph ^ 1u)) &&
                            global_ns() - t0 < a.timeout_ns) {
                     }
                 for (int g = 0; g < kGroups; ++g)
-                    for (int s = 0; s < kLStages; ++s)
+                    for (int s = 0; s < t.l_stages; ++s)
                         while (!mbar_try_wait(&bar_L_full[g][s], s < ls[g] ? lph[g] : (lph[g] ^ 1u)) &&
                                global_ns() - t0 < a.timeout_ns) {
                         }
@@ -265,7 +268,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 mma_issue<false>(d, sw128_kmajor_desc(a_addr + 32 * k),
                                                  sw128_kmajor_desc(b_addr + 32 * k), idesc, (kb | k) != 0 ? 1u : 0u);
                             mma_commit(&bar_w2_empty[w2st]);
-                            if (++w2st == kW2Stages) { w2st = 0; w2ph ^= 1u; }
+                            if (++w2st == t.w2_stages) { w2st = 0; w2ph ^= 1u; }
                         }
                         if (!dead) mma_commit(&bar_tile[tl]);
                     }
@@ -274,10 +277,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
             } else {
                 unsigned long long* slot = a.lay.slots + static_cast<size_t>(i) * a.B;
                 uint32_t* lbs = a.lay.lb + static_cast<size_t>(i) * a.B;
+                const int row_lines = a.r * 2 / 128;                   // 128-byte lines of a w1 row
+                // ---- pass 1 over this group's chunks: z = (base + bias) / T into TMEM, argmax of z ----
                 for (int ro = 0; ro < rounds; ++ro) {
                     const int c = ro * kGroups + grp;
                     if (c >= n_chunks) continue;                       // uniform over the group
-                    // ---- pass 1: z = (base + bias) / T into TMEM, argmax of z ----
                     float bz[kChunk];
                     int bv[kChunk];
 #pragma unroll
@@ -294,7 +298,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             uint32_t r[kChunk];
                             tmem_ld16(taddr, r);
                             tmem_wait_ld();
-                            const float* Lt = reinterpret_cast<const float*>(Ls + (grp * kLStages + lsg) * kLStageBytes);
+                            const float* Lt = reinterpret_cast<const float*>(Ls + (grp * t.l_stages + lsg) * kLStageBytes);
 #pragma unroll
                             for (int j = 0; j < kChunk; ++j) {
                                 const float s = __fadd_rn(Lt[j * kTileV + quad * 32 + lane], __uint_as_float(r[j]));
@@ -307,7 +311,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             tmem_st16(taddr, r);
                         }
                         mbar_arrive(&bar_L_empty[grp][lsg]);
-                        if (++lsg == kLStages) { lsg = 0; lphg ^= 1u; }
+                        if (++lsg == t.l_stages) { lsg = 0; lphg ^= 1u; }
                     }
                     if (!dead) tmem_wait_st();
 #pragma unroll
@@ -317,10 +321,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
                     if (grp_lead && lane < kChunk) {
+                        // the block's best z, perturbed by its own noise, is a value some element
+                        // reaches: publish it as a lower bound of the step's maximum
                         const int b = c * kChunk + static_cast<int>(lane);
                         unsigned long long k = 0;
                         for (int q = 0; q < 4; ++q) k = s_part[grp][q][lane] > k ? s_part[grp][q][lane] : k;
-                        float lbv = INFINITY;                          // nothing to sample
                         if (b < a.B && k != 0ull) {
                             const uint32_t vb = key_index(k);
                             if (s_invT[b] > 0.f) {
@@ -328,18 +333,44 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 const float y = __fadd_rn(zb, gumbel_at(a, b, i, static_cast<int>(vb)));
                                 atomicMax(lbs + b, float_order_bits(y));
                                 atomicMax(slot + b, argmax_key(y, vb));
-                                lbv = float_from_order_bits(__ldcg(lbs + b));
                             } else {
                                 atomicMax(slot + b, k);                 // greedy: argmax of z is the token
                             }
+                            // the next step may gather this row: bring it into L2 now
+                            for (int l = 0; l < row_lines; ++l)
+                                prefetch_l2(static_cast<const uint8_t*>(a.w1) + static_cast<size_t>(vb) * a.r * 2 + 128 * l);
                         }
-                        s_lb[grp][lane] = lbv;
+                    }
+                    named_bar_sync(kBarGroup0 + grp, 128);
+                }
+
+                // ---- wait (bounded) until every block has published its bounds for this step ----
+                named_bar_sync(kBarEpi, 32 * kEpiWarps);
+                if (epi == 0 && lane == 0) {
+                    uint32_t* pub = a.lay.pub + i;
+                    __threadfence();
+                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(pub) : "memory");
+                    const long long t0 = global_ns();
+                    while (ld_acquire_u32(pub) < gridDim.x && !aborted(a.ws) &&
+                           global_ns() - t0 < a.timeout_ns)
+                        __nanosleep(32);
+                    // running out only weakens the bound; the result stays exact
+                }
+                named_bar_sync(kBarEpi, 32 * kEpiWarps);
+
+                // ---- pass 2 over this group's chunks: Gumbel noise only where z can still beat
+                //      the bound; surviving (request, v) pairs are compacted into a per-warp
+                //      queue so that Philox and the two logarithms run 32 lanes wide ----
+                for (int ro = 0; ro < rounds; ++ro) {
+                    const int c = ro * kGroups + grp;
+                    if (c >= n_chunks) continue;
+                    if (grp_lead && lane < kChunk) {
+                        const int b = c * kChunk + static_cast<int>(lane);
+                        s_lb[grp][lane] = (b < a.B && s_invT[b] > 0.f) ? float_from_order_bits(__ldcg(lbs + b))
+                                                                        : INFINITY;
                         s_best[grp][lane] = 0ull;
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
-                    // ---- pass 2: Gumbel noise only where z can still beat the bound; the
-                    //      surviving (request, v) pairs are compacted into a per-warp queue so
-                    //      that Philox and the two logarithms run 32 lanes wide ----
                     float lb[kChunk];
 #pragma unroll
                     for (int j = 0; j < kChunk; ++j) lb[j] = s_lb[grp][j];
@@ -391,9 +422,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                     if (grp_lead && lane < kChunk) {
                         const int b = c * kChunk + static_cast<int>(lane);
                         const unsigned long long k = s_best[grp][lane];
-                        if (b < a.B && k != 0ull) atomicMax(slot + b, k);
+                        if (b < a.B && k != 0ull) {
+                            atomicMax(slot + b, k);
+                            const uint32_t vb = key_index(k);
+                            for (int l = 0; l < row_lines; ++l)
+                                prefetch_l2(static_cast<const uint8_t*>(a.w1) + static_cast<size_t>(vb) * a.r * 2 + 128 * l);
+                        }
                     }
-                    named_bar_sync(kBarGroup0 + grp, 128);
                 }
             }
             // ---- every block agrees on the step's winners ----
@@ -420,8 +455,17 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     }
 }
 
+// Ring depths: deep w2 ring (L2 stream) when the E operand leaves room.
+void tc_rings(int B_pad, int r, int* w2_stages, int* l_stages) {
+    const bool small_e = static_cast<size_t>(B_pad) * r * 2 <= 32 * 1024;
+    *w2_stages = small_e ? 8 : 4;
+    *l_stages = small_e ? 3 : 5;
+}
+
 size_t tc_smem_bytes(int B_pad, int r) {
-    return 1024 + kW2Stages * kW2StageBytes + kGroups * kLStages * kLStageBytes +
+    int w2s, ls;
+    tc_rings(B_pad, r, &w2s, &ls);
+    return 1024 + static_cast<size_t>(w2s) * kW2StageBytes + static_cast<size_t>(kGroups) * ls * kLStageBytes +
            static_cast<size_t>(B_pad) * r * 2;
 }
 
@@ -444,6 +488,7 @@ bool markov_tc_eligible(int B, int N, int V, int r, dspark_dtype wdtype, const f
 dspark_status launch_markov_tc(const MarkovArgs& a, cudaStream_t stream, const DeviceInfo& dev) {
     TcArgs t;
     t.B_pad = (a.B + 15) & ~15;
+    tc_rings(t.B_pad, a.r, &t.w2_stages, &t.l_stages);
     t.n_tiles = (a.V + kTileV - 1) / kTileV;
     const int grid = std::min(dev.sm_count, t.n_tiles);
     const int max_local = (t.n_tiles + grid - 1) / grid;
