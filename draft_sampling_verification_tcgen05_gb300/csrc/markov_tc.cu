@@ -68,12 +68,17 @@ __device__ __forceinline__ void tile_range(const TcArgs& t, int& lo, int& hi) {
 }
 
 // One queued candidate: request c*16 + j, vocabulary entry v, scaled logit z.
+// Folds its perturbed value into this lane's running maximum for request j
+// (registers; the unrolled selects avoid both atomics and local memory).
 __device__ __forceinline__ void drain_candidate(const MarkovArgs& a, uint32_t e, float z, int c, int i,
-                                                unsigned long long* best) {
+                                                unsigned long long (&best)[kChunk]) {
     const int j = static_cast<int>(e >> 27);
     const int v = static_cast<int>(e & 0x7FFFFFFu);
     const float y = __fadd_rn(z, gumbel_at(a, c * kChunk + j, i, v));
-    if (y == y) atomicMax(best + j, argmax_key(y, static_cast<uint32_t>(v)));
+    const unsigned long long k = (y == y) ? argmax_key(y, static_cast<uint32_t>(v)) : 0ull;
+#pragma unroll
+    for (int jj = 0; jj < kChunk; ++jj)
+        if (jj == j && k > best[jj]) best[jj] = k;
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -94,7 +99,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ float s_invT[256];
     __shared__ float s_lb[kGroups][kChunk];
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
-    __shared__ unsigned long long s_best[kGroups][kChunk];
     __shared__ uint32_t s_qv[kEpiWarps][64];
     __shared__ float s_qz[kEpiWarps][64];
     __shared__ int s_ok;
@@ -368,19 +372,18 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                         const int b = c * kChunk + static_cast<int>(lane);
                         s_lb[grp][lane] = (b < a.B && s_invT[b] > 0.f) ? float_from_order_bits(__ldcg(lbs + b))
                                                                         : INFINITY;
-                        s_best[grp][lane] = 0ull;
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
                     float lb[kChunk];
+                    unsigned long long best[kChunk];
 #pragma unroll
-                    for (int j = 0; j < kChunk; ++j) lb[j] = s_lb[grp][j];
+                    for (int j = 0; j < kChunk; ++j) { lb[j] = s_lb[grp][j]; best[j] = 0ull; }
                     bool any = false;
 #pragma unroll
                     for (int j = 0; j < kChunk; ++j) any |= lb[j] < INFINITY;
                     if (any && !dead) {
                         uint32_t* qv = s_qv[epi];
                         float* qz = s_qz[epi];
-                        unsigned long long* best = s_best[grp];
                         int qn = 0;
                         for (int tl = 0; tl < nt; ++tl) {
                             const int v = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32 + lane);
@@ -418,10 +421,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                         __syncwarp();
                         if (static_cast<int>(lane) < qn) drain_candidate(a, qv[lane], qz[lane], c, i, best);
                     }
+#pragma unroll
+                    for (int j = 0; j < kChunk; ++j) {
+                        const unsigned long long k = warp_max_u64(best[j]);
+                        if (lane == 0) s_part[grp][quad][j] = k;
+                    }
                     named_bar_sync(kBarGroup0 + grp, 128);
                     if (grp_lead && lane < kChunk) {
                         const int b = c * kChunk + static_cast<int>(lane);
-                        const unsigned long long k = s_best[grp][lane];
+                        unsigned long long k = 0;
+                        for (int q = 0; q < 4; ++q) k = s_part[grp][q][lane] > k ? s_part[grp][q][lane] : k;
                         if (b < a.B && k != 0ull) {
                             atomicMax(slot + b, k);
                             const uint32_t vb = key_index(k);
