@@ -274,3 +274,78 @@ dspark_status launch_schedule(const float* cond_accept, const double* sps, int S
 }
 
 }  // namespace dspark
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of dspark_schedule.
+//
+// Some callers cannot hand this library a workspace: a serving loop that must
+// never block (cudaMalloc and cudaFree can synchronise with work already queued
+// on the device), or a host whose device memory is entirely reserved by another
+// allocator (a framework's memory pool), where a fresh allocation would fail.
+// For them the scratch that dspark_schedule takes from its workspace (a status
+// header and two radix-sort key buffers) lives here instead, in one fixed array
+// that every GPU loading the library holds until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace dspark {
+namespace {
+
+constexpr int kNoAllocMaxCandidates = 16384;                 // B * N limit
+constexpr size_t kNoAllocScratchBytes =
+    sizeof(WsHeader) + 2 * sizeof(unsigned long long) * static_cast<size_t>(kNoAllocMaxCandidates);
+
+static __device__ __align__(256) unsigned char g_schedule_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+
+// Device address of g_schedule_scratch on the current device, looked up once per device.
+dspark_status schedule_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) {
+        set_error("device index %d out of range", dev);
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_schedule_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(schedule scratch)");
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return DSPARK_OK;
+}
+
+}  // namespace
+}  // namespace dspark
+
+extern "C" dspark_status dspark_schedule_noalloc(const float* cond_accept, const double* sps, int S, int B,
+                                                 int N, int K_in, float* survival, int32_t* K_out,
+                                                 int32_t* lengths, int32_t* selected, void* stream) {
+    using namespace dspark;
+    set_error("%s", "");
+    if (!(cond_accept && survival && K_out && lengths && selected)) {
+        set_error("schedule_noalloc: null pointer");
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    if (B < 1 || N < 1 || static_cast<long long>(B) * N > kNoAllocMaxCandidates) {
+        set_error("schedule_noalloc: B*N must be between 1 and %d (got B=%d N=%d); "
+                  "larger pools need dspark_schedule with a workspace", kNoAllocMaxCandidates, B, N);
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    if (K_in < 0 && (sps == nullptr || S < 1)) {
+        set_error("schedule_noalloc: choosing K needs an SPS table (S >= 1)");
+        return DSPARK_ERR_INVALID_ARG;
+    }
+    DeviceInfo dev;
+    if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    const dspark_status st = schedule_scratch(&scratch);
+    if (st != DSPARK_OK) return st;
+    return launch_schedule(cond_accept, sps, S, B, N, K_in, survival, K_out, lengths, selected, scratch,
+                           static_cast<cudaStream_t>(stream), dev);
+}

@@ -213,6 +213,32 @@ DSPARK_API dspark_status dspark_schedule(const float* cond_accept, const double*
                               void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Allocation-free variant of dspark_schedule (no counterpart on the pages: it
+ * exists for callers, not for the method).  Same arguments, results and
+ * requirements as dspark_schedule, without the workspace.
+ *
+ * For callers that cannot provide device scratch memory: a serving loop that
+ * must never block (cudaMalloc/cudaFree can synchronise with work already
+ * queued on the device), or a host whose device memory is wholly reserved by
+ * another allocator, so that a new allocation would fail.  The scratch lives in
+ * one fixed array inside the library (262,400 bytes, held on every GPU that
+ * loads the library until the process exits); the call allocates nothing.
+ *   - B*N must be at most 16384; larger pools return DSPARK_ERR_INVALID_ARG
+ *     (use dspark_schedule with a workspace).
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the array and each call clears its status header first.
+ *     Calls that overlap on the GPU (different streams, or several threads)
+ *     race on it and must be serialised by the caller.
+ *   - Device-side status bits (clamped confidences) go to the shared array
+ *     and are not reported; use dspark_schedule when they are needed.
+ */
+DSPARK_API dspark_status dspark_schedule_noalloc(const float* cond_accept, const double* sps, int S,
+                                                 int B, int N, int K_in,
+                                                 float* survival, int32_t* K_out, int32_t* lengths,
+                                                 int32_t* selected, void* stream);
+
+/*
  * Synchronises `stream`, reads the status word of `workspace` written by the
  * last call that used it, stores the raw DSPARK_STATUS_* bits in *bits (if
  * bits != NULL) and returns the most severe matching dspark_status
