@@ -17,8 +17,13 @@ verification uses a seeded uniform ("DSpark implementation and evaluation"
 
   key      = (lo32(seed), hi32(seed))
   counter  = (j, b, (stream << 16) | i, offset)       offset < 2**32
-  stream 0 = draft Gumbel noise      (b = request, i = draft step, element v
-                                      uses word v & 3 of counter j = v >> 2)
+  stream 0 = draft noise, high halves (b = request, i = draft step)
+  stream 3 = draft noise, low halves  (same counters)
+             element v takes 16 bits from each stream, from counter j = v >> 3:
+             word (v & 7) >> 1, bits 0-15 for even v and 16-31 for odd v;
+             its 32-bit word is (high half << 16) | low half
+  (the split lets a sampler rule an element out from its high half alone,
+  since u, and so g, is increasing in the word)
   stream 1 = verify accept uniform   (i = draft position k, j = 0, word 0)
   stream 2 = verify resample         (i = position, j = 0, words 0 and 1)
 
@@ -39,6 +44,7 @@ S32 = np.uint64(32)
 STREAM_GUMBEL = 0
 STREAM_ACCEPT = 1
 STREAM_RESAMPLE = 2
+STREAM_GUMBEL_LO = 3
 
 
 def philox4x32_10(c0, c1, c2, c3, k0, k1):
@@ -87,13 +93,26 @@ def gumbel_from_word(w) -> np.ndarray:
     return -np.log(-np.log(u))
 
 
+def draft_halfword(seed: int, offset: int, b, i, v, stream: int) -> np.ndarray:
+    """16-bit piece of element v's draft word from `stream` (0: high half, 3: low half)."""
+    v = np.asarray(v, dtype=np.uint64)
+    words = philox_words(seed, offset, v >> np.uint64(3), b, stream, i)
+    sel = ((v & np.uint64(7)) >> np.uint64(1)).astype(np.int64)
+    w = np.where(sel == 0, words[0], np.where(sel == 1, words[1],
+                 np.where(sel == 2, words[2], words[3])))
+    shift = (v & np.uint64(1)) * np.uint64(16)
+    return (w >> shift) & np.uint64(0xFFFF)
+
+
+def draft_word(seed: int, offset: int, b, i, v) -> np.ndarray:
+    """32-bit draft-noise word of element v: (high half << 16) | low half."""
+    hi = draft_halfword(seed, offset, b, i, v, STREAM_GUMBEL)
+    lo = draft_halfword(seed, offset, b, i, v, STREAM_GUMBEL_LO)
+    return (hi << np.uint64(16)) | lo
+
+
 def draft_gumbel(seed: int, offset: int, b, i, V: int) -> np.ndarray:
     """Gumbel noise g[b, v] (float64) of draft step i for requests b (array) over v in [0, V)."""
     b = np.asarray(b, dtype=np.uint64).reshape(-1, 1)
     v = np.arange(V, dtype=np.uint64).reshape(1, -1)
-    j = v >> np.uint64(2)
-    words = philox_words(seed, offset, j, b, STREAM_GUMBEL, i)
-    sel = (v & np.uint64(3)).astype(np.int64)
-    w = np.where(sel == 0, words[0], np.where(sel == 1, words[1],
-                 np.where(sel == 2, words[2], words[3])))
-    return gumbel_from_word(w)
+    return gumbel_from_word(draft_word(seed, offset, b, i, v))

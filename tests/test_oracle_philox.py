@@ -128,9 +128,30 @@ def test_gumbel_distribution_and_bounds():
     assert 16.63 < gmax < 16.64 and -2.82 < gmin < -2.81
 
 
-def test_draft_gumbel_word_selection():
-    # element v uses word v & 3 of counter j = v >> 2
-    g = draft_gumbel(3, 4, np.array([2]), 5, 10)
-    for v in range(10):
-        w = philox_words(3, 4, v >> 2, 2, 0, 5)[v & 3]
-        assert g[0, v] == gumbel_from_word(w)
+def test_draft_gumbel_word_layout():
+    # element v: high half from stream 0 and low half from stream 3, both from counter
+    # v >> 3, word (v & 7) >> 1, bits 0-15 (even v) or 16-31 (odd v)
+    g = draft_gumbel(3, 4, np.array([2]), 5, 20)
+    for v in range(20):
+        hw = philox_words(3, 4, v >> 3, 2, 0, 5)[(v & 7) >> 1]
+        lw = philox_words(3, 4, v >> 3, 2, 3, 5)[(v & 7) >> 1]
+        sh = 16 * (v & 1)
+        word = (((int(hw) >> sh) & 0xFFFF) << 16) | ((int(lw) >> sh) & 0xFFFF)
+        assert g[0, v] == gumbel_from_word(np.uint64(word))
+
+
+def test_draft_words_uniform_and_halves_independent():
+    from oracle.philox import draft_word, draft_halfword
+    v = np.arange(200_000, dtype=np.uint64)
+    w = draft_word(9, 1, 4, 2, v)
+    counts, _ = np.histogram((w >> np.uint64(16)).astype(np.float64), bins=64, range=(0, 65536))
+    assert stats.chisquare(counts).pvalue > 0.01
+    counts, _ = np.histogram((w & np.uint64(0xFFFF)).astype(np.float64), bins=64, range=(0, 65536))
+    assert stats.chisquare(counts).pvalue > 0.01
+    hi = draft_halfword(9, 1, 4, 2, v, 0)
+    lo = draft_halfword(9, 1, 4, 2, v, 3)
+    joint = np.histogram2d((hi >> np.uint64(13)).astype(float), (lo >> np.uint64(13)).astype(float),
+                           bins=8, range=[[0, 8], [0, 8]])[0].ravel()
+    assert stats.chisquare(joint).pvalue > 0.01
+    # neighbouring elements get different words (no sharing of halves)
+    assert len(np.unique(w[:4096])) == 4096
