@@ -150,7 +150,7 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 }
 
 // Counter layout of this library: (j, b, (stream << 16) | i, offset).
-enum : uint32_t { kStreamGumbel = 0, kStreamAccept = 1, kStreamResample = 2 };
+enum : uint32_t { kStreamGumbel = 0, kStreamAccept = 1, kStreamResample = 2, kStreamGumbelLo = 3 };
 
 __device__ __forceinline__ uint4 philox_at(uint64_t seed, uint32_t offset, uint32_t j, uint32_t b,
                                            uint32_t stream, uint32_t i) {
@@ -167,6 +167,24 @@ __device__ __forceinline__ float uniform_from_word(uint32_t w) {
 __device__ __forceinline__ float gumbel_from_word(uint32_t w) {
     const float u = uniform_from_word(w);
     return -logf(-logf(u));
+}
+
+// Draft noise of element v: a 16-bit high half from stream 0 and a 16-bit low
+// half from stream 3, both from counter j = v >> 3, word (v & 7) >> 1, bits 0-15
+// for even v and 16-31 for odd v.  The uniform, and so the Gumbel variate, is
+// increasing in the 32-bit word (high << 16) | low, so the high half alone
+// bounds the variate.
+__device__ __forceinline__ uint32_t draft_half(uint4 w, uint32_t v) {
+    const uint32_t sel = (v & 7u) >> 1;
+    const uint32_t word = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
+    return (word >> (16u * (v & 1u))) & 0xFFFFu;
+}
+
+__device__ __forceinline__ uint32_t draft_word(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i,
+                                               uint32_t v) {
+    const uint32_t hi = draft_half(philox_at(seed, offset, v >> 3, b, kStreamGumbel, i), v);
+    const uint32_t lo = draft_half(philox_at(seed, offset, v >> 3, b, kStreamGumbelLo, i), v);
+    return (hi << 16) | lo;
 }
 
 // Every Gumbel variate produced above is below this bound: the largest u is

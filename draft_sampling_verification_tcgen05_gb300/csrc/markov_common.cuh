@@ -55,11 +55,8 @@ struct MarkovArgs {
 };
 
 __device__ __forceinline__ float gumbel_at(const MarkovArgs& a, int b, int i, int v) {
-    const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(b),
-                              kStreamGumbel, static_cast<uint32_t>(i));
-    const uint32_t sel = static_cast<uint32_t>(v) & 3u;
-    const uint32_t word = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
-    return gumbel_from_word(word);
+    return gumbel_from_word(draft_word(a.seed, a.offset, static_cast<uint32_t>(b), static_cast<uint32_t>(i),
+                                       static_cast<uint32_t>(v)));
 }
 
 __device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {

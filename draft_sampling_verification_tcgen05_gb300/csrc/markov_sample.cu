@@ -33,7 +33,7 @@ namespace {
 
 using namespace markov;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr size_t kW2CacheBytes = 144 * 1024;           // w2 slice kept in shared memory when it fits
 constexpr size_t kZStoreBytes = 32 * 1024;             // z rows kept in shared memory when they fit
@@ -45,42 +45,46 @@ template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// dot(w2 row, E row) over r, fp32 accumulation in k order.
+// dot(w2 row, E row) over r in fp32: four independent partial sums (k mod 8 in
+// {0,1}, {2,3}, {4,5}, {6,7} of each 16-byte piece) added at the end, so the
+// dependent FMA chain is a quarter as long.
 template <typename WT>
 __device__ __forceinline__ float bias_dot(const uint8_t* row, const float* e, int r) {
-    float acc = 0.f;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int k = 0;
     if constexpr (sizeof(WT) == 2) {
-        int k = 0;
         if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
             for (; k + 8 <= r; k += 8) {
                 const uint4 q = *reinterpret_cast<const uint4*>(row + 2 * k);
                 const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = __bfloat1622float2(h[j]);
-                    acc = fmaf(f.x, e[k + 2 * j], acc);
-                    acc = fmaf(f.y, e[k + 2 * j + 1], acc);
-                }
+                const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
+                const float2 f2 = __bfloat1622float2(h[2]), f3 = __bfloat1622float2(h[3]);
+                acc0 = fmaf(f0.x, e[k + 0], acc0);
+                acc1 = fmaf(f1.x, e[k + 2], acc1);
+                acc2 = fmaf(f2.x, e[k + 4], acc2);
+                acc3 = fmaf(f3.x, e[k + 6], acc3);
+                acc0 = fmaf(f0.y, e[k + 1], acc0);
+                acc1 = fmaf(f1.y, e[k + 3], acc1);
+                acc2 = fmaf(f2.y, e[k + 5], acc2);
+                acc3 = fmaf(f3.y, e[k + 7], acc3);
             }
         }
         for (; k < r; ++k)
-            acc = fmaf(__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(row)[k]), e[k], acc);
+            acc0 = fmaf(__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(row)[k]), e[k], acc0);
     } else {
-        int k = 0;
         if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
             for (; k + 4 <= r; k += 4) {
                 const float4 q = *reinterpret_cast<const float4*>(row + 4 * k);
-                acc = fmaf(q.x, e[k], acc);
-                acc = fmaf(q.y, e[k + 1], acc);
-                acc = fmaf(q.z, e[k + 2], acc);
-                acc = fmaf(q.w, e[k + 3], acc);
+                acc0 = fmaf(q.x, e[k], acc0);
+                acc1 = fmaf(q.y, e[k + 1], acc1);
+                acc2 = fmaf(q.z, e[k + 2], acc2);
+                acc3 = fmaf(q.w, e[k + 3], acc3);
             }
         }
-        for (; k < r; ++k) acc = fmaf(reinterpret_cast<const float*>(row)[k], e[k], acc);
+        for (; k < r; ++k) acc0 = fmaf(reinterpret_cast<const float*>(row)[k], e[k], acc0);
     }
-    return acc;
+    return (acc0 + acc1) + (acc2 + acc3);
 }
-
 
 __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long k, unsigned long long* red) {
     k = warp_max_u64(k);

@@ -67,18 +67,14 @@ __device__ __forceinline__ void tile_range(const TcArgs& t, int& lo, int& hi) {
     hi = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * t.n_tiles) / gridDim.x);
 }
 
-// One queued candidate: request c*16 + j, vocabulary entry v, scaled logit z.
-// Folds its perturbed value into this lane's running maximum for request j
-// (registers; the unrolled selects avoid both atomics and local memory).
-__device__ __forceinline__ void drain_candidate(const MarkovArgs& a, uint32_t e, float z, int c, int i,
-                                                unsigned long long (&best)[kChunk]) {
-    const int j = static_cast<int>(e >> 27);
-    const int v = static_cast<int>(e & 0x7FFFFFFu);
-    const float y = __fadd_rn(z, gumbel_at(a, c * kChunk + j, i, v));
-    const unsigned long long k = (y == y) ? argmax_key(y, static_cast<uint32_t>(v)) : 0ull;
-#pragma unroll
-    for (int jj = 0; jj < kChunk; ++jj)
-        if (jj == j && k > best[jj]) best[jj] = k;
+// Full noise of one element that its high half could not rule out (rare):
+// draws the low half, returns the argmax key of z + g (0 for NaN).  Kept out
+// of line so the unrolled test loop stays small.
+__device__ __noinline__ unsigned long long rare_candidate(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i,
+                                                          uint32_t v, float z, uint32_t hi) {
+    const uint32_t lo = draft_half(philox_at(seed, offset, v >> 3, b, kStreamGumbelLo, i), v);
+    const float y = __fadd_rn(z, gumbel_from_word((hi << 16) | lo));
+    return (y == y) ? argmax_key(y, v) : 0ull;
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -99,8 +95,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ float s_invT[256];
     __shared__ float s_lb[kGroups][kChunk];
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
-    __shared__ uint32_t s_qv[kEpiWarps][64];
-    __shared__ float s_qz[kEpiWarps][64];
+    __shared__ __align__(16) uint16_t s_hi[kEpiWarps][kChunk][32];    // high halves of a tile-chunk
+    __shared__ uint32_t s_mask[kEpiWarps][kChunk];                     // elements that pass the z test
+    __shared__ float s_gtab[256];                                      // bound on g per top byte
     __shared__ int s_ok;
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -143,6 +140,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         s_invT[b] = inv;
     }
     if (bad_t) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+    // s_gtab[k] bounds the variate of every word whose top byte is k: the variate of
+    // the largest such word (it increases with the word), plus a margin that covers
+    // logf's rounding; the top bin is capped by the global bound
+    for (int k = threadIdx.x; k < 256; k += kThreadsTC)
+        s_gtab[k] = k == 255 ? kGumbelMax : gumbel_from_word((static_cast<uint32_t>(k + 1) << 24) - 1u) + 1e-3f;
     {   // zero E once: padding rows (b >= B) stay zero for the whole call
         uint4* e4 = reinterpret_cast<uint4*>(Es);
         const int n16 = Bp * a.r * 2 / 16;
@@ -362,9 +364,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 }
                 named_bar_sync(kBarEpi, 32 * kEpiWarps);
 
-                // ---- pass 2 over this group's chunks: Gumbel noise only where z can still beat
-                //      the bound; surviving (request, v) pairs are compacted into a per-warp
-                //      queue so that Philox and the two logarithms run 32 lanes wide ----
+                // ---- pass 2 over this group's chunks: noise only where z can still beat the
+                //      bound.  The high halves of the noise words come 8 per Philox call (lane
+                //      l draws the counter of 8 consecutive entries for two requests); a table
+                //      bound on g from the top byte rules out almost every element, and only
+                //      the rest draw their low half and the exact variate ----
                 for (int ro = 0; ro < rounds; ++ro) {
                     const int c = ro * kGroups + grp;
                     if (c >= n_chunks) continue;
@@ -382,44 +386,55 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 #pragma unroll
                     for (int j = 0; j < kChunk; ++j) any |= lb[j] < INFINITY;
                     if (any && !dead) {
-                        uint32_t* qv = s_qv[epi];
-                        float* qz = s_qz[epi];
-                        int qn = 0;
+                        uint16_t (*hs)[32] = s_hi[epi];
+                        uint32_t* sm = s_mask[epi];
                         for (int tl = 0; tl < nt; ++tl) {
-                            const int v = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32 + lane);
+                            const int v0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32);
+                            const int v = v0 + static_cast<int>(lane);
                             const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
                             uint32_t r[kChunk];
                             tmem_ld16(taddr, r);
                             tmem_wait_ld();
+                            uint32_t m[kChunk];
+                            uint32_t anym = 0;
 #pragma unroll
                             for (int j = 0; j < kChunk; ++j) {
-                                const float z = __uint_as_float(r[j]);
-                                const bool pred = v < a.V && __fadd_rn(z, kGumbelMax) >= lb[j];
-                                const uint32_t mask = __ballot_sync(0xFFFFFFFFu, pred);
-                                if (mask == 0u) continue;
-                                if (pred) {
-                                    const int pos = qn + __popc(mask & ((1u << lane) - 1u));
-                                    qv[pos] = (static_cast<uint32_t>(j) << 27) | static_cast<uint32_t>(v);
-                                    qz[pos] = z;
-                                }
-                                qn += __popc(mask);
-                                if (qn >= 32) {
-                                    __syncwarp();
-                                    const uint32_t e = qv[lane];
-                                    const float ze = qz[lane];
-                                    const bool mv = static_cast<int>(lane) < qn - 32;
-                                    uint32_t e2 = 0;
-                                    float z2 = 0.f;
-                                    if (mv) { e2 = qv[32 + lane]; z2 = qz[32 + lane]; }
-                                    __syncwarp();
-                                    if (mv) { qv[lane] = e2; qz[lane] = z2; }
-                                    qn -= 32;
-                                    drain_candidate(a, e, ze, c, i, best);
+                                const bool pass = v < a.V && __fadd_rn(__uint_as_float(r[j]), kGumbelMax) >= lb[j];
+                                m[j] = __ballot_sync(0xFFFFFFFFu, pass);
+                                anym |= m[j];
+                                if (lane == 0) sm[j] = m[j];
+                            }
+                            if (anym == 0u) continue;
+                            __syncwarp();
+                            // lane l: counter (v0 >> 3) + (l & 3) for requests (l >> 2) and (l >> 2) + 8
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int jj = static_cast<int>(lane >> 2) + 8 * h;
+                                const int q = static_cast<int>(lane & 3u);
+                                if ((sm[jj] >> (8 * q)) & 0xFFu) {
+                                    const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>((v0 >> 3) + q),
+                                                              static_cast<uint32_t>(c * kChunk + jj), kStreamGumbel,
+                                                              static_cast<uint32_t>(i));
+                                    // 8 high halves in element order (even entry in the low 16 bits)
+                                    *reinterpret_cast<uint4*>(&hs[jj][8 * q]) = w;
                                 }
                             }
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < kChunk; ++j) {
+                                if ((m[j] >> lane) & 1u) {
+                                    const float z = __uint_as_float(r[j]);
+                                    const uint32_t hi = hs[j][lane];
+                                    if (__fadd_rn(z, s_gtab[hi >> 8]) >= lb[j]) {
+                                        const unsigned long long k =
+                                            rare_candidate(a.seed, a.offset, static_cast<uint32_t>(c * kChunk + j),
+                                                           static_cast<uint32_t>(i), static_cast<uint32_t>(v), z, hi);
+                                        if (k > best[j]) best[j] = k;
+                                    }
+                                }
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
-                        if (static_cast<int>(lane) < qn) drain_candidate(a, qv[lane], qz[lane], c, i, best);
                     }
 #pragma unroll
                     for (int j = 0; j < kChunk; ++j) {
