@@ -37,12 +37,12 @@ namespace {
 
 using namespace markov;
 
-constexpr int kGroups = 2;
+constexpr int kGroups = 4;
 constexpr int kEpiWarps = 4 * kGroups;
 constexpr int kThreadsTC = 32 * (2 + kEpiWarps);
 constexpr uint32_t kStepThreads = 32 * (1 + kEpiWarps);
-constexpr int kW2Stages = 8;                    // upper bound; the launcher picks 4 or 8
-constexpr int kLStages = 5;                      // upper bound per epilogue group; the launcher picks 3 or 5
+constexpr int kW2Stages = 4;                    // w2 ring depth (the L2 stream is bandwidth-, not latency-bound)
+constexpr int kLStages = 3;                      // upper bound per epilogue group; the launcher picks 2 or 3
 constexpr int kTileV = 128;
 constexpr int kChunk = 16;                       // requests per epilogue chunk
 constexpr int kMaxLocalTiles = 32;
@@ -95,6 +95,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ float s_invT[256];
     __shared__ float s_lb[kGroups][kChunk];
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
+    __shared__ unsigned long long s_best[kGroups][kChunk];
     __shared__ __align__(16) uint16_t s_hi[kEpiWarps][kChunk][32];    // high halves of a tile-chunk
     __shared__ uint32_t s_mask[kEpiWarps][kChunk];                     // elements that pass the z test
     __shared__ float s_gtab[256];                                      // bound on g per top byte
@@ -376,15 +377,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                         const int b = c * kChunk + static_cast<int>(lane);
                         s_lb[grp][lane] = (b < a.B && s_invT[b] > 0.f) ? float_from_order_bits(__ldcg(lbs + b))
                                                                         : INFINITY;
+                        s_best[grp][lane] = 0ull;
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
-                    float lb[kChunk];
-                    unsigned long long best[kChunk];
-#pragma unroll
-                    for (int j = 0; j < kChunk; ++j) { lb[j] = s_lb[grp][j]; best[j] = 0ull; }
                     bool any = false;
 #pragma unroll
-                    for (int j = 0; j < kChunk; ++j) any |= lb[j] < INFINITY;
+                    for (int j = 0; j < kChunk; ++j) any |= s_lb[grp][j] < INFINITY;
                     if (any && !dead) {
                         uint16_t (*hs)[32] = s_hi[epi];
                         uint32_t* sm = s_mask[epi];
@@ -399,7 +397,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             uint32_t anym = 0;
 #pragma unroll
                             for (int j = 0; j < kChunk; ++j) {
-                                const bool pass = v < a.V && __fadd_rn(__uint_as_float(r[j]), kGumbelMax) >= lb[j];
+                                const bool pass = v < a.V && __fadd_rn(__uint_as_float(r[j]), kGumbelMax) >= s_lb[grp][j];
                                 m[j] = __ballot_sync(0xFFFFFFFFu, pass);
                                 anym |= m[j];
                                 if (lane == 0) sm[j] = m[j];
@@ -425,27 +423,21 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 if ((m[j] >> lane) & 1u) {
                                     const float z = __uint_as_float(r[j]);
                                     const uint32_t hi = hs[j][lane];
-                                    if (__fadd_rn(z, s_gtab[hi >> 8]) >= lb[j]) {
+                                    if (__fadd_rn(z, s_gtab[hi >> 8]) >= s_lb[grp][j]) {
                                         const unsigned long long k =
                                             rare_candidate(a.seed, a.offset, static_cast<uint32_t>(c * kChunk + j),
                                                            static_cast<uint32_t>(i), static_cast<uint32_t>(v), z, hi);
-                                        if (k > best[j]) best[j] = k;
+                                        if (k != 0ull) atomicMax(&s_best[grp][j], k);   // rare: survivors only
                                     }
                                 }
                             }
                             __syncwarp();
                         }
                     }
-#pragma unroll
-                    for (int j = 0; j < kChunk; ++j) {
-                        const unsigned long long k = warp_max_u64(best[j]);
-                        if (lane == 0) s_part[grp][quad][j] = k;
-                    }
                     named_bar_sync(kBarGroup0 + grp, 128);
                     if (grp_lead && lane < kChunk) {
                         const int b = c * kChunk + static_cast<int>(lane);
-                        unsigned long long k = 0;
-                        for (int q = 0; q < 4; ++q) k = s_part[grp][q][lane] > k ? s_part[grp][q][lane] : k;
+                        const unsigned long long k = s_best[grp][lane];
                         if (b < a.B && k != 0ull) {
                             atomicMax(slot + b, k);
                             const uint32_t vb = key_index(k);
@@ -482,8 +474,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 // Ring depths: deep w2 ring (L2 stream) when the E operand leaves room.
 void tc_rings(int B_pad, int r, int* w2_stages, int* l_stages) {
     const bool small_e = static_cast<size_t>(B_pad) * r * 2 <= 32 * 1024;
-    *w2_stages = small_e ? 8 : 4;
-    *l_stages = small_e ? 3 : 5;
+    *w2_stages = kW2Stages;
+    *l_stages = small_e ? 3 : 2;
 }
 
 size_t tc_smem_bytes(int B_pad, int r) {
