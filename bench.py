@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--workload", default="qwen3_8b_single", choices=sorted(DRAFT_CONFIGS))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the four calls eagerly each step")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle sample")
     return ap.parse_args()
@@ -229,6 +230,26 @@ def run_gpu(args):
         if st not in (0,):
             raise RuntimeError(f"device status {st} bits {bits:#x} after warm-up")
 
+    # The step is replayed as one CUDA graph (all buffers at fixed addresses, as a serving
+    # engine runs its draft step); an eager pass with events between the calls gives the
+    # per-kernel times used for the roofline.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            graph.replay()
+        torch.cuda.synchronize()
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
     # ---------------- timed region (device-resident inputs) ----------------
     if dist is not None:
         dist.barrier()
@@ -238,7 +259,12 @@ def run_gpu(args):
         wall0 = time.perf_counter()
         for k in range(args.steps):
             flush.fill_(float(k))                 # L2 flush between timed steps (not timed)
-            step(k)
+            if graph is not None:
+                g0[k].record(stream)
+                graph.replay()
+                g1[k].record(stream)
+            else:
+                step(k)
         torch.cuda.synchronize()
         wall1 = time.perf_counter()
         wall = wall1 - wall0
@@ -246,9 +272,18 @@ def run_gpu(args):
         time.sleep(0.3)
     if dist is not None:
         dist.barrier()
+    if graph is not None:
+        # per-kernel times: the same K steps run eagerly with events between the calls
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            step(k)
+        torch.cuda.synchronize()
     per = np.array([[ev[k][j].elapsed_time(ev[k][j + 1]) for j in range(4)] for k in range(args.steps)])
-    step_ms = float(per.sum(axis=1).mean())
     kernel_ms = per.mean(axis=0)                  # draft_logits, markov, verify, schedule
+    if graph is not None:
+        step_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(g0, g1)]))
+    else:
+        step_ms = float(per.sum(axis=1).mean())
     if dist is not None:
         t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -348,6 +383,8 @@ def run_gpu(args):
                             "unit": "GB/s", "frac": markov_bytes / (kernel_ms[1] / 1e3) / 1e9 / hbm_peak},
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
+        "step_launch": "one CUDA graph replay per step" if graph is not None else "four eager calls per step",
+        "kernel_ms_note": "per-kernel CUDA-event times from an eager pass over the same K steps",
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }

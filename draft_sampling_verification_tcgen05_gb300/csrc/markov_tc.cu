@@ -67,6 +67,19 @@ __device__ __forceinline__ void tile_range(const TcArgs& t, int& lo, int& hi) {
     hi = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * t.n_tiles) / gridDim.x);
 }
 
+// Can an element whose noise word has high half `hi` reach a perturbed value
+// d above its scaled logit?  Its uniform is below u_max = (hi + 1) / 2^16 and g
+// increases with u, so if u_max < exp(-exp(-(d - 1e-3))) then g < d - 1e-3 and
+// the element stays strictly below the bound.  The fast exponentials carry a
+// relative error far below the 1e-5 slack, and 1e-3 covers the rounding of g
+// and of z + g, so a "no" is always right.
+__device__ __forceinline__ bool high_half_can_reach(uint32_t hi, float d) {
+    if (d < 2.0f) return true;                               // too close to the bound: draw exactly
+    const float thr = __expf(-__expf(-(d - 1e-3f))) * (1.0f - 1e-5f);
+    const float u_max = static_cast<float>(hi + 1u) * 0x1p-16f;
+    return u_max >= thr;
+}
+
 // Full noise of one element that its high half could not rule out (rare):
 // draws the low half, returns the argmax key of z + g (0 for NaN).  Kept out
 // of line so the unrolled test loop stays small.
@@ -98,7 +111,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ unsigned long long s_best[kGroups][kChunk];
     __shared__ __align__(16) uint16_t s_hi[kEpiWarps][kChunk][32];    // high halves of a tile-chunk
     __shared__ uint32_t s_mask[kEpiWarps][kChunk];                     // elements that pass the z test
-    __shared__ float s_gtab[256];                                      // bound on g per top byte
     __shared__ int s_ok;
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -141,11 +153,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         s_invT[b] = inv;
     }
     if (bad_t) set_status(a.ws, DSPARK_STATUS_NUMERIC);
-    // s_gtab[k] bounds the variate of every word whose top byte is k: the variate of
-    // the largest such word (it increases with the word), plus a margin that covers
-    // logf's rounding; the top bin is capped by the global bound
-    for (int k = threadIdx.x; k < 256; k += kThreadsTC)
-        s_gtab[k] = k == 255 ? kGumbelMax : gumbel_from_word((static_cast<uint32_t>(k + 1) << 24) - 1u) + 1e-3f;
     {   // zero E once: padding rows (b >= B) stay zero for the whole call
         uint4* e4 = reinterpret_cast<uint4*>(Es);
         const int n16 = Bp * a.r * 2 / 16;
@@ -367,9 +374,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 
                 // ---- pass 2 over this group's chunks: noise only where z can still beat the
                 //      bound.  The high halves of the noise words come 8 per Philox call (lane
-                //      l draws the counter of 8 consecutive entries for two requests); a table
-                //      bound on g from the top byte rules out almost every element, and only
-                //      the rest draw their low half and the exact variate ----
+                //      l draws the counter of 8 consecutive entries for two requests); a bound
+                //      on g from the 16-bit high half rules out almost every element, and
+                //      only the rest draw their low half and the exact variate ----
                 for (int ro = 0; ro < rounds; ++ro) {
                     const int c = ro * kGroups + grp;
                     if (c >= n_chunks) continue;
@@ -423,7 +430,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 if ((m[j] >> lane) & 1u) {
                                     const float z = __uint_as_float(r[j]);
                                     const uint32_t hi = hs[j][lane];
-                                    if (__fadd_rn(z, s_gtab[hi >> 8]) >= s_lb[grp][j]) {
+                                    if (high_half_can_reach(hi, __fsub_rn(s_lb[grp][j], z))) {
                                         const unsigned long long k =
                                             rare_candidate(a.seed, a.offset, static_cast<uint32_t>(c * kChunk + j),
                                                            static_cast<uint32_t>(i), static_cast<uint32_t>(v), z, hi);

@@ -12,7 +12,8 @@
 //      and 64-bit keys ((~survival bits) << 32 | b*N+k), in index order
 //   2. stable LSD radix sort of the keys on their upper 32 bits (4 passes of
 //      8 bits; rounds of 1024 keys ranked with warp match + per-warp digit
-//      counts), ping-ponging between two workspace buffers (L2-resident)
+//      counts), ping-ponging between two workspace buffers (L2-resident);
+//      pools of at most 1024 candidates are ranked by counting, in shared memory
 //   3. if K is to be chosen: block-wide prefix sum of floor(s * 2^32) over the
 //      sorted order, f(K) = float64(B * 2^32 + prefix) * SPS[K-1] for every K,
 //      block argmax with ties to the smallest K
@@ -89,7 +90,10 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
     const int B = a.B, N = a.N;
     const int n = B * N;
 
-    // ---- 1. survival chain and keys ----
+    // ---- 1. survival chain and keys (small pools keep their keys in shared memory) ----
+    const bool small = n <= kThreads;
+    unsigned long long* sk = reinterpret_cast<unsigned long long*>(&s_cnt[0][0]);   // [2][kThreads] when small
+    unsigned long long* keys = small ? sk : a.keys0;
     bool bad = false;
     for (int b = tid; b < B; b += kThreads) {
         float s = 1.f;
@@ -98,33 +102,31 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
             const float c = clamp_prob(a.c[idx], bad);
             s = (k == 0) ? c : __fmul_rn(s, c);
             a.survival[idx] = s;
-            a.keys0[idx] = (static_cast<unsigned long long>(0xFFFFFFFFu - __float_as_uint(s)) << 32) |
-                           static_cast<unsigned long long>(idx);
+            keys[idx] = (static_cast<unsigned long long>(0xFFFFFFFFu - __float_as_uint(s)) << 32) |
+                        static_cast<unsigned long long>(idx);
         }
         a.lengths[b] = 0;
     }
     if (bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
-    for (int i = tid; i < kWarps * kRadix; i += kThreads) (&s_cnt[0][0])[i] = 0;
+    if (!small)
+        for (int i = tid; i < kWarps * kRadix; i += kThreads) (&s_cnt[0][0])[i] = 0;
     __syncthreads();
 
     // ---- 2. sort: keys are unique (the index is part of the key) ----
     unsigned long long* src = a.keys0;
     unsigned long long* dst = a.keys1;
-    if (n <= kThreads) {
-        // small pools: rank of each key = number of smaller keys (one key per thread)
-        unsigned long long* sk = reinterpret_cast<unsigned long long*>(&s_cnt[0][0]);
-        const unsigned long long mine = tid < n ? src[tid] : 0ull;
-        if (tid < n) sk[tid] = mine;
-        __syncthreads();
+    if (small) {
+        // rank of each key = number of smaller keys (one key per thread), all in shared memory
+        const unsigned long long mine = tid < n ? sk[tid] : 0ull;
         if (tid < n) {
             int rank = 0;
             for (int j = 0; j < n; ++j) rank += sk[j] < mine ? 1 : 0;
-            dst[rank] = mine;
+            sk[kThreads + rank] = mine;
         }
         __syncthreads();
-        src = dst;
+        src = sk + kThreads;
     }
-    for (int pass = 0; pass < (n <= kThreads ? 0 : 4); ++pass) {
+    for (int pass = 0; pass < (small ? 0 : 4); ++pass) {
         const int shift = 32 + 8 * pass;
         if (tid < kRadix) s_base[tid] = 0;
         __syncthreads();
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
         src = dst;
         dst = t;
     }
-    // sorted keys are in src (keys0 after the 4 radix passes, keys1 after the rank sort)
+    // sorted keys are in src (keys0 after the 4 radix passes, shared memory after the rank sort)
 
     // ---- 3. capacity K ----
     if (a.K_in >= 0) {
