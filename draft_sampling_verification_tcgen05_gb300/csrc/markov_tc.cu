@@ -109,6 +109,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ float s_lb[kGroups][kChunk];
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
     __shared__ unsigned long long s_best[kGroups][kChunk];
+    __shared__ float s_gtab[256];                                      // bound on g per top byte
     __shared__ __align__(16) uint16_t s_hi[kEpiWarps][kChunk][32];    // high halves of a tile-chunk
     __shared__ uint32_t s_mask[kEpiWarps][kChunk];                     // elements that pass the z test
     __shared__ int s_ok;
@@ -153,6 +154,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         s_invT[b] = inv;
     }
     if (bad_t) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+    // s_gtab[k] bounds the variate of every word whose top byte is k: the variate of
+    // the largest such word (it increases with the word) plus a margin for logf's
+    // rounding; the top bin is capped by the global bound
+    for (int k = threadIdx.x; k < 256; k += kThreadsTC)
+        s_gtab[k] = k == 255 ? kGumbelMax : gumbel_from_word((static_cast<uint32_t>(k + 1) << 24) - 1u) + 1e-3f;
     {   // zero E once: padding rows (b >= B) stay zero for the whole call
         uint4* e4 = reinterpret_cast<uint4*>(Es);
         const int n16 = Bp * a.r * 2 / 16;
@@ -374,9 +380,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 
                 // ---- pass 2 over this group's chunks: noise only where z can still beat the
                 //      bound.  The high halves of the noise words come 8 per Philox call (lane
-                //      l draws the counter of 8 consecutive entries for two requests); a bound
-                //      on g from the 16-bit high half rules out almost every element, and
-                //      only the rest draw their low half and the exact variate ----
+                //      l draws the counter of 8 consecutive entries for two requests); a table
+                //      bound on g from the top byte, then the exact bound from the 16-bit
+                //      high half, rule out almost every element; only the rest draw their
+                //      low half and the exact variate ----
                 for (int ro = 0; ro < rounds; ++ro) {
                     const int c = ro * kGroups + grp;
                     if (c >= n_chunks) continue;
@@ -425,16 +432,28 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 }
                             }
                             __syncwarp();
+                            // straight-line: a table bound on g from the top byte of the high half
+                            uint32_t need = 0;
 #pragma unroll
                             for (int j = 0; j < kChunk; ++j) {
-                                if ((m[j] >> lane) & 1u) {
-                                    const float z = __uint_as_float(r[j]);
-                                    const uint32_t hi = hs[j][lane];
-                                    if (high_half_can_reach(hi, __fsub_rn(s_lb[grp][j], z))) {
-                                        const unsigned long long k =
-                                            rare_candidate(a.seed, a.offset, static_cast<uint32_t>(c * kChunk + j),
-                                                           static_cast<uint32_t>(i), static_cast<uint32_t>(v), z, hi);
-                                        if (k != 0ull) atomicMax(&s_best[grp][j], k);   // rare: survivors only
+                                const uint32_t hi = hs[j][lane];
+                                const bool p = ((m[j] >> lane) & 1u) &&
+                                               __fadd_rn(__uint_as_float(r[j]), s_gtab[hi >> 8]) >= s_lb[grp][j];
+                                need |= (p ? 1u : 0u) << j;
+                            }
+                            // rare: the full 16-bit bound, then the exact draw
+                            if (__any_sync(0xFFFFFFFFu, need != 0u)) {
+#pragma unroll
+                                for (int j = 0; j < kChunk; ++j) {
+                                    if ((need >> j) & 1u) {
+                                        const float z = __uint_as_float(r[j]);
+                                        const uint32_t hi = hs[j][lane];
+                                        if (high_half_can_reach(hi, __fsub_rn(s_lb[grp][j], z))) {
+                                            const unsigned long long k =
+                                                rare_candidate(a.seed, a.offset, static_cast<uint32_t>(c * kChunk + j),
+                                                               static_cast<uint32_t>(i), static_cast<uint32_t>(v), z, hi);
+                                            if (k != 0ull) atomicMax(&s_best[grp][j], k);
+                                        }
                                     }
                                 }
                             }

@@ -7,7 +7,7 @@
 // curve is jagged, so every K is evaluated; K may also be fixed ahead of time
 // and only the fill done now.  No token value is read at any point.
 //
-// Steps (one block of 1024 threads):
+// Steps (one block of 1024 threads, 256 for pools of at most 256 candidates):
 //   1. survival chain per request (fp32, round to nearest, no contraction)
 //      and 64-bit keys ((~survival bits) << 32 | b*N+k), in index order
 //   2. stable LSD radix sort of the keys on their upper 32 bits (4 passes of
@@ -24,8 +24,6 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 constexpr int kRadix = 256;
 
 struct ScheduleArgs {
@@ -61,7 +59,7 @@ __device__ unsigned long long block_excl_scan_u64(unsigned long long x, unsigned
     if (lane == 31) sm[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        unsigned long long w = sm[lane];
+        unsigned long long w = lane < blockDim.x / 32 ? sm[lane] : 0ull;
         unsigned long long wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -76,11 +74,13 @@ __device__ unsigned long long block_excl_scan_u64(unsigned long long x, unsigned
     return sm[warp] + incl - x;
 }
 
+template <int kThreads>
 __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
+    constexpr int kWarps = kThreads / 32;
     __shared__ uint32_t s_cnt[kWarps][kRadix];
     __shared__ uint32_t s_base[kRadix];
     __shared__ uint32_t s_tmp[kRadix];
-    __shared__ unsigned long long s_scan[kWarps + 1];
+    __shared__ unsigned long long s_scan[33];                 // 32 warp slots + total
     __shared__ double s_bf[kWarps];
     __shared__ int s_bk[kWarps];
     __shared__ int s_K;
@@ -269,7 +269,11 @@ dspark_status launch_schedule(const float* cond_accept, const double* sps, int S
     a.B = B;
     a.N = N;
     a.K_in = K_in;
-    schedule_kernel<<<1, kThreads, 0, stream>>>(a);
+    // one block: 256 threads are plenty for pools of up to 256 candidates
+    if (static_cast<long long>(B) * N <= 256)
+        schedule_kernel<256><<<1, 256, 0, stream>>>(a);
+    else
+        schedule_kernel<1024><<<1, 1024, 0, stream>>>(a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "launch(schedule)");
     return DSPARK_OK;
