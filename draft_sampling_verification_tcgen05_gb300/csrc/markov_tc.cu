@@ -41,7 +41,7 @@ constexpr int kGroups = 4;
 constexpr int kEpiWarps = 4 * kGroups;
 constexpr int kThreadsTC = 32 * (2 + kEpiWarps);
 constexpr uint32_t kStepThreads = 32 * (1 + kEpiWarps);
-constexpr int kW2Stages = 4;                    // w2 ring depth (the L2 stream is bandwidth-, not latency-bound)
+constexpr int kW2Stages = 6;                    // upper bound of the w2 ring (the stream from L2 is bound by bytes in flight)
 constexpr int kLStages = 3;                      // upper bound per epilogue group; the launcher picks 2 or 3
 constexpr int kTileV = 128;
 constexpr int kChunk = 16;                       // requests per epilogue chunk
@@ -182,7 +182,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
             uint32_t wph = 0, lph[kGroups];
             for (int g = 0; g < kGroups; ++g) { ls[g] = 0; lph[g] = 0; }
             bool ok = true;
+            // the base logits of a step are independent of the sampled tokens: pull them
+            // into L2 one step ahead, so the shared-memory ring only covers L2 latency
+            for (int tl = 0; tl < nt; ++tl)
+                for (int c = 0; c < n_chunks; ++c)
+                    tma_prefetch_l2_3d(&tmL, (tile_lo + tl) * kTileV, 0, c * kChunk);
             for (int i = 0; i < a.N && ok; ++i) {
+                if (i + 1 < a.N)
+                    for (int tl = 0; tl < nt; ++tl)
+                        for (int c = 0; c < n_chunks; ++c)
+                            tma_prefetch_l2_3d(&tmL, (tile_lo + tl) * kTileV, i + 1, c * kChunk);
                 for (int ro = 0; ro < rounds && ok; ++ro) {
                     for (int tl = 0; tl < nt && ok; ++tl) {
                         const int v0 = (tile_lo + tl) * kTileV;
@@ -500,8 +509,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 // Ring depths: deep w2 ring (L2 stream) when the E operand leaves room.
 void tc_rings(int B_pad, int r, int* w2_stages, int* l_stages) {
     const bool small_e = static_cast<size_t>(B_pad) * r * 2 <= 32 * 1024;
-    *w2_stages = kW2Stages;
-    *l_stages = small_e ? 3 : 2;
+    *w2_stages = small_e ? 6 : 4;
+    *l_stages = 2;
 }
 
 size_t tc_smem_bytes(int B_pad, int r) {
