@@ -8,15 +8,17 @@
 // tiles [tile_lo, tile_hi) of 128 entries for the whole call.
 //   warp 0        one thread streams, ahead of use and across steps, the w2
 //                 tiles of the block (TMA, 128-byte swizzle, kept in L2 with
-//                 evict_last) and the base-logit tiles [16 requests x 128 v]
-//                 (3-D TMA, evict_first) into shared-memory rings
+//                 evict_last) into a shared-memory ring
+//   last warp     one thread prefetches each step's base logits into L2 a step
+//                 ahead and streams the tiles [16 requests x 128 v] (3-D TMA,
+//                 evict_first) into one ring per epilogue group
 //   warp 1        allocates tensor memory; per step one thread issues, for
 //                 every local tile, tcgen05.mma (M=128 vocab rows, N=B rounded
 //                 to 16, K=16) with A = w2 tile and B = E = w1[prev] (gathered
 //                 by the block into a swizzled shared-memory operand), into its
 //                 own TMEM columns
-//   warps 2..9    epilogue in two groups of four warps (one per TMEM lane
-//                 quadrant); group g handles request chunks g, g+2, ...:
+//   warps 2..17   epilogue in four groups of four warps (one per TMEM lane
+//                 quadrant); group g handles request chunks g, g+4, ...:
 //                 pass 1   bias (tcgen05.ld) + base logit -> z = (base + bias)/T,
 //                          written back in place (tcgen05.st): TMEM holds the
 //                          block's whole [tiles x 128, B] slab of z for the step;
@@ -39,7 +41,8 @@ using namespace markov;
 
 constexpr int kGroups = 4;
 constexpr int kEpiWarps = 4 * kGroups;
-constexpr int kThreadsTC = 32 * (2 + kEpiWarps);
+constexpr int kLProdWarp = 2 + kEpiWarps;                    // last warp: base-logit producer
+constexpr int kThreadsTC = 32 * (3 + kEpiWarps);
 constexpr uint32_t kStepThreads = 32 * (1 + kEpiWarps);
 constexpr int kW2Stages = 6;                    // upper bound of the w2 ring (the stream from L2 is bound by bytes in flight)
 constexpr int kLStages = 3;                      // upper bound per epilogue group; the launcher picks 2 or 3
@@ -175,11 +178,42 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- producer: w2 and base-logit tiles for every step ----------------
+            // ---------------- w2 producer: the block's w2 tiles, every step ----------------
             const uint64_t pol_keep = l2_policy_evict_last();
+            int ws = 0;
+            uint32_t wph = 0;
+            bool ok = true;
+            for (int i = 0; i < a.N && ok; ++i) {
+                for (int tl = 0; tl < nt && ok; ++tl) {
+                    const int v0 = (tile_lo + tl) * kTileV;
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        if (!mbar_wait(&bar_w2_empty[ws], wph ^ 1u, a.ws, a.timeout_ns, kWaitProducer)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bar_w2_full[ws], kW2StageBytes);
+                        tma_load_2d(w2s + ws * kW2StageBytes, &tmW2, kb * 64, v0, &bar_w2_full[ws], pol_keep);
+                        if (++ws == t.w2_stages) { ws = 0; wph ^= 1u; }
+                    }
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the block exits: stages before the
+                // ring position were last filled in the current phase, the rest one phase
+                // earlier (or never, which reads as complete)
+                const long long t0 = global_ns();
+                for (int s = 0; s < t.w2_stages; ++s)
+                    while (!mbar_try_wait(&bar_w2_full[s], s < ws ? wph : (wph ^ 1u)) &&
+                           global_ns() - t0 < a.timeout_ns) {
+                    }
+            }
+        }
+    } else if (warp == kLProdWarp) {
+        if (lane == 0) {
+            // ---------------- logit producer: base-logit tiles for every step ----------------
             const uint64_t pol_stream = l2_policy_evict_first();
-            int ws = 0, ls[kGroups];
-            uint32_t wph = 0, lph[kGroups];
+            int ls[kGroups];
+            uint32_t lph[kGroups];
             for (int g = 0; g < kGroups; ++g) { ls[g] = 0; lph[g] = 0; }
             bool ok = true;
             // the base logits of a step are independent of the sampled tokens: pull them
@@ -195,17 +229,6 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 for (int ro = 0; ro < rounds && ok; ++ro) {
                     for (int tl = 0; tl < nt && ok; ++tl) {
                         const int v0 = (tile_lo + tl) * kTileV;
-                        if (ro == 0) {
-                            for (int kb = 0; kb < kblocks; ++kb) {
-                                if (!mbar_wait(&bar_w2_empty[ws], wph ^ 1u, a.ws, a.timeout_ns, kWaitProducer)) {
-                                    ok = false;
-                                    break;
-                                }
-                                mbar_arrive_expect_tx(&bar_w2_full[ws], kW2StageBytes);
-                                tma_load_2d(w2s + ws * kW2StageBytes, &tmW2, kb * 64, v0, &bar_w2_full[ws], pol_keep);
-                                if (++ws == t.w2_stages) { ws = 0; wph ^= 1u; }
-                            }
-                        }
                         for (int g = 0; g < kGroups && ok; ++g) {
                             const int c = ro * kGroups + g;
                             if (c >= n_chunks) continue;
@@ -222,14 +245,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 }
             }
             if (!ok) {
-                // let copies already issued land before the block exits: stages before the
-                // ring position were last filled in the current phase, the rest one phase
-                // earlier (or never, which reads as complete)
                 const long long t0 = global_ns();
-                for (int s = 0; s < t.w2_stages; ++s)
-                    while (!mbar_try_wait(&bar_w2_full[s], s < ws ? wph : (wph ^ 1u)) &&
-                           global_ns() - t0 < a.timeout_ns) {
-                    }
                 for (int g = 0; g < kGroups; ++g)
                     for (int s = 0; s < t.l_stages; ++s)
                         while (!mbar_try_wait(&bar_L_full[g][s], s < ls[g] ? lph[g] : (lph[g] ^ 1u)) &&
