@@ -9,9 +9,8 @@
 //   warp 0        one thread streams, ahead of use and across steps, the w2
 //                 tiles of the block (TMA, 128-byte swizzle, kept in L2 with
 //                 evict_last) into a shared-memory ring
-//   last warp     one thread prefetches each step's base logits into L2 a step
-//                 ahead and streams the tiles [16 requests x 128 v] (3-D TMA,
-//                 evict_first) into one ring per epilogue group
+//   last warp     one thread streams the base-logit tiles [16 requests x 128 v]
+//                 (3-D TMA, evict_first) into one ring per epilogue group
 //   warp 1        allocates tensor memory; per step one thread issues, for
 //                 every local tile, tcgen05.mma (M=128 vocab rows, N=B rounded
 //                 to 16, K=16) with A = w2 tile and B = E = w1[prev] (gathered
@@ -216,16 +215,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
             uint32_t lph[kGroups];
             for (int g = 0; g < kGroups; ++g) { ls[g] = 0; lph[g] = 0; }
             bool ok = true;
-            // the base logits of a step are independent of the sampled tokens: pull them
-            // into L2 one step ahead, so the shared-memory ring only covers L2 latency
-            for (int tl = 0; tl < nt; ++tl)
-                for (int c = 0; c < n_chunks; ++c)
-                    tma_prefetch_l2_3d(&tmL, (tile_lo + tl) * kTileV, 0, c * kChunk);
+            // (no L2 prefetch a step ahead: w2 must stay L2-resident across steps, and a
+            // second step of logits in L2 would push it out)
             for (int i = 0; i < a.N && ok; ++i) {
-                if (i + 1 < a.N)
-                    for (int tl = 0; tl < nt; ++tl)
-                        for (int c = 0; c < n_chunks; ++c)
-                            tma_prefetch_l2_3d(&tmL, (tile_lo + tl) * kTileV, i + 1, c * kChunk);
                 for (int ro = 0; ro < rounds && ok; ++ro) {
                     for (int tl = 0; tl < nt && ok; ++tl) {
                         const int v0 = (tile_lo + tl) * kTileV;
@@ -264,7 +256,12 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         int w2st = 0, lsg = 0;
         uint32_t w2ph = 0, lphg = 0;
         bool alive = true, dead = false, nan_seen = false;
-        const uint32_t idesc = mma_idesc(128, Bp, false);
+        // Bias MMAs of one tile accumulate into one region, so a single narrow-N chain is
+        // latency-bound; split the requests into two halves (two independent chains in
+        // adjacent TMEM columns, the same layout) and interleave them.
+        const int n_half = (Bp % 32 == 0) ? Bp / 2 : Bp;
+        const int n_parts = Bp / n_half;
+        const uint32_t idesc = mma_idesc(128, n_half, false);
         const int chunks16 = a.r / 8;                         // 16-byte pieces of a w1 row
 
         for (int i = 0; i < a.N && alive; ++i) {
@@ -310,8 +307,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             const uint32_t b_addr = smem_u32(Es + kb * e_kb_bytes);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                mma_issue<false>(d, sw128_kmajor_desc(a_addr + 32 * k),
-                                                 sw128_kmajor_desc(b_addr + 32 * k), idesc, (kb | k) != 0 ? 1u : 0u);
+                                for (int h = 0; h < n_parts; ++h)   // rows h*n_half.. of E: 8-row groups of 1024 B
+                                    mma_issue<false>(d + static_cast<uint32_t>(h * n_half),
+                                                     sw128_kmajor_desc(a_addr + 32 * k),
+                                                     sw128_kmajor_desc(b_addr + static_cast<uint32_t>(h * n_half) * 128u + 32 * k),
+                                                     idesc, (kb | k) != 0 ? 1u : 0u);
                             mma_commit(&bar_w2_empty[w2st]);
                             if (++w2st == t.w2_stages) { w2st = 0; w2ph ^= 1u; }
                         }
