@@ -256,12 +256,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         int w2st = 0, lsg = 0;
         uint32_t w2ph = 0, lphg = 0;
         bool alive = true, dead = false, nan_seen = false;
-        // Bias MMAs of one tile accumulate into one region, so a single narrow-N chain is
-        // latency-bound; split the requests into two halves (two independent chains in
-        // adjacent TMEM columns, the same layout) and interleave them.
-        const int n_half = (Bp % 32 == 0) ? Bp / 2 : Bp;
-        const int n_parts = Bp / n_half;
-        const uint32_t idesc = mma_idesc(128, n_half, false);
+        // one MMA covers all B_pad requests: measured on sm_103a, a tcgen05.mma of
+        // M=128, K=16 costs about the same time for N=32, 64 or 256, so the widest N wins
+        const uint32_t idesc = mma_idesc(128, Bp, false);
         const int chunks16 = a.r / 8;                         // 16-byte pieces of a w1 row
 
         for (int i = 0; i < a.N && alive; ++i) {
@@ -307,11 +304,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             const uint32_t b_addr = smem_u32(Es + kb * e_kb_bytes);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                for (int h = 0; h < n_parts; ++h)   // rows h*n_half.. of E: 8-row groups of 1024 B
-                                    mma_issue<false>(d + static_cast<uint32_t>(h * n_half),
-                                                     sw128_kmajor_desc(a_addr + 32 * k),
-                                                     sw128_kmajor_desc(b_addr + static_cast<uint32_t>(h * n_half) * 128u + 32 * k),
-                                                     idesc, (kb | k) != 0 ? 1u : 0u);
+                                mma_issue<false>(d, sw128_kmajor_desc(a_addr + 32 * k),
+                                                 sw128_kmajor_desc(b_addr + 32 * k), idesc, (kb | k) != 0 ? 1u : 0u);
                             mma_commit(&bar_w2_empty[w2st]);
                             if (++w2st == t.w2_stages) { w2st = 0; w2ph ^= 1u; }
                         }
