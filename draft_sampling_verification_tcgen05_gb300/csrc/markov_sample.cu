@@ -86,6 +86,40 @@ __device__ __forceinline__ float bias_dot(const uint8_t* row, const float* e, in
     return (acc0 + acc1) + (acc2 + acc3);
 }
 
+// Two rows against the same E row at once (independent chains, shared E reads).
+template <typename WT>
+__device__ __forceinline__ void bias_dot2(const uint8_t* row0, const uint8_t* row1, const float* e, int r,
+                                          float& out0, float& out1) {
+    if constexpr (sizeof(WT) == 2) {
+        if (((reinterpret_cast<uintptr_t>(row0) | reinterpret_cast<uintptr_t>(row1)) & 15) == 0 && (r & 7) == 0 &&
+            (reinterpret_cast<uintptr_t>(e) & 15) == 0) {
+            float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+            for (int k = 0; k < r; k += 8) {
+                const uint4 q0 = *reinterpret_cast<const uint4*>(row0 + 2 * k);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(row1 + 2 * k);
+                const float4 e0 = *reinterpret_cast<const float4*>(e + k);
+                const float4 e1 = *reinterpret_cast<const float4*>(e + k + 4);
+                const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&q0);
+                const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&q1);
+                float2 f;
+                f = __bfloat1622float2(h0[0]); a0 = fmaf(f.x, e0.x, a0); c0 = fmaf(f.y, e0.y, c0);
+                f = __bfloat1622float2(h0[1]); a0 = fmaf(f.x, e0.z, a0); c0 = fmaf(f.y, e0.w, c0);
+                f = __bfloat1622float2(h0[2]); a0 = fmaf(f.x, e1.x, a0); c0 = fmaf(f.y, e1.y, c0);
+                f = __bfloat1622float2(h0[3]); a0 = fmaf(f.x, e1.z, a0); c0 = fmaf(f.y, e1.w, c0);
+                f = __bfloat1622float2(h1[0]); a1 = fmaf(f.x, e0.x, a1); c1 = fmaf(f.y, e0.y, c1);
+                f = __bfloat1622float2(h1[1]); a1 = fmaf(f.x, e0.z, a1); c1 = fmaf(f.y, e0.w, c1);
+                f = __bfloat1622float2(h1[2]); a1 = fmaf(f.x, e1.x, a1); c1 = fmaf(f.y, e1.y, c1);
+                f = __bfloat1622float2(h1[3]); a1 = fmaf(f.x, e1.z, a1); c1 = fmaf(f.y, e1.w, c1);
+            }
+            out0 = a0 + c0;
+            out1 = a1 + c1;
+            return;
+        }
+    }
+    out0 = bias_dot<WT>(row0, e, r);
+    out1 = bias_dot<WT>(row1, e, r);
+}
+
 __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long k, unsigned long long* red) {
     k = warp_max_u64(k);
     __syncthreads();
@@ -122,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     __shared__ unsigned long long s_red[kWarps];
     __shared__ float2 s_red2[kWarps];
     __shared__ float s_bcast[2];
+    __shared__ float s_temp[256];                     // temperatures of the first 256 requests
 
     const int v_lo = blockIdx.x * a.slice;
     const int v_hi = min(a.V, v_lo + a.slice);
@@ -153,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
 
+    for (int b = tid; b < 256 && b < a.B; b += kThreads) s_temp[b] = __ldg(a.temperature + b);
     bool alive = true;
     for (int i = 0; i < a.N && alive; ++i) {
         // ---- 1. previous tokens and the Markov embedding E[b] = w1[prev_b] ----
@@ -183,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         float2* lse_part = a.lay.lse_part + static_cast<size_t>(i & 1) * kMaxGrid * a.B;
 
         for (int b = 0; b < a.B; ++b) {
-            float T = __ldg(a.temperature + b);
+            float T = b < 256 ? s_temp[b] : __ldg(a.temperature + b);
             if (!(T >= 0.f) || isinf(T)) {
                 if (tid == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
                 T = 0.f;
@@ -197,6 +233,36 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             unsigned long long best = 0ull;
             float2 ls = make_float2(0.f, 0.f);
             bool bad = false;
+            if (hot && a.single_pass && a.lse == nullptr) {
+                // one pass with noise on every entry; each thread takes two adjacent entries,
+                // which share their noise counter (v >> 3) and interleave for ILP
+                for (int t = 2 * tid; t < n_local; t += 2 * kThreads) {
+                    const int v = v_lo + t;
+                    const bool two = t + 1 < n_local;
+                    const uint8_t* wrow0 = a.w2_cached ? w2s + static_cast<size_t>(t) * a.w2_pitch
+                                                       : static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v) * row_bytes;
+                    const uint8_t* wrow1 = a.w2_cached ? wrow0 + a.w2_pitch : wrow0 + row_bytes;
+                    float b0, b1;
+                    bias_dot2<WT>(wrow0, two ? wrow1 : wrow0, e, a.r, b0, b1);
+                    const float l0 = __ldcs(lrow + v);
+                    const float l1 = two ? __ldcs(lrow + v + 1) : 0.f;
+                    const uint4 wh = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
+                                               kStreamGumbel, static_cast<uint32_t>(i));
+                    const uint4 wl = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
+                                               kStreamGumbelLo, static_cast<uint32_t>(i));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && !two) break;
+                        const uint32_t vv = static_cast<uint32_t>(v + h);
+                        const float z = __fmul_rn(__fadd_rn(h ? l1 : l0, h ? b1 : b0), invT);
+                        if (z != z) { bad = true; continue; }
+                        const float y = __fadd_rn(z, gumbel_from_word((draft_half(wh, vv) << 16) | draft_half(wl, vv)));
+                        if (y != y) continue;
+                        const unsigned long long k = argmax_key(y, vv);
+                        best = k > best ? k : best;
+                    }
+                }
+            } else
             for (int t = tid; t < n_local; t += kThreads) {
                 const int v = v_lo + t;
                 const uint8_t* wrow = a.w2_cached ? w2s + static_cast<size_t>(t) * a.w2_pitch
