@@ -88,6 +88,42 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* ws, uint32_t phase, long 
     return s_ok != 0;
 }
 
+// The same barrier in two halves, so a block can do work that does not depend
+// on the other blocks between arriving and waiting.
+__device__ __forceinline__ void grid_arrive(WsHeader* ws) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(&ws->barrier) : "memory");
+    }
+}
+
+__device__ __forceinline__ bool grid_wait(WsHeader* ws, uint32_t phase, long long timeout_ns, uint32_t where) {
+    __shared__ int s_ok2;
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const uint32_t target = (phase + 1u) * gridDim.x;
+        const long long t0 = global_ns();
+        uint32_t spins = 0;
+        while (ld_acquire_u32(&ws->barrier) < target) {
+            if ((++spins & 63u) == 0) {
+                if (aborted(ws)) { ok = 0; break; }
+                if (global_ns() - t0 > timeout_ns) {
+                    atomicOr(&ws->status, DSPARK_STATUS_TIMEOUT);
+                    atomicExch(&ws->detail, where);
+                    ok = 0;
+                    break;
+                }
+            }
+            __nanosleep(32);
+        }
+        __threadfence();
+        s_ok2 = ok;
+    }
+    __syncthreads();
+    return s_ok2 != 0;
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }

@@ -189,6 +189,29 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     }
 
     for (int b = tid; b < 256 && b < a.B; b += kThreads) s_temp[b] = __ldg(a.temperature + b);
+    // Decode fast path (one request, one pair of entries per thread): the base logits and
+    // the noise of step i+1 do not depend on the token of step i, so they are fetched and
+    // drawn while the block waits at step i's grid barrier.
+    const bool fast = a.B == 1 && a.single_pass && a.lse == nullptr && 2 * kThreads >= n_local;
+    float pl0 = 0.f, pl1 = 0.f, pg0 = 0.f, pg1 = 0.f;
+    auto prepare = [&](int j) {
+        const int t = 2 * tid;
+        if (t >= n_local) return;
+        const int v = v_lo + t;
+        const bool two = t + 1 < n_local;
+        const float* lr = a.base + static_cast<size_t>(j) * a.V;
+        pl0 = __ldcs(lr + v);
+        pl1 = two ? __ldcs(lr + v + 1) : 0.f;
+        const uint4 wh = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, 0u, kStreamGumbel,
+                                   static_cast<uint32_t>(j));
+        const uint4 wl = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, 0u, kStreamGumbelLo,
+                                   static_cast<uint32_t>(j));
+        pg0 = gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v)) << 16) | draft_half(wl, static_cast<uint32_t>(v)));
+        pg1 = two ? gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v + 1)) << 16) |
+                                     draft_half(wl, static_cast<uint32_t>(v + 1)))
+                  : 0.f;
+    };
+    if (fast) prepare(0);
     bool alive = true;
     for (int i = 0; i < a.N && alive; ++i) {
         // ---- 1. previous tokens and the Markov embedding E[b] = w1[prev_b] ----
@@ -244,19 +267,29 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                     const uint8_t* wrow1 = a.w2_cached ? wrow0 + a.w2_pitch : wrow0 + row_bytes;
                     float b0, b1;
                     bias_dot2<WT>(wrow0, two ? wrow1 : wrow0, e, a.r, b0, b1);
-                    const float l0 = __ldcs(lrow + v);
-                    const float l1 = two ? __ldcs(lrow + v + 1) : 0.f;
-                    const uint4 wh = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
-                                               kStreamGumbel, static_cast<uint32_t>(i));
-                    const uint4 wl = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
-                                               kStreamGumbelLo, static_cast<uint32_t>(i));
+                    float l0, l1, g0, g1;
+                    if (fast) {
+                        l0 = pl0; l1 = pl1; g0 = pg0; g1 = pg1;
+                    } else {
+                        l0 = __ldcs(lrow + v);
+                        l1 = two ? __ldcs(lrow + v + 1) : 0.f;
+                        const uint4 wh = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
+                                                   kStreamGumbel, static_cast<uint32_t>(i));
+                        const uint4 wl = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
+                                                   kStreamGumbelLo, static_cast<uint32_t>(i));
+                        g0 = gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v)) << 16) |
+                                              draft_half(wl, static_cast<uint32_t>(v)));
+                        g1 = two ? gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v + 1)) << 16) |
+                                                    draft_half(wl, static_cast<uint32_t>(v + 1)))
+                                 : 0.f;
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (h == 1 && !two) break;
                         const uint32_t vv = static_cast<uint32_t>(v + h);
                         const float z = __fmul_rn(__fadd_rn(h ? l1 : l0, h ? b1 : b0), invT);
                         if (z != z) { bad = true; continue; }
-                        const float y = __fadd_rn(z, gumbel_from_word((draft_half(wh, vv) << 16) | draft_half(wl, vv)));
+                        const float y = __fadd_rn(z, h ? g1 : g0);
                         if (y != y) continue;
                         const unsigned long long k = argmax_key(y, vv);
                         best = k > best ? k : best;
@@ -328,7 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         }
 
         // ---- 4. all blocks agree on the step's winners ----
-        alive = grid_barrier(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i);
+        grid_arrive(a.ws);
+        if (fast && i + 1 < a.N) prepare(i + 1);
+        alive = grid_wait(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i);
     }
     if (!alive) return;
     __threadfence();
