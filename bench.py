@@ -36,6 +36,28 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 * 1024 * 1024      # > 4x the 129 MB L2
 WORKLOAD_TEMPERATURE = {"qwen3_8b_single": 1.0, "batched_draft": 0.8, "tiny": 1.0}
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one dspark_draft_logits launch,
+# from one ncu capture per workload (summarised under profiles/), with a digest of the kernel's
+# sources at capture time: once the sources change the figure is reported as null.
+GEMM_TRAFFIC = {
+    "qwen3_8b_single": {"bytes": 1244784128 + 5522176, "src_digest": "1bf1cf3ec429",
+                        "profile": "profiles/draft_logits_qwen3_8b_single.md"},
+    "batched_draft": {"bytes": 1268480512 + 588143616, "src_digest": "1bf1cf3ec429",
+                      "profile": "profiles/draft_logits_batched_draft.md"},
+}
+GEMM_SOURCES = ("draft_sampling_verification_tcgen05_gb300/csrc/draft_logits.cu",
+                "draft_sampling_verification_tcgen05_gb300/csrc/device_common.cuh")
+
+
+def gemm_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -187,7 +209,15 @@ def run_gpu(args):
     ws_v = ds.Workspace(ds.OP_VERIFY, B, N, V, device=dev)
     ws_s = ds.Workspace(ds.OP_SCHEDULE, B, N, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(k):
+        # Write 512 MB (every L2 line replaced), then read back half of it: the read evicts
+        # the dirty lines the write left behind, so their write-back happens here rather
+        # than inside the next timed step.  The step starts with a cold, clean L2.
+        flush.fill_(float(k))
+        torch.sum(flush[: flush.numel() // 2], dim=0, out=flush_sink)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
 
@@ -222,7 +252,7 @@ def run_gpu(args):
         if e: e[4].record(stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush_l2(1)
         step()
     torch.cuda.synchronize()
     for wsx in (ws_g, ws_m, ws_v, ws_s):
@@ -244,7 +274,7 @@ def run_gpu(args):
         with torch.cuda.graph(graph, stream=side):
             step()
         for _ in range(args.warmup):
-            flush.fill_(1.0)
+            flush_l2(1)
             graph.replay()
         torch.cuda.synchronize()
     g0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -258,7 +288,7 @@ def run_gpu(args):
         time.sleep(0.5)                           # let the sampler start before the timed region
         wall0 = time.perf_counter()
         for k in range(args.steps):
-            flush.fill_(float(k))                 # L2 flush between timed steps (not timed)
+            flush_l2(k)                           # L2 flush between timed steps (not timed)
             if graph is not None:
                 g0[k].record(stream)
                 graph.replay()
@@ -275,7 +305,7 @@ def run_gpu(args):
     if graph is not None:
         # per-kernel times: the same K steps run eagerly with events between the calls
         for k in range(args.steps):
-            flush.fill_(float(k))
+            flush_l2(k)
             step(k)
         torch.cuda.synchronize()
     per = np.array([[ev[k][j].elapsed_time(ev[k][j + 1]) for j in range(4)] for k in range(args.steps)])
@@ -313,7 +343,7 @@ def run_gpu(args):
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for k in range(args.warmup + args.steps):
             timed = k >= args.warmup
-            flush.fill_(float(k))
+            flush_l2(k)
             if timed:
                 e0[k - args.warmup].record(stream)
             for dst, src in ins:
@@ -356,7 +386,10 @@ def run_gpu(args):
         roof = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s", "frac": ach / bf16_peak}
     roof["kernel"] = "dspark_draft_logits"
     roof["peak_source"] = peak_src
-    roof["traffic"] = None
+    tr = GEMM_TRAFFIC.get(args.workload)
+    roof["traffic"] = tr["bytes"] if tr is not None and tr["src_digest"] == gemm_source_digest() else None
+    if roof["traffic"] is not None:
+        roof["traffic_source"] = tr["profile"]
 
     if dist is not None and rank != 0:
         dist.barrier()
@@ -372,7 +405,7 @@ def run_gpu(args):
                                f"schedule over B*N={M} candidates",
                    "global_batch_requests": B * world, "draft_tokens_per_step": M * world,
                    "parallelism": f"replicas x{world} (requests sharded, no collective)",
-                   "l2": "flushed (512 MB write) between timed steps",
+                   "l2": "flushed between timed steps: 512 MB write, then a 256 MB read-back that evicts the dirty lines",
                    "markov_input": ("base logits + per-row Zipf(1.1) rank offset, offset applied once "
                                     "before timing" if d.zipf > 0 else "this step's base logits")},
         "kernel_ms": {"draft_logits": kernel_ms[0], "markov_sample": kernel_ms[1],

@@ -7,17 +7,22 @@
 // curve is jagged, so every K is evaluated; K may also be fixed ahead of time
 // and only the fill done now.  No token value is read at any point.
 //
-// Steps (one block of 1024 threads, 256 for pools of at most 256 candidates):
-//   1. survival chain per request (fp32, round to nearest, no contraction)
-//      and 64-bit keys ((~survival bits) << 32 | b*N+k), in index order
-//   2. stable LSD radix sort of the keys on their upper 32 bits (4 passes of
-//      8 bits; rounds of 1024 keys ranked with warp match + per-warp digit
-//      counts), ping-ponging between two workspace buffers (L2-resident);
-//      pools of at most 1024 candidates are ranked by counting, in shared memory
-//   3. if K is to be chosen: block-wide prefix sum of floor(s * 2^32) over the
-//      sorted order, f(K) = float64(B * 2^32 + prefix) * SPS[K-1] for every K,
-//      block argmax with ties to the smallest K
-//   4. fill: the first K sorted candidates are admitted; lengths by counting.
+// Pools of up to 16384 candidates (every admission pool of a serving batch) run
+// entirely in shared memory, one block of 1024 threads (256 for pools of at
+// most 256):
+//   1. coalesced load of c; survival chain per request (fp32, round to nearest,
+//      no contraction); sort key (~bits(s)) per candidate, index order
+//   2. stable LSD radix sort of candidate indices by that key: 4 passes of 8
+//      bits; each warp ranks a contiguous run of the current order with warp
+//      match, per-warp digit counters are turned into output positions by one
+//      block scan, then scattered (the index breaks survival ties for free)
+//   3. if K is to be chosen: fixed-point masses floor(s * 2^32) from the float
+//      bits, block prefix sum, f(K) = float64(B * 2^32 + prefix) * SPS[K-1]
+//      for every K with the rounding done in integer arithmetic (the FP64 pipe
+//      of this GPU is narrow), block argmax with ties to the smallest K
+//   4. fill: selected in rank order, lengths by counting admitted flags
+// Larger pools (up to 2^20) take the same steps with the keys in the
+// workspace (global memory, L2-resident) instead of shared memory.
 #include "device_common.cuh"
 #include "host_common.h"
 
@@ -45,44 +50,478 @@ __device__ __forceinline__ float clamp_prob(float x, bool& bad) {
     return x;
 }
 
-// Exclusive block scan of one u64 per thread; returns the exclusive prefix, *total the sum.
-__device__ unsigned long long block_excl_scan_u64(unsigned long long x, unsigned long long* sm,
-                                                  unsigned long long* total) {
-    const uint32_t lane = lane_id(), warp = warp_id();
-    unsigned long long incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= static_cast<uint32_t>(o)) incl += y;
-    }
-    __syncthreads();
-    if (lane == 31) sm[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        unsigned long long w = lane < blockDim.x / 32 ? sm[lane] : 0ull;
-        unsigned long long wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
-            if (lane >= static_cast<uint32_t>(o)) wi += y;
-        }
-        sm[lane] = wi - w;                 // exclusive prefix of warp totals
-        if (lane == 31) sm[32] = wi;
-    }
-    __syncthreads();
-    *total = sm[32];
-    return sm[warp] + incl - x;
+// Sort key of a survival value: smaller key = earlier in the admission order.  -0 and +0
+// are one value (the key of +0).
+__device__ __forceinline__ uint32_t order_key(float s) {
+    return 0xFFFFFFFFu - __float_as_uint(__fadd_rn(s, 0.f));
 }
 
+// Survival back from its key.
+__device__ __forceinline__ float key_survival(uint32_t key) { return __uint_as_float(0xFFFFFFFFu - key); }
+
+// floor(s * 2^32) for s in [0, 1] from the float's bits (s = m * 2^(e - 150) for biased
+// exponent e and 24-bit significand m, so s * 2^32 = m * 2^(e - 118)); subnormals give 0.
+__device__ __forceinline__ unsigned long long mass32(float s) {
+    const uint32_t bits = __float_as_uint(s) & 0x7FFFFFFFu;
+    const int e = static_cast<int>(bits >> 23);
+    const unsigned long long m = (bits & 0x7FFFFFu) | 0x800000u;
+    const int sh = e - 118;
+    if (e == 0 || sh <= -24) return 0ull;
+    return sh >= 0 ? m << sh : m >> -sh;          // s <= 1 keeps sh <= 9
+}
+
+constexpr unsigned long long kMant52 = 0xFFFFFFFFFFFFFull;
+
+// Bits of float64(E), round to nearest even, for E >= 1 (integer operations only).
+__device__ __forceinline__ unsigned long long u64_to_f64_bits(unsigned long long E) {
+    const int lz = __clzll(static_cast<long long>(E));
+    const unsigned long long m = E << lz;          // leading one at bit 63
+    unsigned long long hi = m >> 11;               // 53 significant bits
+    const unsigned long long rem = m & 0x7FFull;
+    int ex = 63 - lz;
+    if (rem > 0x400ull || (rem == 0x400ull && (hi & 1ull))) {
+        ++hi;
+        if (hi >> 53) {
+            hi >>= 1;
+            ++ex;
+        }
+    }
+    return (static_cast<unsigned long long>(ex + 1023) << 52) | (hi & kMant52);
+}
+
+// Bits of fl64(a * b), round to nearest even, for a positive normal double a (bits ab) when
+// b (bits bb) is a positive normal double and the rounded product is normal; returns false
+// in every other case, where the caller multiplies with __dmul_rn instead.  The significands
+// (53 bits each) multiply exactly into 106 bits, which are cut back to 53 with the
+// round-half-even rule.
+__device__ __forceinline__ bool f64_mul_bits(unsigned long long ab, unsigned long long bb,
+                                             unsigned long long* out) {
+    const int eb = static_cast<int>((bb >> 52) & 0x7FFull);
+    if ((bb >> 63) != 0ull || eb == 0 || eb == 0x7FF) return false;
+    const int ea = static_cast<int>(ab >> 52);
+    const unsigned long long ma = (ab & kMant52) | (1ull << 52);
+    const unsigned long long mb = (bb & kMant52) | (1ull << 52);
+    const unsigned long long lo = ma * mb, hi = __umul64hi(ma, mb);      // product in [2^104, 2^106)
+    const int top = static_cast<int>((hi >> 41) & 1ull);                  // product >= 2^105
+    const int sh = 52 + top;
+    unsigned long long r = (hi << (64 - sh)) | (lo >> sh);                // 53 bits
+    const unsigned long long rest = lo & ((1ull << sh) - 1ull);
+    const unsigned long long half = 1ull << (sh - 1);
+    int e = ea + eb - 1023 + top;                                         // biased exponent
+    if (rest > half || (rest == half && (r & 1ull))) {
+        ++r;
+        if (r >> 53) {
+            r >>= 1;
+            ++e;
+        }
+    }
+    if (e <= 0 || e >= 0x7FF) return false;
+    *out = (static_cast<unsigned long long>(e) << 52) | (r & kMant52);
+    return true;
+}
+
+// f(K) = float64(E) * sps as a key that orders like the double (larger key = larger f);
+// 0 for a NaN or -inf product, which never wins (the search starts below every f > -inf).
+__device__ __forceinline__ unsigned long long objective_key(unsigned long long E, double sps) {
+    const unsigned long long eb = u64_to_f64_bits(E);
+    unsigned long long fb;
+    if (!f64_mul_bits(eb, static_cast<unsigned long long>(__double_as_longlong(sps)), &fb)) {
+        const double f = __dmul_rn(__longlong_as_double(static_cast<long long>(eb)), sps);
+        if (!(f > -INFINITY)) return 0ull;
+        fb = static_cast<unsigned long long>(__double_as_longlong(f));
+        if ((fb << 1) == 0ull) fb = 0ull;                               // -0 is +0
+    }
+    return (fb >> 63) ? ~fb : (fb | 0x8000000000000000ull);
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    return x;
+}
+
+// Capacity K* over the sorted order (sorted(j) = the sort key of the j-th candidate), shared by
+// both kernels.  Warp w owns a contiguous run of ranks and walks it 32 at a time: a first
+// walk sums its masses, a block scan of the warp sums gives each run's starting prefix, a
+// second walk forms every E(K) with an inclusive warp scan and keeps the best f(K).
+// Returns K* to every thread.
+template <int kThreads, typename SortedKey>
+__device__ int choose_capacity(const ScheduleArgs& a, int n, SortedKey sorted, unsigned long long* s_wsum,
+                               unsigned long long* s_bk, int* s_bK, int* s_K) {
+    constexpr int kWarps = kThreads / 32;
+    const int tid = threadIdx.x;
+    const uint32_t lane = lane_id(), warp = warp_id();
+    const int Kmax = a.S < n ? a.S : n;
+    const int run = (((Kmax + kWarps - 1) / kWarps) + 31) & ~31;
+    const int j0 = static_cast<int>(warp) * run, j1 = min(Kmax, j0 + run);
+    unsigned long long part = 0;
+    for (int j = j0 + static_cast<int>(lane); j < j1; j += 32) part += mass32(key_survival(sorted(j)));
+    part = warp_sum_u64(part);
+    if (lane == 0) s_wsum[warp] = part;
+    __syncthreads();
+    unsigned long long carry = static_cast<unsigned long long>(a.B) << 32;
+    for (int w = 0; w < static_cast<int>(warp); ++w) carry += s_wsum[w];
+    unsigned long long best_key = 0ull;                   // below every f > -inf
+    int best_K = 0x7FFFFFFF;
+    for (int jg = j0; jg < j1; jg += 4 * 32) {
+        double sps4[4];                                    // four rounds of SPS loads in flight
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = jg + i * 32 + static_cast<int>(lane);
+            sps4[i] = j < j1 ? __ldg(a.sps + j) : 0.0;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = jg + i * 32 + static_cast<int>(lane);
+            const bool valid = j < j1;
+            const unsigned long long q = valid ? mass32(key_survival(sorted(j))) : 0ull;
+            unsigned long long incl = q;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= static_cast<uint32_t>(o)) incl += y;
+            }
+            if (valid) {
+                const unsigned long long k = objective_key(carry + incl, sps4[i]);
+                if (k > best_key) {                        // ascending K per lane: strict keeps the smallest
+                    best_key = k;
+                    best_K = j + 1;
+                }
+            }
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best_key, o);
+        const int oK = __shfl_xor_sync(0xFFFFFFFFu, best_K, o);
+        if (ok > best_key || (ok == best_key && oK < best_K)) {
+            best_key = ok;
+            best_K = oK;
+        }
+    }
+    if (lane == 0) {
+        s_bk[warp] = best_key;
+        s_bK[warp] = best_K;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long bkey = 0ull;
+        int bK = 0x7FFFFFFF;
+        for (int w = 0; w < kWarps; ++w) {
+            if (s_bk[w] > bkey || (s_bk[w] == bkey && s_bK[w] < bK)) {
+                bkey = s_bk[w];
+                bK = s_bK[w];
+            }
+        }
+        if (bK == 0x7FFFFFFF) {             // every f was NaN or -inf: K = 1, flagged
+            set_status(a.ws, DSPARK_STATUS_NUMERIC);
+            bK = 1;
+        }
+        *s_K = bK;
+    }
+    __syncthreads();
+    return *s_K;
+}
+
+// ---------------------------------------------------------------------------
+// Pools of at most 32 candidates (a few decode requests): one warp, one candidate per lane,
+// no block barrier at all.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(32) schedule_warp_kernel(ScheduleArgs a) {
+    __shared__ int s_at_rank[32];
+    const int lane = static_cast<int>(threadIdx.x);
+    const int B = a.B, N = a.N, n = B * N;
+    const bool valid = lane < n;
+    const int k = lane % N;
+    bool bad = false;
+    const float c = valid ? clamp_prob(__ldg(a.c + lane), bad) : 1.f;
+    // survival chain: at step t the lanes with k == t multiply their left neighbour's
+    // (final) survival by their own confidence
+    float s = c;
+    for (int t = 1; t < N; ++t) {
+        const float left = __shfl_up_sync(0xFFFFFFFFu, s, 1);
+        if (k == t) s = __fmul_rn(left, c);
+    }
+    if (valid) a.survival[lane] = s;
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+    // rank = keys before this one in (key, index) order; empty lanes sort last
+    const uint32_t my = valid ? order_key(s) : 0xFFFFFFFFu;
+    int rank = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t other = __shfl_sync(0xFFFFFFFFu, my, i);
+        rank += (other < my || (other == my && i < lane)) ? 1 : 0;
+    }
+    s_at_rank[rank] = lane;
+    __syncwarp();
+    const int at = s_at_rank[lane];                        // candidate at rank `lane`
+    const float s_at = __shfl_sync(0xFFFFFFFFu, s, at);
+    int K;
+    if (a.K_in >= 0) {
+        K = a.K_in < n ? a.K_in : n;
+    } else {
+        const int Kmax = a.S < n ? a.S : n;
+        const bool in = lane < Kmax;
+        unsigned long long incl = in ? mass32(s_at) : 0ull;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        unsigned long long best_key = in ? objective_key((static_cast<unsigned long long>(B) << 32) + incl,
+                                                         __ldg(a.sps + lane))
+                                         : 0ull;
+        int best_K = best_key != 0ull ? lane + 1 : 0x7FFFFFFF;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best_key, o);
+            const int oK = __shfl_xor_sync(0xFFFFFFFFu, best_K, o);
+            if (ok > best_key || (ok == best_key && oK < best_K)) {
+                best_key = ok;
+                best_K = oK;
+            }
+        }
+        if (best_K == 0x7FFFFFFF) {                       // every f was NaN or -inf: K = 1, flagged
+            if (lane == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+            best_K = 1;
+        }
+        K = best_K;
+    }
+    if (valid) a.selected[lane] = lane < K ? at : -1;
+    const unsigned long long admitted = __ballot_sync(0xFFFFFFFFu, valid && rank < K);
+    if (lane < B) {
+        const unsigned long long mask = (N >= 64 ? ~0ull : ((1ull << N) - 1ull)) << (lane * N);
+        a.lengths[lane] = __popcll(admitted & mask);
+    }
+    if (lane == 0) a.K_out[0] = K;
+}
+
+// ---------------------------------------------------------------------------
+// Pools of up to kSmemMaxCandidates: everything in shared memory.
+// ---------------------------------------------------------------------------
+constexpr int kSmemMaxCandidates = 16384;
+constexpr int kMaxRounds = kSmemMaxCandidates / (32 * 32);       // rounds of 32 keys per warp (1024 threads)
+
+// Dynamic shared memory: key[nn] u32 | idxA[nn] u16 | idxB[nn] u16 | cnt[kWarps][256] u16, nn = n
+// rounded up to 32 (whole swizzle rows)
+size_t smem_schedule_bytes(int n, int warps) {
+    const size_t nn = (static_cast<size_t>(n) + 31) & ~static_cast<size_t>(31);
+    return 4 * nn + 2 * 2 * nn + 2 * static_cast<size_t>(warps) * kRadix;
+}
+
+// Lanes of the warp holding the same 8-bit digit as this lane (bit 8 set = no digit: such a
+// lane matches only lanes that also have no digit), from nine ballots; a warp match would do
+// the same in one instruction, but it is far slower on this GPU.
+__device__ __forceinline__ uint32_t same_digit_lanes(uint32_t d) {
+    uint32_t peers = 0xFFFFFFFFu;
+#pragma unroll
+    for (int bit = 0; bit < 9; ++bit) {
+        const uint32_t ones = __ballot_sync(0xFFFFFFFFu, (d >> bit) & 1u);
+        peers &= ((d >> bit) & 1u) ? ones : ~ones;
+    }
+    return peers;
+}
+
+// Shared-memory slot of candidate id's key: rows of 32 words are permuted by the row index, so
+// one thread per request walking its N consecutive keys (lanes N words apart) does not hit
+// the same bank from every lane.
+__device__ __forceinline__ int swz(int id) { return id ^ ((id >> 5) & 31); }
+
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs a) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kQuarters = kThreads / kRadix;        // (digit, quarter) threads of the scan
+    constexpr int kWarpsPerQuarter = kWarps / kQuarters;
+    static_assert(kWarpsPerQuarter * kQuarters == kWarps, "scan layout");
+    // rounds of 32 keys per warp: 16 at 1024 threads (16384 keys), 1 at 256 threads (256 keys)
+    constexpr int kRounds = kThreads == 1024 ? kMaxRounds : 1;
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    __shared__ uint32_t s_qs[kQuarters][kRadix];
+    __shared__ uint32_t s_wt[kRadix / 32];
+    __shared__ unsigned long long s_wsum[kWarps];
+    __shared__ unsigned long long s_bk[kWarps];
+    __shared__ int s_bK[kWarps];
+    __shared__ int s_K;
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x;
+    const uint32_t lane = lane_id(), warp = warp_id();
+    const int B = a.B, N = a.N;
+    const int n = B * N;
+    const int nn = (n + 31) & ~31;
+    uint32_t* key = reinterpret_cast<uint32_t*>(s_dyn);   // key[swz(id)], nn words
+    uint16_t* idxA = reinterpret_cast<uint16_t*>(key + nn);
+    uint16_t* idxB = idxA + nn;
+    uint16_t* cnt = idxB + nn;                           // [kWarps][kRadix]
+
+    // the SPS table is read late (step 3): start pulling it into L2 now
+    if (a.K_in < 0) {
+        const int Kmax = a.S < n ? a.S : n;
+        for (int j = tid * 16; j < Kmax; j += kThreads * 16) prefetch_l2(a.sps + j);
+    }
+
+    // ---- 1. coalesced load of c, survival chain (one thread per request), keys ----
+    if (tid == 0) s_bad = 0;
+    for (int j = tid; j < n; j += kThreads) {
+        key[swz(j)] = __float_as_uint(__ldg(a.c + j));
+        idxA[j] = static_cast<uint16_t>(j);
+    }
+    __syncthreads();
+    bool bad = false;
+    for (int b = tid; b < B; b += kThreads) {
+        float s = 1.f;
+        for (int k = 0; k < N; ++k) {
+            const int id = b * N + k;
+            const float c = clamp_prob(__uint_as_float(key[swz(id)]), bad);
+            s = (k == 0) ? c : __fmul_rn(s, c);
+            a.survival[id] = s;
+            key[swz(id)] = order_key(s);
+        }
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (tid == 0 && s_bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+
+    // ---- 2. stable LSD radix sort of the indices by key ----
+    // warp w ranks the run [w0, w1) of the current order; chunk is a multiple of 32
+    const int chunk = (((n + kWarps - 1) / kWarps) + 31) & ~31;
+    const int w0 = static_cast<int>(warp) * chunk;
+    const int w1 = min(n, w0 + chunk);
+    const int rounds = w1 > w0 ? (w1 - w0 + 31) / 32 : 0;
+    uint16_t* src = idxA;
+    uint16_t* dst = idxB;
+    uint16_t* mycnt = cnt + warp * kRadix;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 8 * pass;
+        for (int i = tid; i < kWarps * kRadix / 2; i += kThreads) reinterpret_cast<uint32_t*>(cnt)[i] = 0u;
+        // (a) digits of this warp's keys, all loads first
+        uint32_t slot[kRounds];
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+            const int j = w0 + r * 32 + static_cast<int>(lane);
+            slot[r] = (r < rounds && j < w1) ? ((key[swz(src[j])] >> shift) & 0xFFu) : (0x100u | lane);
+        }
+        __syncthreads();                                  // counters cleared
+        // per-warp digit counts; each key keeps (digit << 16 | offset within the warp's digit)
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+            if (r < rounds) {
+                const uint32_t d = slot[r];
+                const bool valid = d < 0x100u;
+                const uint32_t peers = same_digit_lanes(d);
+                const uint32_t below = peers & ((1u << lane) - 1u);
+                const uint32_t base = valid ? mycnt[d] : 0u;
+                __syncwarp();
+                if (valid && below == 0u) mycnt[d] = static_cast<uint16_t>(base + __popc(peers));
+                __syncwarp();
+                slot[r] = (d << 16) | (base + __popc(below));
+            }
+        }
+        __syncthreads();
+        // (b) output position of (warp, digit): digit start + the same digit in earlier warps
+        const int sd = tid & (kRadix - 1), sq = tid / kRadix;
+        {
+            uint32_t run = 0;
+#pragma unroll
+            for (int i = 0; i < kWarpsPerQuarter; ++i) {
+                uint16_t* c = cnt + (sq * kWarpsPerQuarter + i) * kRadix + sd;
+                const uint32_t v = *c;
+                *c = static_cast<uint16_t>(run);
+                run += v;
+            }
+            s_qs[sq][sd] = run;
+        }
+        __syncthreads();
+        uint32_t digit_excl = 0;                      // digits below this one, within this warp's 32
+        if (tid < kRadix) {
+            uint32_t tot = 0;
+#pragma unroll
+            for (int q = 0; q < kQuarters; ++q) {     // quarters: exclusive prefix in place
+                const uint32_t v = s_qs[q][tid];
+                s_qs[q][tid] = tot;
+                tot += v;
+            }
+            uint32_t incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= static_cast<uint32_t>(o)) incl += y;
+            }
+            if (lane == 31) s_wt[warp] = incl;
+            digit_excl = incl - tot;
+        }
+        __syncthreads();
+        if (tid < kRadix) {
+            uint32_t before = digit_excl;
+            for (int w = 0; w < static_cast<int>(warp); ++w) before += s_wt[w];
+#pragma unroll
+            for (int q = 0; q < kQuarters; ++q) s_qs[q][tid] += before;
+        }
+        __syncthreads();
+        {
+            const uint32_t add = s_qs[sq][sd];
+#pragma unroll
+            for (int i = 0; i < kWarpsPerQuarter; ++i) {
+                uint16_t* c = cnt + (sq * kWarpsPerQuarter + i) * kRadix + sd;
+                *c = static_cast<uint16_t>(*c + add);
+            }
+        }
+        __syncthreads();
+        // (c) scatter
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+            if (r < rounds) {
+                const int j = w0 + r * 32 + static_cast<int>(lane);
+                if (j < w1) {
+                    const uint32_t d = slot[r] >> 16;
+                    dst[mycnt[d] + (slot[r] & 0xFFFFu)] = src[j];
+                }
+            }
+        }
+        __syncthreads();
+        uint16_t* t = src;
+        src = dst;
+        dst = t;
+    }
+    // sorted candidate indices are in src
+
+    // ---- 3. capacity K ----
+    int K;
+    if (a.K_in >= 0) {
+        K = a.K_in < n ? a.K_in : n;
+    } else {
+        K = choose_capacity<kThreads>(a, n, [&](int j) { return key[swz(src[j])]; }, s_wsum, s_bk, s_bK, &s_K);
+    }
+
+    // ---- 4. fill: selected in rank order; admitted flags (in the key slots) give the lengths ----
+    __syncthreads();
+    for (int j = tid; j < n; j += kThreads) {
+        const int idx = src[j];
+        a.selected[j] = j < K ? idx : -1;
+        key[swz(idx)] = j < K ? 1u : 0u;
+    }
+    __syncthreads();
+    for (int b = tid; b < B; b += kThreads) {
+        int len = 0;
+        for (int k = 0; k < N; ++k) len += static_cast<int>(key[swz(b * N + k)]);
+        a.lengths[b] = len;
+    }
+    if (tid == 0) a.K_out[0] = K;
+}
+
+// ---------------------------------------------------------------------------
+// Pools above kSmemMaxCandidates: 64-bit keys (order key << 32 | index) in the workspace.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024, 1) schedule_global_kernel(ScheduleArgs a) {
+    constexpr int kThreads = 1024;
     constexpr int kWarps = kThreads / 32;
     __shared__ uint32_t s_cnt[kWarps][kRadix];
     __shared__ uint32_t s_base[kRadix];
     __shared__ uint32_t s_tmp[kRadix];
-    __shared__ unsigned long long s_scan[33];                 // 32 warp slots + total
-    __shared__ double s_bf[kWarps];
-    __shared__ int s_bk[kWarps];
+    __shared__ unsigned long long s_wsum[kWarps];
+    __shared__ unsigned long long s_bk[kWarps];
+    __shared__ int s_bK[kWarps];
     __shared__ int s_K;
 
     const int tid = threadIdx.x;
@@ -90,10 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
     const int B = a.B, N = a.N;
     const int n = B * N;
 
-    // ---- 1. survival chain and keys (small pools keep their keys in shared memory) ----
-    const bool small = n <= kThreads;
-    unsigned long long* sk = reinterpret_cast<unsigned long long*>(&s_cnt[0][0]);   // [2][kThreads] when small
-    unsigned long long* keys = small ? sk : a.keys0;
+    // ---- 1. survival chain and keys ----
     bool bad = false;
     for (int b = tid; b < B; b += kThreads) {
         float s = 1.f;
@@ -102,38 +538,24 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
             const float c = clamp_prob(a.c[idx], bad);
             s = (k == 0) ? c : __fmul_rn(s, c);
             a.survival[idx] = s;
-            keys[idx] = (static_cast<unsigned long long>(0xFFFFFFFFu - __float_as_uint(s)) << 32) |
-                        static_cast<unsigned long long>(idx);
+            a.keys0[idx] = (static_cast<unsigned long long>(order_key(s)) << 32) | static_cast<unsigned long long>(idx);
         }
         a.lengths[b] = 0;
     }
     if (bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
-    if (!small)
-        for (int i = tid; i < kWarps * kRadix; i += kThreads) (&s_cnt[0][0])[i] = 0;
+    for (int i = tid; i < kWarps * kRadix; i += kThreads) (&s_cnt[0][0])[i] = 0;
     __syncthreads();
 
-    // ---- 2. sort: keys are unique (the index is part of the key) ----
+    // ---- 2. stable LSD radix sort on the upper 32 bits (rounds of 1024 keys) ----
     unsigned long long* src = a.keys0;
     unsigned long long* dst = a.keys1;
-    if (small) {
-        // rank of each key = number of smaller keys (one key per thread), all in shared memory
-        const unsigned long long mine = tid < n ? sk[tid] : 0ull;
-        if (tid < n) {
-            int rank = 0;
-            for (int j = 0; j < n; ++j) rank += sk[j] < mine ? 1 : 0;
-            sk[kThreads + rank] = mine;
-        }
-        __syncthreads();
-        src = sk + kThreads;
-    }
-    for (int pass = 0; pass < (small ? 0 : 4); ++pass) {
+    for (int pass = 0; pass < 4; ++pass) {
         const int shift = 32 + 8 * pass;
         if (tid < kRadix) s_base[tid] = 0;
         __syncthreads();
         for (int j = tid; j < n; j += kThreads)
             atomicAdd(&s_base[static_cast<uint32_t>(src[j] >> shift) & 0xFFu], 1u);
         __syncthreads();
-        // exclusive scan of the 256-bin histogram (8 warps, then warp totals)
         uint32_t hv = 0, hincl = 0;
         if (tid < kRadix) {
             hv = s_base[tid];
@@ -155,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
         for (int r0 = 0; r0 < n; r0 += kThreads) {
             const int j = r0 + tid;
             const bool valid = j < n;
-            const unsigned long long key = valid ? src[j] : 0ull;
-            const uint32_t d = valid ? (static_cast<uint32_t>(key >> shift) & 0xFFu) : (0x100u | lane);
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
+            const unsigned long long k = valid ? src[j] : 0ull;
+            const uint32_t d = valid ? (static_cast<uint32_t>(k >> shift) & 0xFFu) : (0x100u | lane);
+            const uint32_t peers = same_digit_lanes(d);
             const uint32_t rank = __popc(peers & ((1u << lane) - 1u));
             if (valid && rank == 0) s_cnt[warp][d] = __popc(peers);
             __syncthreads();
@@ -171,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
                 s_base[tid] = run;
             }
             __syncthreads();
-            if (valid) dst[s_cnt[warp][d] + rank] = key;
+            if (valid) dst[s_cnt[warp][d] + rank] = k;
             __syncthreads();
             for (int i = tid; i < kWarps * kRadix; i += kThreads) (&s_cnt[0][0])[i] = 0;
             __syncthreads();
@@ -180,54 +602,15 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(ScheduleArgs a) {
         src = dst;
         dst = t;
     }
-    // sorted keys are in src (keys0 after the 4 radix passes, shared memory after the rank sort)
 
     // ---- 3. capacity K ----
+    int K;
     if (a.K_in >= 0) {
-        if (tid == 0) s_K = a.K_in < n ? a.K_in : n;
+        K = a.K_in < n ? a.K_in : n;
     } else {
-        const int Kmax = a.S < n ? a.S : n;
-        const int per = (Kmax + kThreads - 1) / kThreads;
-        const int j0 = tid * per, j1 = min(Kmax, j0 + per);
-        unsigned long long mine = 0;
-        for (int j = j0; j < j1; ++j) {
-            const float s = __uint_as_float(0xFFFFFFFFu - static_cast<uint32_t>(src[j] >> 32));
-            mine += __double2ull_rz(static_cast<double>(s) * 4294967296.0);
-        }
-        unsigned long long total;
-        unsigned long long prefix = block_excl_scan_u64(mine, s_scan, &total);
-        double best_f = -INFINITY;
-        int best_K = 0x7FFFFFFF;
-        const unsigned long long base = static_cast<unsigned long long>(a.B) << 32;
-        for (int j = j0; j < j1; ++j) {
-            const float s = __uint_as_float(0xFFFFFFFFu - static_cast<uint32_t>(src[j] >> 32));
-            prefix += __double2ull_rz(static_cast<double>(s) * 4294967296.0);
-            const double f = __dmul_rn(static_cast<double>(base + prefix), a.sps[j]);
-            if (f > best_f) { best_f = f; best_K = j + 1; }      // ascending K: strict keeps smallest
-        }
-        // block argmax (larger f, then smaller K)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const double of = __shfl_xor_sync(0xFFFFFFFFu, best_f, o);
-            const int ok = __shfl_xor_sync(0xFFFFFFFFu, best_K, o);
-            if (of > best_f || (of == best_f && ok < best_K)) { best_f = of; best_K = ok; }
-        }
-        if (lane == 0) { s_bf[warp] = best_f; s_bk[warp] = best_K; }
-        __syncthreads();
-        if (tid == 0) {
-            double bf = s_bf[0];
-            int bk = s_bk[0];
-            for (int w = 1; w < kWarps; ++w)
-                if (s_bf[w] > bf || (s_bf[w] == bf && s_bk[w] < bk)) { bf = s_bf[w]; bk = s_bk[w]; }
-            if (bk == 0x7FFFFFFF) {          // every f was NaN
-                set_status(a.ws, DSPARK_STATUS_NUMERIC);
-                bk = 1;
-            }
-            s_K = bk;
-        }
+        K = choose_capacity<kThreads>(a, n, [&](int j) { return static_cast<uint32_t>(src[j] >> 32); },
+                                      s_wsum, s_bk, s_bK, &s_K);
     }
-    __syncthreads();
-    const int K = s_K;
 
     // ---- 4. fill ----
     for (int j = tid; j < n; j += kThreads) {
@@ -269,11 +652,21 @@ dspark_status launch_schedule(const float* cond_accept, const double* sps, int S
     a.B = B;
     a.N = N;
     a.K_in = K_in;
-    // one block: 256 threads are plenty for pools of up to 256 candidates
-    if (static_cast<long long>(B) * N <= 256)
-        schedule_kernel<256><<<1, 256, 0, stream>>>(a);
-    else
-        schedule_kernel<1024><<<1, 1024, 0, stream>>>(a);
+    const long long n = static_cast<long long>(B) * N;
+    if (n <= 32) {
+        schedule_warp_kernel<<<1, 32, 0, stream>>>(a);
+    } else if (n <= 256) {                    // one block: 256 threads are plenty for small pools
+        schedule_smem_kernel<256><<<1, 256, smem_schedule_bytes(static_cast<int>(n), 8), stream>>>(a);
+    } else if (n <= kSmemMaxCandidates) {
+        const size_t smem = smem_schedule_bytes(static_cast<int>(n), 32);
+        const cudaError_t e = cudaFuncSetAttribute(schedule_smem_kernel<1024>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem_schedule_bytes(kSmemMaxCandidates, 32)));
+        if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(schedule)");
+        schedule_smem_kernel<1024><<<1, 1024, smem, stream>>>(a);
+    } else {
+        schedule_global_kernel<<<1, 1024, 0, stream>>>(a);
+    }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "launch(schedule)");
     return DSPARK_OK;

@@ -5,20 +5,21 @@
 // correction from norm(max(0, p_t - p_d)); if all tested tokens pass, a bonus
 // token is drawn from p_t at the position after the block.
 //
-// S blocks per request (S = 1 when the batch alone fills the GPU, more when it
-// does not, so a single request still streams its 1-2 vocabulary rows at full
-// bandwidth).  Every block of request b:
-//   1. checks all tested positions k < L_b at once (one thread each):
-//      fl32(u_k * p_d[x_k]) < p_t[x_k]; k* = the smallest failing k
-//   2. streams its share of the residual (or bonus) row: each warp turns 128
-//      consecutive entries into integer masses q_v = floor(w_v * 2^40) and
-//      writes their sum to the workspace
-// The last block of the request to finish (an atomic counter) then
-//   3. sums the segment masses, t = floor(R * Q / 2^64), finds the segment
-//      holding t with a block-wide exclusive scan, re-reads that segment with
-//      one warp and picks the token with an inclusive warp scan.
-// Integer masses make the result independent of the summation order, so the
-// token equals the CPU reference bit for bit.
+// Two launches.  The decide kernel (one warp per request) checks all tested
+// positions k < L_b at once, one lane each: fl32(u_k * p_d[x_k]) < p_t[x_k];
+// k* = the smallest failing k.  The stream kernel (two blocks per SM, launched
+// as a programmatic dependent of the decide kernel so that its blocks are
+// resident before k* is known) cuts the B * ceil(V / 512) segments of the
+// rows to stream -- residual rows p_t[k*], p_d[k*] for a rejection, the bonus
+// row p_t[L_b] otherwise -- into equal contiguous ranges, one per block; each
+// warp turns 512 consecutive entries into integer masses q_v = floor(w_v * 2^40)
+// and writes their sum to the workspace.  The block that completes a request's
+// segment count (an atomic counter) then sums the segment masses,
+// t = floor(R * Q / 2^64), finds the segment holding t with a block-wide
+// exclusive scan, re-reads that segment with one warp (128 entries at a time)
+// and picks the token with an inclusive warp scan.  Integer masses make the
+// result independent of the summation order, so the token equals the CPU
+// reference bit for bit.
 #include "device_common.cuh"
 #include "host_common.h"
 
@@ -29,7 +30,8 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSeg = 128;                        // entries per warp segment (4 per lane)
+constexpr int kSeg = 512;                        // entries per warp segment (16 per lane)
+constexpr int kSlice = 128;                      // a segment is 4 slices of 4 consecutive entries per lane
 
 struct VerifyArgs {
     const float* p_t;
@@ -39,11 +41,13 @@ struct VerifyArgs {
     int32_t* out;
     int32_t* n_acc;
     WsHeader* ws;
-    uint32_t* done;              // [B] blocks finished per request
+    uint32_t* done;              // [B] segments finished per request
+    int32_t* decision;           // [B] (k* << 1) | rejected, or -1 for a request with bad input
     unsigned long long* seg;     // [B][n_seg] segment masses
     uint64_t seed;
     uint32_t offset;
-    int B, gamma, V, n_seg, splits;
+    int B, gamma, V, n_seg, grid;
+    long long total_seg;         // B * n_seg
 };
 
 // Four consecutive entries starting at e (a multiple of 4), zero past the end.
@@ -57,9 +61,20 @@ __device__ __forceinline__ float4 load4(const float* row, int e, int V, bool vec
     return f;
 }
 
-// q = floor(w * 2^40) for w in [0, 1]; w * 2^40 is exact, the conversion truncates.
+// q = floor(w * 2^40) for w >= 0 (never NaN: it comes out of fmaxf(0, .)), read off the
+// float's bits with integer operations only: w = m * 2^(e - 150) for a normal w with biased
+// exponent e and 24-bit significand m, so w * 2^40 = m * 2^(e - 110).  Subnormals give 0;
+// values whose product reaches 2^64 (only possible for w > 1, i.e. bad input) saturate as a
+// float-to-integer conversion would.  A float-to-u64 conversion runs on the FP64 pipe, which
+// is narrow on this GPU; this keeps the row stream memory-bound.
 __device__ __forceinline__ unsigned long long mass(float w) {
-    return __float2ull_rz(__fmul_rn(w, 0x1p40f));
+    const uint32_t bits = __float_as_uint(w) & 0x7FFFFFFFu;      // -0 (fmaxf may keep it) is 0
+    const int e = static_cast<int>(bits >> 23);
+    const unsigned long long m = (bits & 0x7FFFFFu) | 0x800000u;
+    const int sh = e - 110;
+    if (e == 0 || sh <= -24) return 0ull;
+    if (sh >= 41) return ~0ull;
+    return sh >= 0 ? m << sh : m >> -sh;
 }
 
 __device__ __forceinline__ void masses4(const float* rt, const float* rd, int e, int V, bool vec,
@@ -95,15 +110,31 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
     return x;
 }
 
-// Masses of segments [s0, s1) of the row into dst[segment].
+// Masses of segments [s0, s1) of the row into dst[segment], one warp per segment: a lane's
+// 16 entries are four float4 of each row, all loaded before any is used.
 __device__ void segment_sums(const float* rt, const float* rd, int V, bool vec, int s0, int s1,
                              unsigned long long* dst) {
     const uint32_t warp = warp_id(), lane = lane_id();
     for (int sgi = s0 + static_cast<int>(warp); sgi < s1; sgi += kWarps) {
-        unsigned long long q[4];
-        masses4(rt, rd, sgi * kSeg + 4 * static_cast<int>(lane), V, vec, q);
-        const unsigned long long s = warp_sum_u64(q[0] + q[1] + q[2] + q[3]);
-        if (lane == 0) dst[sgi] = s;
+        const int e0 = sgi * kSeg + 4 * static_cast<int>(lane);
+        float4 t[4], d[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t[i] = load4(rt, e0 + i * kSlice, V, vec);
+        if (rd != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] = load4(rd, e0 + i * kSlice, V, vec);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        unsigned long long sum = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sum += mass(fmaxf(0.f, __fsub_rn(t[i].x, d[i].x))) + mass(fmaxf(0.f, __fsub_rn(t[i].y, d[i].y))) +
+                   mass(fmaxf(0.f, __fsub_rn(t[i].z, d[i].z))) + mass(fmaxf(0.f, __fsub_rn(t[i].w, d[i].w)));
+        }
+        sum = warp_sum_u64(sum);
+        if (lane == 0) dst[sgi] = sum;
     }
 }
 
@@ -117,71 +148,63 @@ __device__ unsigned long long block_sum_u64(unsigned long long x, unsigned long 
     return s;
 }
 
-__global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
-    extern __shared__ unsigned long long s_seg[];         // [n_seg] (last block only)
-    __shared__ unsigned long long s_red[kWarps];
-    __shared__ unsigned long long s_scan[kWarps];
-    __shared__ int s_kstar, s_bad, s_pick, s_last;
-    __shared__ unsigned long long s_tloc;
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-    const int b = blockIdx.x / a.splits;
-    const int split = blockIdx.x % a.splits;
-    const int tid = threadIdx.x;
+constexpr int kDecideWarps = 8;                  // requests per decide block
+
+// k* of every request: one warp per request, one lane per tested position.
+__global__ void __launch_bounds__(kDecideWarps * 32) verify_decide_kernel(VerifyArgs a) {
+    griddep_launch_dependents();                 // the stream kernel may start launching now
+    const int b = static_cast<int>(blockIdx.x) * kDecideWarps + static_cast<int>(warp_id());
+    if (b >= a.B) return;
+    const uint32_t lane = lane_id();
     const int V = a.V, g = a.gamma;
+    const int Lb = a.lengths != nullptr ? a.lengths[b] : g;
+    bool bad = Lb < 0 || Lb > g;
+    int kmin = bad ? 0 : Lb;
+    if (!bad) {
+        for (int k = static_cast<int>(lane); k < Lb; k += 32) {
+            const int x = a.tokens[static_cast<size_t>(b) * g + k];
+            if (x < 0 || x >= V) {
+                bad = true;
+                continue;
+            }
+            const uint4 w = philox_at(a.seed, a.offset, 0u, static_cast<uint32_t>(b), kStreamAccept,
+                                      static_cast<uint32_t>(k));
+            const float u = uniform_from_word(w.x);
+            const float pd = a.p_d[(static_cast<size_t>(b) * g + k) * V + x];
+            const float pt = a.p_t[(static_cast<size_t>(b) * (g + 1) + k) * V + x];
+            if (!(__fmul_rn(u, pd) < pt)) kmin = min(kmin, k);
+        }
+    }
+    bad = __any_sync(0xFFFFFFFFu, bad);
+    kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+    if (lane == 0) {
+        a.decision[b] = bad ? -1 : ((kmin << 1) | (kmin < Lb ? 1 : 0));
+        if (bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+    }
+}
+
+// The last block to stream a request draws its token and writes its outputs.
+__device__ void finish_request(const VerifyArgs& a, int b, int dec, unsigned long long* s_seg,
+                               unsigned long long* s_red, unsigned long long* s_scan, int* s_pick,
+                               unsigned long long* s_tloc) {
+    const int tid = threadIdx.x;
+    const int V = a.V, g = a.gamma, n_seg = a.n_seg;
     int32_t* out = a.out + static_cast<size_t>(b) * (g + 1);
-
-    int Lb = a.lengths != nullptr ? a.lengths[b] : g;
-    if (tid == 0) {
-        s_kstar = (Lb >= 0 && Lb <= g) ? Lb : 0;
-        s_bad = (Lb < 0 || Lb > g) ? 1 : 0;
-        s_pick = -1;
-    }
-    __syncthreads();
-    if (s_bad) Lb = 0;
-
-    // ---- 1. ratio test at every tested position ----
-    for (int k = tid; k < Lb; k += kThreads) {
-        const int x = a.tokens[static_cast<size_t>(b) * g + k];
-        if (x < 0 || x >= V) {
-            atomicExch(&s_bad, 1);
-            continue;
-        }
-        const uint4 w = philox_at(a.seed, a.offset, 0u, static_cast<uint32_t>(b), kStreamAccept,
-                                  static_cast<uint32_t>(k));
-        const float u = uniform_from_word(w.x);
-        const float pd = a.p_d[(static_cast<size_t>(b) * g + k) * V + x];
-        const float pt = a.p_t[(static_cast<size_t>(b) * (g + 1) + k) * V + x];
-        if (!(__fmul_rn(u, pd) < pt)) atomicMin(&s_kstar, k);
-    }
-    __syncthreads();
-    if (s_bad) {
-        if (split == 0) {
-            if (tid == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
-            for (int k = tid; k <= g; k += kThreads) out[k] = -1;
-            if (tid == 0) a.n_acc[b] = 0;
-        }
+    if (dec < 0) {                               // bad input: nothing accepted, no token
+        for (int k = tid; k <= g; k += kThreads) out[k] = -1;
+        if (tid == 0) a.n_acc[b] = 0;
         return;
     }
-    const int kstar = s_kstar;
-    const bool rej = kstar < Lb;
-
-    // ---- 2. this block's share of the residual (or bonus) row ----
+    const int kstar = dec >> 1;
     const float* rt = a.p_t + (static_cast<size_t>(b) * (g + 1) + kstar) * V;
-    const float* rd = rej ? a.p_d + (static_cast<size_t>(b) * g + kstar) * V : nullptr;
+    const float* rd = (dec & 1) ? a.p_d + (static_cast<size_t>(b) * g + kstar) * V : nullptr;
     const bool vec = (V & 3) == 0;
-    const int n_seg = a.n_seg;
-    unsigned long long* seg = a.seg + static_cast<size_t>(b) * n_seg;
-    const int s0 = static_cast<int>((static_cast<long long>(split) * n_seg) / a.splits);
-    const int s1 = static_cast<int>((static_cast<long long>(split + 1) * n_seg) / a.splits);
-    segment_sums(rt, rd, V, vec, s0, s1, seg);
-
-    // ---- the last block of the request finishes it ----
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(a.done + b, 1u) == static_cast<uint32_t>(a.splits - 1);
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+    const unsigned long long* seg = a.seg + static_cast<size_t>(b) * n_seg;
 
     unsigned long long mine = 0;
     for (int s = tid; s < n_seg; s += kThreads) {
@@ -190,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
         mine += v;
     }
     unsigned long long Q = block_sum_u64(mine, s_red);
-    if (Q == 0 && rd != nullptr) {                 // residual without mass: use the p_t row
+    if (Q == 0 && rd != nullptr) {               // residual without mass: use the p_t row
         rd = nullptr;
         __syncthreads();
         segment_sums(rt, rd, V, vec, 0, n_seg, s_seg);
@@ -217,7 +240,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
         y = static_cast<int>(key_index(m));
         if (tid == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
     } else {
-        // ---- 3. inverse CDF: t = floor(R * Q / 2^64) ----
+        // ---- inverse CDF: t = floor(R * Q / 2^64) ----
         const uint4 w = philox_at(a.seed, a.offset, 0u, static_cast<uint32_t>(b), kStreamResample,
                                   static_cast<uint32_t>(kstar));
         const unsigned long long R = (static_cast<unsigned long long>(w.x) << 32) | w.y;
@@ -235,33 +258,44 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
         for (int s = r0; s < r1; ++s) {
             const unsigned long long sv = s_seg[s];
             if (before <= t && t < before + sv) {   // exactly one segment holds t
-                s_pick = s;
-                s_tloc = t - before;
+                *s_pick = s;
+                *s_tloc = t - before;
             }
             before += sv;
         }
         __syncthreads();
-        const int s = s_pick;
+        const int s = *s_pick;
         if (warp_id() == 0) {
-            const unsigned long long tl = s_tloc;
-            unsigned long long q[4];
-            masses4(rt, rd, s * kSeg + 4 * static_cast<int>(lane_id()), V, vec, q);
-            const unsigned long long lane_sum = q[0] + q[1] + q[2] + q[3];
-            const unsigned long long incl_l = warp_incl_scan_u64(lane_sum);
-            unsigned long long acc = incl_l - lane_sum;
-            int pick = -1;
-            for (int j = 0; j < 4; ++j) {
-                acc += q[j];
-                if (pick < 0 && acc > tl) pick = j;
+            // walk the segment's four 128-entry slices to the one holding tl, then pick inside it
+            unsigned long long tl = *s_tloc;
+            int pick_v = -1;
+            for (int i = 0; i < 4 && pick_v < 0; ++i) {
+                unsigned long long q[4];
+                const int e = s * kSeg + i * kSlice;
+                masses4(rt, rd, e + 4 * static_cast<int>(lane_id()), V, vec, q);
+                const unsigned long long lane_sum = q[0] + q[1] + q[2] + q[3];
+                const unsigned long long incl_l = warp_incl_scan_u64(lane_sum);
+                const unsigned long long slice = __shfl_sync(0xFFFFFFFFu, incl_l, 31);
+                if (tl >= slice) {
+                    tl -= slice;
+                    continue;
+                }
+                unsigned long long acc = incl_l - lane_sum;
+                int pick = -1;
+                for (int j = 0; j < 4; ++j) {
+                    acc += q[j];
+                    if (pick < 0 && acc > tl) pick = j;
+                }
+                const bool has = (incl_l - lane_sum <= tl) && (tl < incl_l);
+                const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, has);
+                const int src = __ffs(ballot) - 1;
+                const int pj = __shfl_sync(0xFFFFFFFFu, pick, src < 0 ? 0 : src);
+                pick_v = src < 0 ? -2 : e + 4 * src + pj;
             }
-            const bool has = (incl_l - lane_sum <= tl) && (tl < incl_l);
-            const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, has);
-            const int src = __ffs(ballot) - 1;
-            const int pj = __shfl_sync(0xFFFFFFFFu, pick, src < 0 ? 0 : src);
-            if (lane_id() == 0) s_pick = src < 0 ? -1 : s * kSeg + 4 * src + pj;
+            if (lane_id() == 0) *s_pick = pick_v < 0 ? -1 : pick_v;
         }
         __syncthreads();
-        y = s_pick;
+        y = *s_pick;
         if (y < 0 || y >= V) {            // cannot happen when Q > 0; kept as a guard
             if (tid == 0) set_status(a.ws, DSPARK_STATUS_INTERNAL);
             y = 0;
@@ -278,6 +312,49 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(VerifyArgs a) {
     if (tid == 0) a.n_acc[b] = kstar;
 }
 
+// Streams block blockIdx.x's contiguous range of the B * n_seg row segments.
+__global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(VerifyArgs a) {
+    extern __shared__ unsigned long long s_seg[];         // [n_seg] (finishing blocks only)
+    __shared__ unsigned long long s_red[kWarps];
+    __shared__ unsigned long long s_scan[kWarps];
+    __shared__ int s_pick, s_last;
+    __shared__ unsigned long long s_tloc;
+
+    const int tid = threadIdx.x;
+    const int V = a.V, g = a.gamma, n_seg = a.n_seg;
+    const bool vec = (V & 3) == 0;
+    const long long T = a.total_seg;
+    long long f = T * blockIdx.x / a.grid;
+    const long long f1 = T * (blockIdx.x + 1) / a.grid;
+
+    griddep_wait();                                       // every k* is written and visible
+    while (f < f1) {
+        const int b = static_cast<int>(f / n_seg);
+        const int s0 = static_cast<int>(f - static_cast<long long>(b) * n_seg);
+        const int s1 = static_cast<int>(min(static_cast<long long>(n_seg), s0 + (f1 - f)));
+        const int dec = a.decision[b];
+        if (dec >= 0) {
+            const int kstar = dec >> 1;
+            const float* rt = a.p_t + (static_cast<size_t>(b) * (g + 1) + kstar) * V;
+            const float* rd = (dec & 1) ? a.p_d + (static_cast<size_t>(b) * g + kstar) * V : nullptr;
+            segment_sums(rt, rd, V, vec, s0, s1, a.seg + static_cast<size_t>(b) * n_seg);
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const uint32_t cnt = static_cast<uint32_t>(s1 - s0);
+            s_last = atomicAdd(a.done + b, cnt) + cnt == static_cast<uint32_t>(n_seg);
+        }
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            finish_request(a, b, dec, s_seg, s_red, s_scan, &s_pick, &s_tloc);
+            __syncthreads();                              // shared scratch is reused by the next request
+        }
+        f += s1 - s0;
+    }
+}
+
 int n_segments(int V) { return (V + kSeg - 1) / kSeg; }
 
 size_t done_bytes(int B) { return (sizeof(uint32_t) * static_cast<size_t>(B) + 15) & ~static_cast<size_t>(15); }
@@ -285,7 +362,7 @@ size_t done_bytes(int B) { return (sizeof(uint32_t) * static_cast<size_t>(B) + 1
 }  // namespace
 
 size_t verify_workspace_bytes(int B, int V) {
-    return sizeof(WsHeader) + done_bytes(B) + sizeof(unsigned long long) * static_cast<size_t>(B) * n_segments(V);
+    return sizeof(WsHeader) + 2 * done_bytes(B) + sizeof(unsigned long long) * static_cast<size_t>(B) * n_segments(V);
 }
 
 dspark_status launch_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,
@@ -300,7 +377,7 @@ dspark_status launch_verify(const float* p_target, const float* p_draft, const i
     }
     dspark_status st = clear_workspace(ws, sizeof(WsHeader) + done_bytes(B), stream);
     if (st != DSPARK_OK) return st;
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(verify)");
     VerifyArgs a;
@@ -311,24 +388,39 @@ dspark_status launch_verify(const float* p_target, const float* p_draft, const i
     a.out = out_tokens;
     a.n_acc = num_accepted;
     a.ws = static_cast<WsHeader*>(ws);
-    a.done = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader));
-    a.seg = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + sizeof(WsHeader) + done_bytes(B));
+    uint8_t* p = static_cast<uint8_t*>(ws) + sizeof(WsHeader);
+    a.done = reinterpret_cast<uint32_t*>(p);
+    a.decision = reinterpret_cast<int32_t*>(p + done_bytes(B));
+    a.seg = reinterpret_cast<unsigned long long*>(p + 2 * done_bytes(B));
     a.seed = seed;
     a.offset = offset;
     a.B = B;
     a.gamma = gamma;
     a.V = V;
     a.n_seg = n_seg;
-    // enough blocks to cover the GPU twice, but at least 8 segments (1024 entries) per block
-    a.splits = B >= dev.sm_count ? 1 : std::max(1, std::min((2 * dev.sm_count + B - 1) / B, n_seg / 8));
-    const long long grid = static_cast<long long>(B) * a.splits;
-    if (grid > 0x7FFFFFFFLL) {
-        set_error("verify: too many requests (%d)", B);
-        return DSPARK_ERR_UNSUPPORTED;
-    }
-    verify_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+    a.total_seg = static_cast<long long>(B) * n_seg;
+    // two resident blocks per SM, each streaming at least 2 segments (1024 row entries)
+    a.grid = static_cast<int>(std::max(1LL, std::min(2LL * dev.sm_count, (a.total_seg + 1) / 2)));
+
+    const unsigned decide_grid = static_cast<unsigned>((B + kDecideWarps - 1) / kDecideWarps);
+    verify_decide_kernel<<<decide_grid, kDecideWarps * 32, 0, stream>>>(a);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "launch(verify)");
+    if (e != cudaSuccess) return cuda_error(e, "launch(verify decide)");
+
+    // programmatic dependent launch: the stream kernel's blocks become resident while the
+    // decide kernel runs and wait (griddepcontrol.wait) for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, verify_stream_kernel, a);
+    if (e != cudaSuccess) return cuda_error(e, "launch(verify stream)");
     return DSPARK_OK;
 }
 

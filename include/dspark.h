@@ -81,7 +81,7 @@ typedef enum {
  * does not use are ignored:
  *   DSPARK_OP_DRAFT_LOGITS  256 (the status word)
  *   DSPARK_OP_MARKOV_SAMPLE grows with B*N and B (argmax slots, bounds, lse partials)
- *   DSPARK_OP_VERIFY        grows with B*V/128 (per-128-entry integer masses); N = gamma
+ *   DSPARK_OP_VERIFY        grows with B*V/512 (per-512-entry integer masses); N = gamma
  *   DSPARK_OP_SCHEDULE      grows with B*N (radix-sort key buffers)
  * Returns 0 for an unknown op or negative sizes.
  */
@@ -171,6 +171,8 @@ DSPARK_API dspark_status dspark_markov_sample(const float* base_logits, const in
  * offset < 2^32; p_target/p_draft 16-byte aligned.
  * Device-side: a token or length out of range sets INPUT_RANGE (the request
  * outputs num_accepted 0 and -1 tokens).
+ * Launches two kernels on `stream`, the second as a programmatic dependent
+ * launch of the first (both are captured by CUDA stream capture).
  * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY, ...) bytes.
  */
 DSPARK_API dspark_status dspark_verify(const float* p_target, const float* p_draft,

@@ -61,3 +61,64 @@ def test_out_of_range_confidences_are_clamped_and_flagged(cuda_lib):
     c = np.array([[0.9, 1.5, 0.5], [np.nan, 0.3, -0.2]], np.float32)
     ref, st, bits = _check(cuda_lib, c, sps_table(6), -1)
     assert ref["clamped"] and bits & cuda_lib.STATUS_INPUT_RANGE
+
+
+@pytest.mark.parametrize("B,N", [(16, 16), (257, 1), (32, 32), (41, 25), (1023, 16), (1, 16384)])
+def test_pool_sizes_around_block_and_round_edges(cuda_lib, B, N):
+    """Pools at and just past 256 and 1024 candidates, ragged warp runs, the 16384 maximum
+    of the shared-memory sort with a single request."""
+    rng = np.random.default_rng(B * 1000 + N)
+    c = rng.beta(4, 1.5, size=(B, N)).astype(np.float32)
+    c[rng.random((B, N)) < 0.15] = 1.0
+    _check(cuda_lib, c, sps_table(B * N), -1)
+
+
+def test_large_pool_beyond_shared_memory(cuda_lib):
+    """B*N = 17600 > 16384: the keys live in the workspace."""
+    rng = np.random.default_rng(7)
+    c = rng.beta(5, 2, size=(1100, 16)).astype(np.float32)
+    c[rng.random(c.shape) < 0.1] = 1.0
+    _check(cuda_lib, c, sps_table(16384), -1)
+    _check(cuda_lib, c, None, 12345)
+
+
+@pytest.mark.parametrize("B,N", [(64, 16), (1100, 16)])
+def test_objective_with_special_sps_values(cuda_lib, B, N):
+    """SPS entries that are zero, subnormal, negative, infinite, NaN, or so large or small that
+    the product overflows or leaves the normal range: K must still match the oracle's fp64."""
+    rng = np.random.default_rng(11 + B)
+    c = rng.beta(3, 1, size=(B, N)).astype(np.float32)
+    S = B * N
+    sps = sps_table(S).copy()
+    specials = np.array([0.0, -0.0, 5e-324, 1e-310, -3.0, np.inf, -np.inf, np.nan, 1e300, 1.7e308,
+                         1e-300, 2.2250738585072014e-308 * 1.5], np.float64)
+    pos = rng.choice(S, size=S // 4, replace=False)
+    sps[pos] = rng.choice(specials, size=pos.size)
+    _check(cuda_lib, c, sps, -1)
+    # every entry NaN or -inf: nothing beats -inf, K = 1 and the numeric flag is raised
+    sps_bad = np.where(rng.random(S) < 0.5, np.nan, -np.inf)
+    ref, st, bits = _check(cuda_lib, c, sps_bad, -1)
+    assert ref["K"] == 1 and bits & cuda_lib.STATUS_NUMERIC
+
+
+def test_negative_zero_confidence_is_zero(cuda_lib):
+    """-0.0 and +0.0 survivals are one value: ties are broken by position, as for any tie."""
+    c = np.array([[0.5, -0.0, 0.7], [0.0, 0.9, 0.3], [-0.0, 0.0, 1.0]], np.float32)
+    _check(cuda_lib, c, sps_table(9), -1)
+    _check(cuda_lib, c, None, 7)
+
+
+@pytest.mark.parametrize("B,N", [(1, 1), (1, 8), (4, 8), (32, 1), (3, 10), (2, 16), (1, 32), (5, 6)])
+@pytest.mark.parametrize("K_in", [-1, 0, 5, 40])
+def test_pools_of_at_most_32_candidates(cuda_lib, B, N, K_in):
+    """One-warp pools (a few decode requests), with ties, special SPS entries and fixed K."""
+    rng = np.random.default_rng(B * 100 + N + K_in)
+    c = rng.beta(3, 1, size=(B, N)).astype(np.float32)
+    c[rng.random((B, N)) < 0.3] = 1.0
+    c[rng.random((B, N)) < 0.1] = 0.0
+    sps = None
+    if K_in < 0:
+        sps = sps_table(B * N + 3)
+        sps[rng.random(sps.size) < 0.2] = np.nan
+        sps[rng.random(sps.size) < 0.1] = 0.0
+    _check(cuda_lib, c, sps, K_in)

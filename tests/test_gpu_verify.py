@@ -115,3 +115,32 @@ def test_zero_mass_and_bad_inputs_set_status(cuda_lib):
     assert bits & cuda_lib.STATUS_INPUT_RANGE and nacc[0] == 0 and np.all(out == -1)
     out, nacc, st, bits = _gpu(cuda_lib, p_t, p_d, np.array([[1]]), np.array([2]), 0, 0)
     assert bits & cuda_lib.STATUS_INPUT_RANGE
+
+
+@pytest.mark.parametrize("V", [700, 151936])
+def test_sparse_rows_with_signed_zeros_exact(cuda_lib, V):
+    """Rows where most entries are +0 or -0 (top-k truncated distributions): a -0 probability has
+    no mass, exactly as +0; the residual often lives in a handful of segments."""
+    rng = np.random.default_rng(V + 17)
+    B, g = 24, 5
+    p_t = np.zeros((B, g + 1, V), np.float32)
+    p_d = np.zeros((B, g, V), np.float32)
+    for b in range(B):
+        for k in range(g + 1):
+            sup = rng.choice(V, size=8, replace=False)
+            w = rng.random(8).astype(np.float32)
+            p_t[b, k, sup] = w / w.sum()
+            if k < g:
+                sup_d = np.concatenate([sup[:4], rng.choice(V, size=4, replace=False)])
+                wd = rng.random(8).astype(np.float32)
+                p_d[b, k, sup_d] = wd / wd.sum()
+    neg = rng.random(p_t.shape) < 0.3
+    p_t[neg & (p_t == 0)] = -0.0
+    negd = rng.random(p_d.shape) < 0.3
+    p_d[negd & (p_d == 0)] = -0.0
+    x = np.empty((B, g), np.int32)
+    for b in range(B):
+        for k in range(g):
+            pk = np.abs(p_d[b, k]).astype(np.float64)
+            x[b, k] = rng.choice(V, p=pk / pk.sum())
+    _check_exact(cuda_lib, p_t, p_d, x, None, 31, 4)
