@@ -11,13 +11,20 @@ namespace markov {
 
 constexpr int kMaxGrid = 1024;                         // workspace is sized for this many blocks
 constexpr uint32_t kWaitStep = 0x200;                  // + step index (grid barrier)
+constexpr int kExchangeMaxBN = 64;                     // B * N limit of the candidate exchange
 
 struct MarkovLayout {
     unsigned long long* slots;   // [N][B] argmax keys
     uint32_t* lb;                // [N][B] order bits of the published lower bound
     uint32_t* pub;               // [N] blocks that have published their bounds (tensor path)
+    unsigned long long* cand;    // [N][grid][B] per-block candidates (exchange; B * N <= kExchangeMaxBN)
     float2* lse_part;            // [2][kMaxGrid][B] (max, sum) partials
 };
+
+__host__ __device__ inline size_t markov_cand_entries(int B, int N) {
+    return static_cast<size_t>(B) * N <= static_cast<size_t>(kExchangeMaxBN)
+               ? static_cast<size_t>(N) * kMaxGrid * B : 0;
+}
 
 __host__ __device__ inline MarkovLayout markov_layout(void* ws, int B, int N) {
     uint8_t* p = static_cast<uint8_t*>(ws) + sizeof(WsHeader);
@@ -29,6 +36,8 @@ __host__ __device__ inline MarkovLayout markov_layout(void* ws, int B, int N) {
     L.pub = reinterpret_cast<uint32_t*>(p);
     p += sizeof(uint32_t) * static_cast<size_t>(N);
     p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15));
+    L.cand = reinterpret_cast<unsigned long long*>(p);
+    p += sizeof(unsigned long long) * markov_cand_entries(B, N);
     L.lse_part = reinterpret_cast<float2*>(p);
     return L;
 }
@@ -51,6 +60,9 @@ struct MarkovArgs {
     int w2_pitch;               // bytes per cached w2 row (padded)
     int z_stored;               // z rows live in shared memory
     int single_pass;            // noise on every element in one pass (few elements per block)
+    int exchange;               // blocks publish per-step candidates and poll each other's
+                                // (instead of step slots and a grid barrier)
+    int w2_split;               // cached w2 rows stored even rows first, then odd rows
     long long timeout_ns;
 };
 

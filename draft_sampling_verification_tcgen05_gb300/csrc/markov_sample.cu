@@ -149,6 +149,13 @@ __device__ __forceinline__ float2 block_lse(float2 v, float2* red) {
 }
 
 
+// Shared-memory slot of local w2 row t.  With w2_split the even rows come first and the odd
+// rows after them, so the threads of a warp that take adjacent row pairs (2t, 2t+1) read
+// consecutive slots: no bank conflicts with the 16-byte row padding.
+__device__ __forceinline__ int w2_slot(const MarkovArgs& a, int t) {
+    return a.w2_split ? ((t & 1) ? (a.slice >> 1) + (t >> 1) : (t >> 1)) : t;
+}
+
 template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -157,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     __shared__ float2 s_red2[kWarps];
     __shared__ float s_bcast[2];
     __shared__ float s_temp[256];                     // temperatures of the first 256 requests
+    __shared__ unsigned long long s_win[kExchangeMaxBN];  // exchange: the step's best key per request
+    __shared__ int s_tok[kExchangeMaxBN];                  // exchange: winners [step][request]
 
     const int v_lo = blockIdx.x * a.slice;
     const int v_hi = min(a.V, v_lo + a.slice);
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         // asynchronous 16-byte copies (many in flight); completed before step 0's first pass
         for (int idx = tid; idx < n_local * chunks; idx += kThreads) {
             const int v = idx / chunks, c = idx % chunks;
-            const uint32_t dst = smem_u32(w2s + static_cast<size_t>(v) * a.w2_pitch + 16 * c);
+            const uint32_t dst = smem_u32(w2s + static_cast<size_t>(w2_slot(a, v)) * a.w2_pitch + 16 * c);
             const uint8_t* g = src + static_cast<size_t>(v) * row_bytes + 16 * c;
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(g) : "memory");
         }
@@ -189,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     }
 
     for (int b = tid; b < 256 && b < a.B; b += kThreads) s_temp[b] = __ldg(a.temperature + b);
+    if (a.exchange)
+        for (int b = tid; b < a.B; b += kThreads) s_win[b] = 0ull;
     // Decode fast path (one request, one pair of entries per thread): the base logits and
     // the noise of step i+1 do not depend on the token of step i, so they are fetched and
     // drawn while the block waits at step i's grid barrier.
@@ -224,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                     p = 0;
                 }
             } else {
-                p = slot_token(a, i - 1, b);
+                p = a.exchange ? s_tok[(i - 1) * a.B + b] : slot_token(a, i - 1, b);
             }
             prev[b] = p;
         }
@@ -262,9 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 for (int t = 2 * tid; t < n_local; t += 2 * kThreads) {
                     const int v = v_lo + t;
                     const bool two = t + 1 < n_local;
-                    const uint8_t* wrow0 = a.w2_cached ? w2s + static_cast<size_t>(t) * a.w2_pitch
+                    const uint8_t* wrow0 = a.w2_cached ? w2s + static_cast<size_t>(w2_slot(a, t)) * a.w2_pitch
                                                        : static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v) * row_bytes;
-                    const uint8_t* wrow1 = a.w2_cached ? wrow0 + a.w2_pitch : wrow0 + row_bytes;
+                    const uint8_t* wrow1 = a.w2_cached ? w2s + static_cast<size_t>(w2_slot(a, t + 1)) * a.w2_pitch
+                                                       : wrow0 + row_bytes;
                     float b0, b1;
                     bias_dot2<WT>(wrow0, two ? wrow1 : wrow0, e, a.r, b0, b1);
                     float l0, l1, g0, g1;
@@ -298,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             } else
             for (int t = tid; t < n_local; t += kThreads) {
                 const int v = v_lo + t;
-                const uint8_t* wrow = a.w2_cached ? w2s + static_cast<size_t>(t) * a.w2_pitch
+                const uint8_t* wrow = a.w2_cached ? w2s + static_cast<size_t>(w2_slot(a, t)) * a.w2_pitch
                                                   : static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v) * row_bytes;
                 const float bias = bias_dot<WT>(wrow, e, a.r);
                 const float s = __fadd_rn(__ldcs(lrow + v), bias);
@@ -328,10 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                     const float y = __fadd_rn(zb, gumbel_at(a, b, i, static_cast<int>(vb)));
                     atomicMax(lbs + b, float_order_bits(y));
                     atomicMax(slot + b, argmax_key(y, vb));
-                } else {
+                } else if (!a.exchange) {
                     atomicMax(slot + b, best);
                 }
             }
+            if (a.exchange && tid == 0)   // 1 = this block has no finite candidate (below every key)
+                st_release_u64(a.lay.cand + (static_cast<size_t>(i) * gridDim.x + blockIdx.x) * a.B + b,
+                               best != 0ull ? best : 1ull);
             if (!hot || a.single_pass) continue;
 
             // ---- 3. pass 2: Gumbel noise where the element can still win ----
@@ -346,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 if (a.z_stored) {
                     z = zs[static_cast<size_t>(b) * a.slice + t];
                 } else {
-                    const uint8_t* wrow = a.w2_cached ? w2s + static_cast<size_t>(t) * a.w2_pitch
+                    const uint8_t* wrow = a.w2_cached ? w2s + static_cast<size_t>(w2_slot(a, t)) * a.w2_pitch
                                                       : static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v) * row_bytes;
                     z = __fmul_rn(__fadd_rn(__ldg(lrow + v), bias_dot<WT>(wrow, e, a.r)), invT);
                 }
@@ -361,17 +376,53 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         }
 
         // ---- 4. all blocks agree on the step's winners ----
-        grid_arrive(a.ws);
-        if (fast && i + 1 < a.N) prepare(i + 1);
-        alive = grid_wait(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i);
+        if (a.exchange) {
+            // every block's candidates for this step, polled (bounded) and reduced here
+            if (fast && i + 1 < a.N) prepare(i + 1);
+            const int n_ent = static_cast<int>(gridDim.x) * a.B;
+            const unsigned long long* cs = a.lay.cand + static_cast<size_t>(i) * n_ent;
+            int fail = 0;
+            for (int e = tid; e < n_ent; e += kThreads) {
+                unsigned long long k = ld_acquire_u64(cs + e);
+                const long long t0 = global_ns();
+                uint32_t spins = 0;
+                while (k == 0ull) {
+                    if ((++spins & 63u) == 0) {
+                        if (aborted(a.ws)) { fail = 1; break; }
+                        if (global_ns() - t0 > a.timeout_ns) {
+                            atomicOr(&a.ws->status, DSPARK_STATUS_TIMEOUT);
+                            atomicExch(&a.ws->detail, kWaitStep + static_cast<uint32_t>(i));
+                            fail = 1;
+                            break;
+                        }
+                    }
+                    k = ld_acquire_u64(cs + e);
+                }
+                if (k > 1ull) atomicMax(&s_win[e % a.B], k);
+            }
+            alive = __syncthreads_or(fail) == 0;
+            for (int b = tid; b < a.B; b += kThreads) {
+                const unsigned long long k = s_win[b];
+                int x = 0;
+                if (k == 0ull) set_status(a.ws, DSPARK_STATUS_NUMERIC);    // no finite candidate at all
+                else x = static_cast<int>(key_index(k));
+                s_tok[i * a.B + b] = x;
+                s_win[b] = 0ull;
+            }
+        } else {
+            grid_arrive(a.ws);
+            if (fast && i + 1 < a.N) prepare(i + 1);
+            alive = grid_wait(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i);
+        }
     }
     if (!alive) return;
     __threadfence();
     finish_lse(a, a.N - 1, tid, kThreads);
     if (blockIdx.x == 0) {
+        if (a.exchange) __syncthreads();          // the last step's winners, written by other threads
         for (int idx = tid; idx < a.B * a.N; idx += kThreads) {
             const int b = idx / a.N, i = idx % a.N;
-            a.tokens[idx] = slot_token(a, i, b);
+            a.tokens[idx] = a.exchange ? s_tok[i * a.B + b] : slot_token(a, i, b);
         }
     }
 }
@@ -390,6 +441,11 @@ dspark_status run_generic(MarkovArgs& a, cudaStream_t stream, const DeviceInfo& 
     // at most 8 elements per thread and step: one pass with noise on every element is
     // cheaper than publishing a bound and making a second pass
     a.single_pass = static_cast<size_t>(a.slice) * a.B <= static_cast<size_t>(8 * kThreads);
+    // few requests and steps, one pass: blocks trade candidates directly (one poll per block
+    // and request) instead of atomics on step slots plus a grid barrier
+    a.exchange = a.single_pass && a.lse == nullptr && markov_cand_entries(a.B, a.N) > 0 &&
+                 static_cast<long long>(grid) * a.B <= kThreads;
+    a.w2_split = a.w2_cached && (a.slice % 2 == 0);
     if (static_cast<size_t>(a.B) * a.r > static_cast<size_t>(kMaxEFloats)) {
         set_error("markov_sample: B*r = %d exceeds the %d the sampler holds on chip", a.B * a.r, kMaxEFloats);
         return DSPARK_ERR_UNSUPPORTED;
@@ -435,6 +491,7 @@ size_t markov_workspace_bytes(int B, int N) {
     size_t bytes = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t) +
                    sizeof(uint32_t) * static_cast<size_t>(N);
     bytes = (bytes + 15) & ~static_cast<size_t>(15);
+    bytes += sizeof(unsigned long long) * markov_cand_entries(B, N);
     bytes += 2 * static_cast<size_t>(kMaxGrid) * B * sizeof(float2);
     return bytes;
 }
@@ -444,10 +501,12 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
                                    uint64_t seed, uint32_t offset, int B, int N, int V, int r,
                                    int32_t* draft_tokens, float* lse, void* ws, cudaStream_t stream,
                                    const DeviceInfo& dev) {
-    // clear header, slots and bounds (the lse partials need no clearing)
-    const size_t nb = static_cast<size_t>(B) * N;
-    const size_t clear = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t) +
-                         sizeof(uint32_t) * static_cast<size_t>(N);
+    // clear header, slots, bounds, publication counters and the candidate entries a grid of
+    // at most one block per SM uses (the lse partials need no clearing)
+    const MarkovLayout lay = markov_layout(ws, B, N);
+    size_t clear = static_cast<size_t>(reinterpret_cast<uint8_t*>(lay.cand) - static_cast<uint8_t*>(ws));
+    if (markov_cand_entries(B, N) > 0)
+        clear += sizeof(unsigned long long) * static_cast<size_t>(N) * std::min(dev.sm_count, kMaxGrid) * B;
     dspark_status st = clear_workspace(ws, clear, stream);
     if (st != DSPARK_OK) return st;
     MarkovArgs a = {};

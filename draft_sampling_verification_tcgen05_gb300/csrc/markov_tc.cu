@@ -48,8 +48,10 @@ constexpr int kLStages = 3;                      // upper bound per epilogue gro
 constexpr int kTileV = 128;
 constexpr int kChunk = 16;                       // requests per epilogue chunk
 constexpr int kMaxLocalTiles = 32;
+constexpr int kZtPitch = 36;                     // floats per request row of the transpose buffer (no bank conflicts)
 constexpr uint32_t kW2StageBytes = kTileV * 128;             // 128 rows x 64 bf16
 constexpr uint32_t kLStageBytes = kTileV * kChunk * 4;       // 16 requests x 128 fp32
+constexpr uint32_t kGtabBytes = 256 * 32 * 4;                // bound table, one copy per bank
 constexpr uint32_t kBarStep = 1;
 constexpr uint32_t kBarGroup0 = 2;
 constexpr uint32_t kBarEpi = kBarGroup0 + kGroups;   // all epilogue warps
@@ -92,6 +94,29 @@ __device__ __noinline__ unsigned long long rare_candidate(uint64_t seed, uint32_
     return (y == y) ? argmax_key(y, v) : 0ull;
 }
 
+// Half h of a tile-chunk seen transposed: the warp holds z for its 32 rows (one per lane) and 16
+// requests (r[0..15], from TMEM); afterwards lane (jj = lane >> 2, q = lane & 3) holds z of rows
+// 8q..8q+7 for request 8h + jj -- the 8 entries whose noise comes from one Philox counter.
+__device__ __forceinline__ void transpose_half(float* zt, const uint32_t (&r)[16], int h, uint32_t lane,
+                                               float (&zz)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) zt[j * kZtPitch + static_cast<int>(lane)] = __uint_as_float(r[8 * h + j]);
+    __syncwarp();
+    const float* src = zt + (lane >> 2) * kZtPitch + 8 * (lane & 3u);
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 b = *reinterpret_cast<const float4*>(src + 4);
+    __syncwarp();
+    zz[0] = a.x; zz[1] = a.y; zz[2] = a.z; zz[3] = a.w;
+    zz[4] = b.x; zz[5] = b.y; zz[6] = b.z; zz[7] = b.w;
+}
+
+// High half (16 bits) of entry k (0..7) of a Philox block of 8 entries: even entries in the low
+// 16 bits of word k/2.
+__device__ __forceinline__ uint32_t half_of(const uint4& w, int k) {
+    const uint32_t word = (k >> 1) == 0 ? w.x : (k >> 1) == 1 ? w.y : (k >> 1) == 2 ? w.z : w.w;
+    return (word >> (16 * (k & 1))) & 0xFFFFu;
+}
+
 __global__ void __launch_bounds__(kThreadsTC, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmL,
                  MarkovArgs a, TcArgs t) {
@@ -100,7 +125,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* w2s = base;
     uint8_t* Ls = w2s + t.w2_stages * kW2StageBytes;
-    uint8_t* Es = Ls + kGroups * t.l_stages * kLStageBytes;
+    // gtab[k][lane]: bound on g for a noise word with top byte k, replicated across the 32 banks
+    // so that a warp's lookups with random k never conflict
+    float* gtab = reinterpret_cast<float*>(Ls + kGroups * t.l_stages * kLStageBytes);
+    uint8_t* Es = Ls + kGroups * t.l_stages * kLStageBytes + kGtabBytes;
 
     __shared__ uint64_t bar_w2_full[kW2Stages], bar_w2_empty[kW2Stages];
     __shared__ uint64_t bar_L_full[kGroups][kLStages], bar_L_empty[kGroups][kLStages];
@@ -111,9 +139,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ float s_lb[kGroups][kChunk];
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
     __shared__ unsigned long long s_best[kGroups][kChunk];
-    __shared__ float s_gtab[256];                                      // bound on g per top byte
-    __shared__ __align__(16) uint16_t s_hi[kEpiWarps][kChunk][32];    // high halves of a tile-chunk
-    __shared__ uint32_t s_mask[kEpiWarps][kChunk];                     // elements that pass the z test
+    __shared__ __align__(16) float s_zt[kEpiWarps][8 * kZtPitch];      // z of 8 requests x 32 rows, transposed
     __shared__ int s_ok;
 
     const uint32_t warp = warp_id(), lane = lane_id();
@@ -156,11 +182,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         s_invT[b] = inv;
     }
     if (bad_t) set_status(a.ws, DSPARK_STATUS_NUMERIC);
-    // s_gtab[k] bounds the variate of every word whose top byte is k: the variate of
+    // gtab[k][.] bounds the variate of every word whose top byte is k: the variate of
     // the largest such word (it increases with the word) plus a margin for logf's
     // rounding; the top bin is capped by the global bound
-    for (int k = threadIdx.x; k < 256; k += kThreadsTC)
-        s_gtab[k] = k == 255 ? kGumbelMax : gumbel_from_word((static_cast<uint32_t>(k + 1) << 24) - 1u) + 1e-3f;
+    for (int k = threadIdx.x; k < 256; k += kThreadsTC) {
+        const float g = k == 255 ? kGumbelMax : gumbel_from_word((static_cast<uint32_t>(k + 1) << 24) - 1u) + 1e-3f;
+        for (int l = 0; l < 32; ++l) gtab[k * 32 + l] = g;
+    }
     {   // zero E once: padding rows (b >= B) stay zero for the whole call
         uint4* e4 = reinterpret_cast<uint4*>(Es);
         const int n16 = Bp * a.r * 2 / 16;
@@ -417,66 +445,56 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 #pragma unroll
                     for (int j = 0; j < kChunk; ++j) any |= s_lb[grp][j] < INFINITY;
                     if (any && !dead) {
-                        uint16_t (*hs)[32] = s_hi[epi];
-                        uint32_t* sm = s_mask[epi];
+                        // lane (jj, q) takes rows 8q..8q+7 of requests jj and 8 + jj: one Philox
+                        // block each, both drawn (independent chains, interleaved) as soon as one
+                        // of the 16 entries passes the z test
+                        const int jj = static_cast<int>(lane >> 2), q = static_cast<int>(lane & 3u);
+                        const float lb0 = s_lb[grp][jj], lb1 = s_lb[grp][8 + jj];
+                        const int b0 = c * kChunk + jj, b1 = b0 + 8;
                         for (int tl = 0; tl < nt; ++tl) {
-                            const int v0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32);
-                            const int v = v0 + static_cast<int>(lane);
+                            const int v0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32) + 8 * q;
                             const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
                             uint32_t r[kChunk];
                             tmem_ld16(taddr, r);
                             tmem_wait_ld();
-                            uint32_t m[kChunk];
-                            uint32_t anym = 0;
+                            float z0[8], z1[8];
+                            transpose_half(s_zt[epi], r, 0, lane, z0);
+                            transpose_half(s_zt[epi], r, 1, lane, z1);
+                            uint32_t p0 = 0, p1 = 0;
 #pragma unroll
-                            for (int j = 0; j < kChunk; ++j) {
-                                const bool pass = v < a.V && __fadd_rn(__uint_as_float(r[j]), kGumbelMax) >= s_lb[grp][j];
-                                m[j] = __ballot_sync(0xFFFFFFFFu, pass);
-                                anym |= m[j];
-                                if (lane == 0) sm[j] = m[j];
+                            for (int k = 0; k < 8; ++k) {
+                                const bool in = v0 + k < a.V;
+                                p0 |= (in && __fadd_rn(z0[k], kGumbelMax) >= lb0 ? 1u : 0u) << k;
+                                p1 |= (in && __fadd_rn(z1[k], kGumbelMax) >= lb1 ? 1u : 0u) << k;
                             }
-                            if (anym == 0u) continue;
-                            __syncwarp();
-                            // lane l: counter (v0 >> 3) + (l & 3) for requests (l >> 2) and (l >> 2) + 8
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int jj = static_cast<int>(lane >> 2) + 8 * h;
-                                const int q = static_cast<int>(lane & 3u);
-                                if ((sm[jj] >> (8 * q)) & 0xFFu) {
-                                    const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>((v0 >> 3) + q),
-                                                              static_cast<uint32_t>(c * kChunk + jj), kStreamGumbel,
-                                                              static_cast<uint32_t>(i));
-                                    // 8 high halves in element order (even entry in the low 16 bits)
-                                    *reinterpret_cast<uint4*>(&hs[jj][8 * q]) = w;
-                                }
-                            }
-                            __syncwarp();
-                            // straight-line: a table bound on g from the top byte of the high half
+                            if ((p0 | p1) == 0u) continue;
+                            const uint4 w0 = philox_at(a.seed, a.offset, static_cast<uint32_t>(v0 >> 3),
+                                                       static_cast<uint32_t>(b0), kStreamGumbel, static_cast<uint32_t>(i));
+                            const uint4 w1 = philox_at(a.seed, a.offset, static_cast<uint32_t>(v0 >> 3),
+                                                       static_cast<uint32_t>(b1), kStreamGumbel, static_cast<uint32_t>(i));
+                            // straight-line: the table bound on g from the top byte of each high half
                             uint32_t need = 0;
 #pragma unroll
-                            for (int j = 0; j < kChunk; ++j) {
-                                const uint32_t hi = hs[j][lane];
-                                const bool p = ((m[j] >> lane) & 1u) &&
-                                               __fadd_rn(__uint_as_float(r[j]), s_gtab[hi >> 8]) >= s_lb[grp][j];
-                                need |= (p ? 1u : 0u) << j;
+                            for (int k = 0; k < 8; ++k) {
+                                need |= (((p0 >> k) & 1u) && __fadd_rn(z0[k], gtab[(half_of(w0, k) >> 8) * 32 + lane]) >= lb0 ? 1u : 0u) << k;
+                                need |= (((p1 >> k) & 1u) && __fadd_rn(z1[k], gtab[(half_of(w1, k) >> 8) * 32 + lane]) >= lb1 ? 1u : 0u) << (8 + k);
                             }
-                            // rare: the full 16-bit bound, then the exact draw
-                            if (__any_sync(0xFFFFFFFFu, need != 0u)) {
+                            // rare: the exact 16-bit bound, then the full draw (compact loop over set bits)
+                            while (need != 0u) {
+                                const int e = __ffs(need) - 1;
+                                need &= need - 1u;
+                                const int hh = e >> 3, k = e & 7;
+                                float z = 0.f;                       // register select, no local array
 #pragma unroll
-                                for (int j = 0; j < kChunk; ++j) {
-                                    if ((need >> j) & 1u) {
-                                        const float z = __uint_as_float(r[j]);
-                                        const uint32_t hi = hs[j][lane];
-                                        if (high_half_can_reach(hi, __fsub_rn(s_lb[grp][j], z))) {
-                                            const unsigned long long k =
-                                                rare_candidate(a.seed, a.offset, static_cast<uint32_t>(c * kChunk + j),
-                                                               static_cast<uint32_t>(i), static_cast<uint32_t>(v), z, hi);
-                                            if (k != 0ull) atomicMax(&s_best[grp][j], k);
-                                        }
-                                    }
-                                }
+                                for (int kk = 0; kk < 8; ++kk) z = kk == k ? (hh ? z1[kk] : z0[kk]) : z;
+                                const float lb = hh ? lb1 : lb0;
+                                const uint32_t hi = half_of(hh ? w1 : w0, k);
+                                if (!high_half_can_reach(hi, __fsub_rn(lb, z))) continue;
+                                const unsigned long long key =
+                                    rare_candidate(a.seed, a.offset, static_cast<uint32_t>(hh ? b1 : b0),
+                                                   static_cast<uint32_t>(i), static_cast<uint32_t>(v0 + k), z, hi);
+                                if (key != 0ull) atomicMax(&s_best[grp][8 * hh + jj], key);
                             }
-                            __syncwarp();
                         }
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
@@ -516,10 +534,10 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     }
 }
 
-// Ring depths: deep w2 ring (L2 stream) when the E operand leaves room.
+// Ring depths: the w2 ring gets what the E operand leaves (deeper rings measured no faster).
 void tc_rings(int B_pad, int r, int* w2_stages, int* l_stages) {
     const bool small_e = static_cast<size_t>(B_pad) * r * 2 <= 32 * 1024;
-    *w2_stages = small_e ? 6 : 4;
+    *w2_stages = small_e ? 4 : 2;
     *l_stages = 2;
 }
 
@@ -527,7 +545,7 @@ size_t tc_smem_bytes(int B_pad, int r) {
     int w2s, ls;
     tc_rings(B_pad, r, &w2s, &ls);
     return 1024 + static_cast<size_t>(w2s) * kW2StageBytes + static_cast<size_t>(kGroups) * ls * kLStageBytes +
-           static_cast<size_t>(B_pad) * r * 2;
+           kGtabBytes + static_cast<size_t>(B_pad) * r * 2;
 }
 
 }  // namespace

@@ -134,3 +134,23 @@ def test_anchor_out_of_range_sets_status(cuda_lib):
     _, _, st, bits = _gpu(cuda_lib, L, np.array([cfg.V + 5], np.int32), inp["w1"], inp["w2"],
                           np.ones(1, np.float32), 0, 0)
     assert bits & cuda_lib.STATUS_INPUT_RANGE and st == 6
+
+
+@pytest.mark.parametrize("V", [1000, 151936])
+def test_step_without_finite_logits_sets_numeric_and_spares_other_requests(cuda_lib, V):
+    """One request's base logits are NaN at one step: that step has no candidate (token 0 and the
+    NUMERIC bit); the other request still matches the oracle."""
+    B, N, r = 2, 3, 64
+    cfg = DraftConfig("nan", B=B, N=N, H=8, V=V, r=r, dtype="f32", temperatures=(1.0,), data_seed=3)
+    L = markov_logits(cfg)
+    L[1, 1, :] = np.nan
+    w1 = normal_rows(V, r, 1.0, 3, "w1")
+    w2 = normal_rows(V, r, 1.0 / np.sqrt(r), 3, "w2")
+    import torch
+    anchor = np.array([5, 9], np.int32)
+    T = np.ones(B, np.float32)
+    tok, _, st, bits = _gpu(cuda_lib, L, anchor, torch.from_numpy(w1), torch.from_numpy(w2), T, 4, 0)
+    assert bits & cuda_lib.STATUS_NUMERIC
+    assert tok[1, 1] == 0
+    ref, gap, _ = oracle.markov_sample(L[:1], anchor[:1], w1, w2, T[:1], 4, 0)
+    compare_markov_tokens(tok[:1], ref, gap)
