@@ -86,11 +86,49 @@ __device__ __forceinline__ float bias_dot(const uint8_t* row, const float* e, in
     return (acc0 + acc1) + (acc2 + acc3);
 }
 
+// Two bf16 rows of fixed width R against the same E row, fully unrolled: every shared-memory
+// load is issued before the first multiply-add, and four independent chains per row.
+template <int R>
+__device__ __forceinline__ void bias_dot2_fixed(const uint8_t* row0, const uint8_t* row1, const float* e,
+                                                float& out0, float& out1) {
+    uint4 q0[R / 8], q1[R / 8];
+#pragma unroll
+    for (int c = 0; c < R / 8; ++c) {
+        q0[c] = *reinterpret_cast<const uint4*>(row0 + 16 * c);
+        q1[c] = *reinterpret_cast<const uint4*>(row1 + 16 * c);
+    }
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < R / 8; ++c) {
+        const float4 e0 = *reinterpret_cast<const float4*>(e + 8 * c);
+        const float4 e1 = *reinterpret_cast<const float4*>(e + 8 * c + 4);
+        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&q0[c]);
+        const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&q1[c]);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float2 f0 = __bfloat1622float2(h0[p]);
+            const float2 f1 = __bfloat1622float2(h1[p]);
+            acc[(p & 1) * 2 + 0] = fmaf(f0.x, ev[2 * p], acc[(p & 1) * 2 + 0]);
+            acc[(p & 1) * 2 + 1] = fmaf(f0.y, ev[2 * p + 1], acc[(p & 1) * 2 + 1]);
+            acc[4 + (p & 1) * 2 + 0] = fmaf(f1.x, ev[2 * p], acc[4 + (p & 1) * 2 + 0]);
+            acc[4 + (p & 1) * 2 + 1] = fmaf(f1.y, ev[2 * p + 1], acc[4 + (p & 1) * 2 + 1]);
+        }
+    }
+    out0 = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    out1 = (acc[4] + acc[5]) + (acc[6] + acc[7]);
+}
+
 // Two rows against the same E row at once (independent chains, shared E reads).
 template <typename WT>
 __device__ __forceinline__ void bias_dot2(const uint8_t* row0, const uint8_t* row1, const float* e, int r,
                                           float& out0, float& out1) {
     if constexpr (sizeof(WT) == 2) {
+        if (((reinterpret_cast<uintptr_t>(row0) | reinterpret_cast<uintptr_t>(row1)) & 15) == 0 &&
+            (reinterpret_cast<uintptr_t>(e) & 15) == 0 && r == 64) {
+            bias_dot2_fixed<64>(row0, row1, e, out0, out1);
+            return;
+        }
         if (((reinterpret_cast<uintptr_t>(row0) | reinterpret_cast<uintptr_t>(row1)) & 15) == 0 && (r & 7) == 0 &&
             (reinterpret_cast<uintptr_t>(e) & 15) == 0) {
             float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
@@ -120,14 +158,18 @@ __device__ __forceinline__ void bias_dot2(const uint8_t* row0, const uint8_t* ro
     out1 = bias_dot<WT>(row1, e, r);
 }
 
-__device__ __forceinline__ unsigned long long block_max_u64(unsigned long long k, unsigned long long* red) {
+// Block maximum, valid in thread 0 only (the only reader).  One barrier: callers rotate over
+// four `red` buffers (request parity x pass), so the barrier of an intermediate call always
+// separates thread 0's read of a buffer from the next writes to it.
+__device__ __forceinline__ unsigned long long block_max_u64_t0(unsigned long long k, unsigned long long* red) {
     k = warp_max_u64(k);
-    __syncthreads();
     if (lane_id() == 0) red[warp_id()] = k;
     __syncthreads();
     unsigned long long m = 0;
+    if (threadIdx.x == 0) {
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) m = red[w] > m ? red[w] : m;
+        for (int w = 0; w < kWarps; ++w) m = red[w] > m ? red[w] : m;
+    }
     return m;
 }
 
@@ -160,10 +202,11 @@ template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sp = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
-    __shared__ unsigned long long s_red[kWarps];
+    __shared__ unsigned long long s_red[4][kWarps];   // [request parity][pass]: see block_max_u64_t0
     __shared__ float2 s_red2[kWarps];
     __shared__ float s_bcast[2];
     __shared__ float s_temp[256];                     // temperatures of the first 256 requests
+    __shared__ float s_inv[256];                      // their reciprocals (1 for greedy)
     __shared__ unsigned long long s_win[kExchangeMaxBN];  // exchange: the step's best key per request
     __shared__ int s_tok[kExchangeMaxBN];                  // exchange: winners [step][request]
 
@@ -197,32 +240,40 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
 
-    for (int b = tid; b < 256 && b < a.B; b += kThreads) s_temp[b] = __ldg(a.temperature + b);
+    for (int b = tid; b < 256 && b < a.B; b += kThreads) {
+        float T = __ldg(a.temperature + b);
+        if (!(T >= 0.f) || isinf(T)) {
+            set_status(a.ws, DSPARK_STATUS_NUMERIC);
+            T = 0.f;
+        }
+        s_temp[b] = T;
+        s_inv[b] = T > 0.f ? __frcp_rn(T) : 1.f;
+    }
     if (a.exchange)
         for (int b = tid; b < a.B; b += kThreads) s_win[b] = 0ull;
     // Decode fast path (one request, one pair of entries per thread): the base logits and
     // the noise of step i+1 do not depend on the token of step i, so they are fetched and
     // drawn while the block waits at step i's grid barrier.
     const bool fast = a.B == 1 && a.single_pass && a.lse == nullptr && 2 * kThreads >= n_local;
-    float pl0 = 0.f, pl1 = 0.f, pg0 = 0.f, pg1 = 0.f;
-    auto prepare = [&](int j) {
+    float pl0 = 0.f, pl1 = 0.f, pg0 = 0.f, pg1 = 0.f;       // this step's logits and noise
+    auto prepare = [&](int j, float& l0, float& l1, float& g0, float& g1) {
         const int t = 2 * tid;
         if (t >= n_local) return;
         const int v = v_lo + t;
         const bool two = t + 1 < n_local;
         const float* lr = a.base + static_cast<size_t>(j) * a.V;
-        pl0 = __ldcs(lr + v);
-        pl1 = two ? __ldcs(lr + v + 1) : 0.f;
+        l0 = __ldcs(lr + v);
+        l1 = two ? __ldcs(lr + v + 1) : 0.f;
         const uint4 wh = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, 0u, kStreamGumbel,
                                    static_cast<uint32_t>(j));
         const uint4 wl = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, 0u, kStreamGumbelLo,
                                    static_cast<uint32_t>(j));
-        pg0 = gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v)) << 16) | draft_half(wl, static_cast<uint32_t>(v)));
-        pg1 = two ? gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v + 1)) << 16) |
-                                     draft_half(wl, static_cast<uint32_t>(v + 1)))
-                  : 0.f;
+        g0 = gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v)) << 16) | draft_half(wl, static_cast<uint32_t>(v)));
+        g1 = two ? gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v + 1)) << 16) |
+                                    draft_half(wl, static_cast<uint32_t>(v + 1)))
+                 : 0.f;
     };
-    if (fast) prepare(0);
+    if (fast) prepare(0, pl0, pl1, pg0, pg1);
     bool alive = true;
     for (int i = 0; i < a.N && alive; ++i) {
         // ---- 1. previous tokens and the Markov embedding E[b] = w1[prev_b] ----
@@ -253,13 +304,19 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         float2* lse_part = a.lay.lse_part + static_cast<size_t>(i & 1) * kMaxGrid * a.B;
 
         for (int b = 0; b < a.B; ++b) {
-            float T = b < 256 ? s_temp[b] : __ldg(a.temperature + b);
-            if (!(T >= 0.f) || isinf(T)) {
-                if (tid == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
-                T = 0.f;
+            float T, invT;
+            if (b < 256) {
+                T = s_temp[b];
+                invT = s_inv[b];
+            } else {
+                T = __ldg(a.temperature + b);
+                if (!(T >= 0.f) || isinf(T)) {
+                    if (tid == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+                    T = 0.f;
+                }
+                invT = T > 0.f ? __frcp_rn(T) : 1.f;
             }
             const bool hot = T > 0.f;
-            const float invT = hot ? __frcp_rn(T) : 1.f;
             const float* lrow = a.base + (static_cast<size_t>(b) * a.N + i) * a.V;
             const float* e = E + static_cast<size_t>(b) * a.r;
 
@@ -325,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 best = k > best ? k : best;
             }
             if (bad) set_status(a.ws, DSPARK_STATUS_NUMERIC);
-            best = block_max_u64(best, s_red);
+            best = block_max_u64_t0(best, s_red[(b & 1) * 2]);
             if (a.lse != nullptr) {
                 ls = block_lse(ls, s_red2);
                 if (tid == 0) lse_part[static_cast<size_t>(blockIdx.x) * a.B + b] = ls;
@@ -345,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 }
             }
             if (a.exchange && tid == 0)   // 1 = this block has no finite candidate (below every key)
-                st_release_u64(a.lay.cand + (static_cast<size_t>(i) * gridDim.x + blockIdx.x) * a.B + b,
+                st_relaxed_u64(a.lay.cand + (static_cast<size_t>(i) * gridDim.x + blockIdx.x) * a.B + b,
                                best != 0ull ? best : 1ull);
             if (!hot || a.single_pass) continue;
 
@@ -371,19 +428,21 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 const unsigned long long k = argmax_key(y, static_cast<uint32_t>(v));
                 best = k > best ? k : best;
             }
-            best = block_max_u64(best, s_red);
+            best = block_max_u64_t0(best, s_red[(b & 1) * 2 + 1]);
             if (tid == 0 && best != 0ull) atomicMax(slot + b, best);
         }
 
         // ---- 4. all blocks agree on the step's winners ----
         if (a.exchange) {
             // every block's candidates for this step, polled (bounded) and reduced here
-            if (fast && i + 1 < a.N) prepare(i + 1);
+            // the next step's logits and noise do not depend on this step's token: drawn
+            // while the other blocks finish
+            if (fast && i + 1 < a.N) prepare(i + 1, pl0, pl1, pg0, pg1);
             const int n_ent = static_cast<int>(gridDim.x) * a.B;
             const unsigned long long* cs = a.lay.cand + static_cast<size_t>(i) * n_ent;
             int fail = 0;
             for (int e = tid; e < n_ent; e += kThreads) {
-                unsigned long long k = ld_acquire_u64(cs + e);
+                unsigned long long k = ld_relaxed_u64(cs + e);
                 const long long t0 = global_ns();
                 uint32_t spins = 0;
                 while (k == 0ull) {
@@ -396,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                             break;
                         }
                     }
-                    k = ld_acquire_u64(cs + e);
+                    k = ld_relaxed_u64(cs + e);
                 }
                 if (k > 1ull) atomicMax(&s_win[e % a.B], k);
             }
@@ -411,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             }
         } else {
             grid_arrive(a.ws);
-            if (fast && i + 1 < a.N) prepare(i + 1);
+            if (fast && i + 1 < a.N) prepare(i + 1, pl0, pl1, pg0, pg1);
             alive = grid_wait(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i);
         }
     }
