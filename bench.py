@@ -166,10 +166,11 @@ def run_gpu(args):
     import torch
     import draft_sampling_verification_tcgen05_gb300 as ds
     from draft_sampling_verification_tcgen05_gb300 import _build
+    from draft_sampling_verification_tcgen05_gb300.replicas import (job_throughput, max_over_ranks, rank_info,
+                                                                    replica_seed)
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    ri = rank_info()
+    rank, world, local = ri.rank, ri.world, ri.local_rank
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -237,15 +238,18 @@ def run_gpu(args):
         L_markov += L
         torch.cuda.synchronize()
 
+    # each replica serves its own requests: independent noise streams per rank
+    seed_draft, seed_verify = replica_seed(0, rank), replica_seed(2, rank)
+
     def step(k=None):
         e = ev[k] if k is not None else None
         if e: e[0].record(stream)
         ds.dspark_draft_logits(X, W, logits=L, workspace=ws_g)
         if e: e[1].record(stream)
-        ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, 0, 0, draft_tokens=tok,
+        ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, draft_tokens=tok,
                                 workspace=ws_m)
         if e: e[2].record(stream)
-        ds.dspark_verify(p_t, p_d, tok, None, 2, 0, out_tokens=out, num_accepted=nacc, workspace=ws_v)
+        ds.dspark_verify(p_t, p_d, tok, None, seed_verify, 0, out_tokens=out, num_accepted=nacc, workspace=ws_v)
         if e: e[3].record(stream)
         ds.dspark_schedule(conf, sps, -1, survival=surv, K_out=K_out, lengths=lens, selected=sel,
                            workspace=ws_s)
@@ -314,11 +318,8 @@ def run_gpu(args):
         step_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(g0, g1)]))
     else:
         step_ms = float(per.sum(axis=1).mean())
-    if dist is not None:
-        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = world * M / (step_ms / 1e3)
+    step_ms = max_over_ranks(step_ms, dist, dev)
+    value = job_throughput(M, world, step_ms)
 
     # ---------------- end to end through host buffers ----------------
     e2e = None
@@ -355,11 +356,8 @@ def run_gpu(args):
                 e1[k - args.warmup].record(stream)
             stream.synchronize()
         e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(e0, e1)]))
-        if dist is not None:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * M / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+        e2e = {"value": job_throughput(M, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
 
     # ---------------- roofline of the dominant kernel ----------------
