@@ -360,6 +360,25 @@ def run_gpu(args):
         e2e = {"value": job_throughput(M, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
 
+    # ---------------- kernels beyond the step, timed on their own ----------------
+    # greedy verification of the step's draft tokens against the same target rows (all rows
+    # k <= gamma are read)
+    ws_g2 = ds.Workspace(ds.OP_VERIFY_GREEDY, B, N, device=dev)
+    g_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    g_nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        ds.dspark_verify_greedy(p_t, tok, None, out_tokens=g_out, num_accepted=g_nacc, workspace=ws_g2)
+    g_ms = []
+    for k in range(20):
+        flush_l2(k)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ds.dspark_verify_greedy(p_t, tok, None, out_tokens=g_out, num_accepted=g_nacc, workspace=ws_g2)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        g_ms.append(e0.elapsed_time(e1))
+    greedy_ms = float(np.median(g_ms))
+
     # ---------------- roofline of the dominant kernel ----------------
     peaks = {}
     try:
@@ -409,6 +428,10 @@ def run_gpu(args):
         "kernel_ms": {"draft_logits": kernel_ms[0], "markov_sample": kernel_ms[1],
                       "verify": kernel_ms[2], "schedule": kernel_ms[3]},
         "roofline": roof,
+        "verify_greedy": {"ms": greedy_ms, "bound": "hbm", "algorithmic_bytes": B * (N + 1) * V * 4,
+                          "achieved": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9, "peak": hbm_peak,
+                          "unit": "GB/s", "frac": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9 / hbm_peak,
+                          "note": "median of 20 launches, L2 flushed, outside the step"},
         "markov_roofline": {"bound": "hbm", "algorithmic_bytes": markov_bytes,
                             "achieved": markov_bytes / (kernel_ms[1] / 1e3) / 1e9, "peak": hbm_peak,
                             "unit": "GB/s", "frac": markov_bytes / (kernel_ms[1] / 1e3) / 1e9 / hbm_peak},

@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "DSparkError", "lib", "Workspace", "OP_DRAFT_LOGITS", "OP_MARKOV_SAMPLE", "OP_VERIFY",
-    "OP_SCHEDULE", "dspark_workspace_size", "dspark_draft_logits", "dspark_markov_sample",
+    "OP_SCHEDULE", "OP_VERIFY_GREEDY", "dspark_workspace_size", "dspark_verify_greedy", "dspark_draft_logits", "dspark_markov_sample",
     "dspark_verify", "dspark_schedule", "dspark_read_status", "dspark_status_string",
     "dspark_selftest_wait_timeout", "STATUS_TIMEOUT", "STATUS_NUMERIC", "STATUS_INPUT_RANGE",
     "STATUS_INTERNAL",
@@ -22,7 +22,7 @@ __all__ = [
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdspark.so")
 
-OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE = 0, 1, 2, 3
+OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE, OP_VERIFY_GREEDY = 0, 1, 2, 3, 4
 F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NUMERIC, ERR_INPUT_RANGE = range(7)
 STATUS_TIMEOUT, STATUS_NUMERIC, STATUS_INPUT_RANGE, STATUS_INTERNAL = 0x1, 0x2, 0x4, 0x8
@@ -52,6 +52,7 @@ def lib() -> ctypes.CDLL:
     L.dspark_markov_sample.argtypes = [vp, vp, vp, vp, i32, vp, u64, u64, i32, i32, i32, i32,
                                        vp, vp, vp, sz, vp]
     L.dspark_verify.argtypes = [vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.dspark_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_schedule.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_read_status.argtypes = [vp, u32p, vp]
     L.dspark_status_string.argtypes = [i32]
@@ -194,6 +195,29 @@ def dspark_verify(p_target, p_draft, draft_tokens, lengths, seed: int, offset: i
     _check(lib().dspark_verify(_ptr(p_target), _ptr(p_draft), _ptr(draft_tokens), _ptr(lengths),
                                seed, offset, B, gamma, V, _ptr(out_tokens), _ptr(num_accepted),
                                ws.ptr, ws.nbytes, _stream(stream)), "dspark_verify")
+    return out_tokens, num_accepted
+
+
+def dspark_verify_greedy(target, draft_tokens, lengths=None, out_tokens=None, num_accepted=None,
+                         workspace=None, stream=None):
+    """Greedy (temperature-0) verification; returns (out_tokens [B, gamma+1], num_accepted [B])."""
+    torch = _torch()
+    _need(target, "target", (torch.float32,), 3)
+    _need(draft_tokens, "draft_tokens", (torch.int32,), 2)
+    B, g1, V = target.shape
+    gamma = g1 - 1
+    if tuple(draft_tokens.shape) != (B, gamma):
+        raise ValueError("shapes must be target [B, gamma+1, V], tokens [B, gamma]")
+    if lengths is not None:
+        _need(lengths, "lengths", (torch.int32,), 1)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=target.device)
+    if num_accepted is None:
+        num_accepted = torch.empty(B, dtype=torch.int32, device=target.device)
+    ws = _ws(workspace, OP_VERIFY_GREEDY, B, gamma, 0, 0, target.device)
+    _check(lib().dspark_verify_greedy(_ptr(target), _ptr(draft_tokens), _ptr(lengths), B, gamma, V,
+                                      _ptr(out_tokens), _ptr(num_accepted), ws.ptr, ws.nbytes, _stream(stream)),
+           "dspark_verify_greedy")
     return out_tokens, num_accepted
 
 

@@ -172,6 +172,8 @@ size_t dspark_workspace_size(int op, int B, int N, int V, int r) {
             return markov_workspace_bytes(B, N);
         case DSPARK_OP_SCHEDULE:
             return schedule_workspace_bytes(B, N);
+        case DSPARK_OP_VERIFY_GREEDY:
+            return verify_greedy_workspace_bytes(B, N);
         default:
             return 0;
     }
@@ -240,6 +242,22 @@ dspark_status dspark_verify(const float* p_target, const float* p_draft, const i
     if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
     return launch_verify(p_target, p_draft, draft_tokens, lengths, seed, static_cast<uint32_t>(offset), B,
                          gamma, V, out_tokens, num_accepted, workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
+dspark_status dspark_verify_greedy(const float* target, const int32_t* draft_tokens, const int32_t* lengths,
+                                   int B, int gamma, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+    g_error[0] = '\0';
+    DSPARK_REQUIRE(target && draft_tokens && out_tokens && num_accepted, "verify_greedy: null pointer");
+    DSPARK_REQUIRE(B >= 1 && gamma >= 1 && gamma <= 65535 && V >= 1,
+                   "verify_greedy: bad sizes (B=%d gamma=%d V=%d)", B, gamma, V);
+    DSPARK_REQUIRE(aligned(target, 16), "verify_greedy: target must be 16-byte aligned");
+    if (bad_ws(workspace, ws_bytes, dspark_workspace_size(DSPARK_OP_VERIFY_GREEDY, B, gamma, 0, 0)))
+        return DSPARK_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
+    return launch_verify_greedy(target, draft_tokens, lengths, B, gamma, V, out_tokens, num_accepted, workspace,
+                                static_cast<cudaStream_t>(stream), dev);
 }
 
 dspark_status dspark_schedule(const float* cond_accept, const double* sps, int S, int B, int N, int K_in,

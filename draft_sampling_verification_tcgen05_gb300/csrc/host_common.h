@@ -52,6 +52,10 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
                                    cudaStream_t stream, const DeviceInfo& dev);
 
 size_t verify_workspace_bytes(int B, int V);
+size_t verify_greedy_workspace_bytes(int B, int gamma);
+dspark_status launch_verify_greedy(const float* target, const int32_t* draft_tokens, const int32_t* lengths,
+                                   int B, int gamma, int V, int32_t* out_tokens, int32_t* num_accepted,
+                                   void* ws, cudaStream_t stream, const DeviceInfo& dev);
 dspark_status launch_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,
                             const int32_t* lengths, uint64_t seed, uint32_t offset, int B, int gamma,
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,

@@ -67,7 +67,8 @@ typedef enum {
     DSPARK_OP_DRAFT_LOGITS = 0,
     DSPARK_OP_MARKOV_SAMPLE = 1,
     DSPARK_OP_VERIFY = 2,
-    DSPARK_OP_SCHEDULE = 3
+    DSPARK_OP_SCHEDULE = 3,
+    DSPARK_OP_VERIFY_GREEDY = 4
 } dspark_op;
 
 /* Device status-word bits (OR-ed by kernels; read with dspark_read_status). */
@@ -83,6 +84,7 @@ typedef enum {
  *   DSPARK_OP_MARKOV_SAMPLE grows with B*N and B (argmax slots, bounds, lse partials)
  *   DSPARK_OP_VERIFY        grows with B*V/512 (per-512-entry integer masses); N = gamma
  *   DSPARK_OP_SCHEDULE      grows with B*N (radix-sort key buffers)
+ *   DSPARK_OP_VERIFY_GREEDY grows with B*(N+1) (row argmax keys); N = gamma
  * Returns 0 for an unknown op or negative sizes.
  */
 DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);
@@ -180,6 +182,35 @@ DSPARK_API dspark_status dspark_verify(const float* p_target, const float* p_dra
                             uint64_t seed, uint64_t offset, int B, int gamma, int V,
                             int32_t* out_tokens, int32_t* num_accepted,
                             void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Greedy (temperature-0) verification of a block of gamma draft tokens per
+ * request.
+ *
+ * "xserv/docs/25-speculative-methods-comparison.md" §2: the longest prefix of
+ * draft tokens that each equal the target's argmax at their position is
+ * accepted; the target's argmax at the first failing position (position L_b
+ * when none fails) is appended.  The output equals the target's own greedy
+ * continuation.  Argmax ties go to the lowest token id; NaN entries never win
+ * (a row without a non-NaN entry gives token 0 and sets NUMERIC).
+ *
+ *   target       [B, gamma+1, V] fp32, device: row k scores position k
+ *                (logits or probabilities: only the argmax is used)
+ *   draft_tokens [B, gamma] int32, device
+ *   lengths      [B] int32 in [0, gamma], device, or NULL (= gamma)
+ *   out_tokens   [B, gamma+1] int32 output: accepted prefix, the target's
+ *                token, then -1
+ *   num_accepted [B] int32 output
+ * Requirements: B >= 1, 1 <= gamma <= 65535, 1 <= V < 2^31; target 16-byte
+ * aligned.  Device-side: a token or length out of range sets INPUT_RANGE
+ * (the request outputs num_accepted 0 and -1 tokens).  Only rows k <= L_b
+ * are read.
+ * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY_GREEDY, B, gamma, 0, 0).
+ */
+DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t* draft_tokens,
+                                   const int32_t* lengths, int B, int gamma, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted,
+                                   void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Confidence-scheduled admission of draft tokens for the next verify batch.

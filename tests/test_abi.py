@@ -28,7 +28,8 @@ def test_every_declared_symbol_is_exported(L):
     assert len(names) >= 9
     for n in names:
         assert hasattr(L, n), n
-    for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule"):
+    for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule",
+               "dspark_verify_greedy"):
         assert op in names
 
 
@@ -38,6 +39,7 @@ def test_workspace_sizes(L):
     m = L.dspark_workspace_size(1, 64, 16, 151936, 256)
     assert m >= 256 + 64 * 16 * 12
     assert L.dspark_workspace_size(3, 1024, 16, 0, 0) == 256 + 2 * 8 * 1024 * 16
+    assert L.dspark_workspace_size(4, 256, 8, 151936, 0) == 256 + 8 * 256 * 9 + 1024
     assert L.dspark_workspace_size(9, 1, 1, 1, 1) == 0
 
 
@@ -53,6 +55,9 @@ def test_host_validation_without_gpu(L):
     assert L.dspark_markov_sample(fake, fake, fake, fake, 1, fake, 0, 0, 1, 0, 100, 64,
                                   fake, null, fake, 1 << 20, null) == 1                   # N = 0
     assert L.dspark_verify(fake, fake, fake, null, 0, 0, 1, 0, 10, fake, fake, fake, 256, null) == 1
+    assert L.dspark_verify_greedy(fake, fake, null, 1, 0, 10, fake, fake, fake, 1 << 20, null) == 1  # gamma = 0
+    assert L.dspark_verify_greedy(null, fake, null, 1, 2, 10, fake, fake, fake, 1 << 20, null) == 1
+    assert L.dspark_verify_greedy(fake, fake, null, 4, 8, 10, fake, fake, fake, 64, null) == 1      # workspace
     assert L.dspark_schedule(fake, null, 0, 4, 4, -1, fake, fake, fake, fake, fake, 1024, null) == 1
     assert L.dspark_schedule(fake, null, 0, 2048, 1024, 5, fake, fake, fake, fake, fake, 1 << 30, null) == 1
     assert b"SPS" in L.dspark_last_error() or len(L.dspark_last_error()) > 0
