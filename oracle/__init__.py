@@ -12,7 +12,7 @@ from the pages that define the method, each function citing its passage:
     §2.2 Sequential Markov Sampling, §3 Markov Head structure, §4 draft step.
   * "Speculative decoding: from zero to DSpark" (bittide.aicompass.dev):
     §2 the loop and its lossless property, §6 scheduling by expected
-    throughput, §7 running in a real engine.
+    throughput and the calibrated confidence head, §7 running in a real engine.
   * "xserv/docs/25-speculative-methods-comparison.md": §2 greedy verification.
 
 Where the pages are silent (the random-number counter layout, the uniform
@@ -29,11 +29,12 @@ from .draft import draft_logits, markov_sample, markov_bias
 from .verify import verify, acceptance_probability_exact
 from .schedule import schedule, survival_chain
 from .greedy import verify_greedy, row_argmax
+from .confidence import confidence
 
 __all__ = [
     "philox4x32_10", "philox_words", "uniform_from_word", "gumbel_from_word",
     "draft_logits", "markov_sample", "markov_bias",
     "verify", "acceptance_probability_exact",
     "schedule", "survival_chain",
-    "verify_greedy", "row_argmax",
+    "verify_greedy", "row_argmax", "confidence",
 ]
