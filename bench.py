@@ -378,6 +378,26 @@ def run_gpu(args):
         torch.cuda.synchronize()
         g_ms.append(e0.elapsed_time(e1))
     greedy_ms = float(np.median(g_ms))
+    # calibrated confidence head on the step's hidden rows and draft tokens (synthetic head weights)
+    hrng = np.random.default_rng(d.data_seed + 7)
+    w_h = torch.from_numpy((hrng.standard_normal(H) / np.sqrt(H)).astype(np.float32)).to(dev)
+    w_e = torch.from_numpy((hrng.standard_normal(r) / np.sqrt(r)).astype(np.float32)).to(dev)
+    tau = torch.from_numpy(hrng.uniform(0.7, 1.6, N).astype(np.float32)).to(dev)
+    ws_c = ds.Workspace(ds.OP_CONFIDENCE, B, N, V, r, device=dev)
+    conf_out = torch.empty(B, N, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        ds.dspark_confidence(X, w1, anchor, tok, w_h, w_e, 0.5, tau, conf=conf_out, workspace=ws_c)
+    c_ms = []
+    for k in range(20):
+        flush_l2(k)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ds.dspark_confidence(X, w1, anchor, tok, w_h, w_e, 0.5, tau, conf=conf_out, workspace=ws_c)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        c_ms.append(e0.elapsed_time(e1))
+    conf_ms = float(np.median(c_ms))
+    conf_bytes = M * H * X.element_size() + M * r * w1.element_size() + (H + r + N) * 4 + M * 4
 
     # ---------------- roofline of the dominant kernel ----------------
     peaks = {}
@@ -428,6 +448,10 @@ def run_gpu(args):
         "kernel_ms": {"draft_logits": kernel_ms[0], "markov_sample": kernel_ms[1],
                       "verify": kernel_ms[2], "schedule": kernel_ms[3]},
         "roofline": roof,
+        "confidence": {"ms": conf_ms, "bound": "hbm", "algorithmic_bytes": conf_bytes,
+                       "achieved": conf_bytes / (conf_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                       "frac": conf_bytes / (conf_ms / 1e3) / 1e9 / hbm_peak,
+                       "note": "median of 20 launches, L2 flushed, outside the step (latency-bound at these sizes)"},
         "verify_greedy": {"ms": greedy_ms, "bound": "hbm", "algorithmic_bytes": B * (N + 1) * V * 4,
                           "achieved": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9, "peak": hbm_peak,
                           "unit": "GB/s", "frac": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9 / hbm_peak,

@@ -14,7 +14,8 @@ import os
 
 __all__ = [
     "DSparkError", "lib", "Workspace", "OP_DRAFT_LOGITS", "OP_MARKOV_SAMPLE", "OP_VERIFY",
-    "OP_SCHEDULE", "OP_VERIFY_GREEDY", "dspark_workspace_size", "dspark_verify_greedy", "dspark_draft_logits", "dspark_markov_sample",
+    "OP_SCHEDULE", "OP_VERIFY_GREEDY", "OP_CONFIDENCE", "dspark_workspace_size", "dspark_verify_greedy",
+    "dspark_confidence", "dspark_draft_logits", "dspark_markov_sample",
     "dspark_verify", "dspark_schedule", "dspark_read_status", "dspark_status_string",
     "dspark_selftest_wait_timeout", "STATUS_TIMEOUT", "STATUS_NUMERIC", "STATUS_INPUT_RANGE",
     "STATUS_INTERNAL",
@@ -22,7 +23,7 @@ __all__ = [
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdspark.so")
 
-OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE, OP_VERIFY_GREEDY = 0, 1, 2, 3, 4
+OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE, OP_VERIFY_GREEDY, OP_CONFIDENCE = 0, 1, 2, 3, 4, 5
 F32, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NUMERIC, ERR_INPUT_RANGE = range(7)
 STATUS_TIMEOUT, STATUS_NUMERIC, STATUS_INPUT_RANGE, STATUS_INTERNAL = 0x1, 0x2, 0x4, 0x8
@@ -53,6 +54,8 @@ def lib() -> ctypes.CDLL:
                                        vp, vp, vp, sz, vp]
     L.dspark_verify.argtypes = [vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.dspark_confidence.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, i32,
+                                    vp, vp, sz, vp]
     L.dspark_schedule.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_read_status.argtypes = [vp, u32p, vp]
     L.dspark_status_string.argtypes = [i32]
@@ -86,6 +89,11 @@ def _stream(stream=None):
     torch = _torch()
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t):
+    """Library dtype code of a bf16 or fp32 tensor."""
+    return BF16 if t.dtype == _torch().bfloat16 else F32
 
 
 def _need(t, name, dtypes, ndim=None):
@@ -219,6 +227,32 @@ def dspark_verify_greedy(target, draft_tokens, lengths=None, out_tokens=None, nu
                                       _ptr(out_tokens), _ptr(num_accepted), ws.ptr, ws.nbytes, _stream(stream)),
            "dspark_verify_greedy")
     return out_tokens, num_accepted
+
+
+def dspark_confidence(hidden, w1, anchor, draft_tokens, w_h, w_e, beta: float, tau, conf=None,
+                      workspace=None, stream=None):
+    """Calibrated confidence head; returns conf [B, N] (the scheduler's cond_accept)."""
+    torch = _torch()
+    _need(hidden, "hidden", (torch.bfloat16, torch.float32), 2)
+    _need(w1, "w1", (torch.bfloat16, torch.float32), 2)
+    _need(anchor, "anchor", (torch.int32,), 1)
+    _need(draft_tokens, "draft_tokens", (torch.int32,), 2)
+    _need(w_h, "w_h", (torch.float32,), 1)
+    _need(w_e, "w_e", (torch.float32,), 1)
+    _need(tau, "tau", (torch.float32,), 1)
+    B, N = draft_tokens.shape
+    H = hidden.shape[1]
+    V, r = w1.shape
+    if hidden.shape[0] != B * N or anchor.shape[0] != B or w_h.shape[0] != H or w_e.shape[0] != r \
+            or tau.shape[0] != N:
+        raise ValueError("shapes: hidden [B*N, H], w1 [V, r], anchor [B], tokens [B, N], w_h [H], w_e [r], tau [N]")
+    if conf is None:
+        conf = torch.empty(B, N, dtype=torch.float32, device=hidden.device)
+    ws = _ws(workspace, OP_CONFIDENCE, B, N, V, r, hidden.device)
+    _check(lib().dspark_confidence(_ptr(hidden), _dt(hidden), _ptr(w1), _dt(w1), _ptr(anchor), _ptr(draft_tokens),
+                                   _ptr(w_h), _ptr(w_e), float(beta), _ptr(tau), B, N, H, V, r, _ptr(conf),
+                                   ws.ptr, ws.nbytes, _stream(stream)), "dspark_confidence")
+    return conf
 
 
 def dspark_schedule(cond_accept, sps, K_in: int, survival=None, K_out=None, lengths=None,

@@ -174,6 +174,8 @@ size_t dspark_workspace_size(int op, int B, int N, int V, int r) {
             return schedule_workspace_bytes(B, N);
         case DSPARK_OP_VERIFY_GREEDY:
             return verify_greedy_workspace_bytes(B, N);
+        case DSPARK_OP_CONFIDENCE:
+            return sizeof(WsHeader);
         default:
             return 0;
     }
@@ -258,6 +260,24 @@ dspark_status dspark_verify_greedy(const float* target, const int32_t* draft_tok
     if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
     return launch_verify_greedy(target, draft_tokens, lengths, B, gamma, V, out_tokens, num_accepted, workspace,
                                 static_cast<cudaStream_t>(stream), dev);
+}
+
+dspark_status dspark_confidence(const void* hidden, dspark_dtype hdtype, const void* w1, dspark_dtype wdtype,
+                                const int32_t* anchor, const int32_t* draft_tokens, const float* w_h,
+                                const float* w_e, float beta, const float* tau, int B, int N, int H, int V, int r,
+                                float* conf, void* workspace, size_t ws_bytes, void* stream) {
+    g_error[0] = '\0';
+    DSPARK_REQUIRE(hidden && w1 && anchor && draft_tokens && w_h && w_e && tau && conf, "confidence: null pointer");
+    DSPARK_REQUIRE((hdtype == DSPARK_F32 || hdtype == DSPARK_BF16) && (wdtype == DSPARK_F32 || wdtype == DSPARK_BF16),
+                   "confidence: unknown dtype");
+    DSPARK_REQUIRE(B >= 1 && N >= 1 && H >= 1 && V >= 1 && r >= 1 && static_cast<long long>(B) * N < (1ll << 31),
+                   "confidence: bad sizes (B=%d N=%d H=%d V=%d r=%d)", B, N, H, V, r);
+    if (bad_ws(workspace, ws_bytes, dspark_workspace_size(DSPARK_OP_CONFIDENCE, B, N, V, r)))
+        return DSPARK_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
+    return launch_confidence(hidden, hdtype, w1, wdtype, anchor, draft_tokens, w_h, w_e, beta, tau, B, N, H, V, r,
+                             conf, workspace, static_cast<cudaStream_t>(stream));
 }
 
 dspark_status dspark_schedule(const float* cond_accept, const double* sps, int S, int B, int N, int K_in,

@@ -68,7 +68,8 @@ typedef enum {
     DSPARK_OP_MARKOV_SAMPLE = 1,
     DSPARK_OP_VERIFY = 2,
     DSPARK_OP_SCHEDULE = 3,
-    DSPARK_OP_VERIFY_GREEDY = 4
+    DSPARK_OP_VERIFY_GREEDY = 4,
+    DSPARK_OP_CONFIDENCE = 5
 } dspark_op;
 
 /* Device status-word bits (OR-ed by kernels; read with dspark_read_status). */
@@ -85,6 +86,7 @@ typedef enum {
  *   DSPARK_OP_VERIFY        grows with B*V/512 (per-512-entry integer masses); N = gamma
  *   DSPARK_OP_SCHEDULE      grows with B*N (radix-sort key buffers)
  *   DSPARK_OP_VERIFY_GREEDY grows with B*(N+1) (row argmax keys); N = gamma
+ *   DSPARK_OP_CONFIDENCE    256 (the status word)
  * Returns 0 for an unknown op or negative sizes.
  */
 DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);
@@ -211,6 +213,36 @@ DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t
                                    const int32_t* lengths, int B, int gamma, int V,
                                    int32_t* out_tokens, int32_t* num_accepted,
                                    void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Conditional acceptance probability of every draft token from the calibrated
+ * confidence head.
+ *
+ * "Speculative decoding: from zero to DSpark" §6: a linear projection of the
+ * backbone's hidden state together with the Markov embedding, calibrated per
+ * position by temperature scaling:
+ *   conf[b, i] = 1 / (1 + exp(-(w_h . hidden[b*N+i] + w_e . w1[prev] + beta) / tau[i]))
+ * with prev = anchor[b] for i = 0 and draft_tokens[b, i-1] after (the
+ * embedding the Markov head used at step i).  conf is dspark_schedule's
+ * cond_accept.
+ *
+ *   hidden       [B*N, H] hdtype (bf16 or fp32), device: the LM head's input rows
+ *   w1           [V, r] wdtype, device: markov_w1
+ *   anchor       [B] int32, draft_tokens [B, N] int32, device
+ *   w_h [H], w_e [r] fp32, device: the head's weights; beta: its bias (host value)
+ *   tau          [N] fp32 > 0, device: per-position calibration temperatures
+ *   conf         [B, N] fp32 output
+ * Requirements: B, N, H, r >= 1, V >= 1.  Device-side: a previous token
+ * outside [0, V) is read as 0 and sets INPUT_RANGE; a temperature that is not
+ * positive and finite gives conf 0 and sets NUMERIC.
+ * workspace: >= dspark_workspace_size(DSPARK_OP_CONFIDENCE, ...) bytes.
+ */
+DSPARK_API dspark_status dspark_confidence(const void* hidden, dspark_dtype hdtype, const void* w1,
+                                dspark_dtype wdtype, const int32_t* anchor,
+                                const int32_t* draft_tokens, const float* w_h,
+                                const float* w_e, float beta, const float* tau,
+                                int B, int N, int H, int V, int r, float* conf,
+                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Confidence-scheduled admission of draft tokens for the next verify batch.

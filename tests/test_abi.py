@@ -29,7 +29,7 @@ def test_every_declared_symbol_is_exported(L):
     for n in names:
         assert hasattr(L, n), n
     for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule",
-               "dspark_verify_greedy"):
+               "dspark_verify_greedy", "dspark_confidence"):
         assert op in names
 
 
@@ -40,6 +40,7 @@ def test_workspace_sizes(L):
     assert m >= 256 + 64 * 16 * 12
     assert L.dspark_workspace_size(3, 1024, 16, 0, 0) == 256 + 2 * 8 * 1024 * 16
     assert L.dspark_workspace_size(4, 256, 8, 151936, 0) == 256 + 8 * 256 * 9 + 1024
+    assert L.dspark_workspace_size(5, 64, 16, 151936, 256) == 256
     assert L.dspark_workspace_size(9, 1, 1, 1, 1) == 0
 
 
@@ -58,6 +59,10 @@ def test_host_validation_without_gpu(L):
     assert L.dspark_verify_greedy(fake, fake, null, 1, 0, 10, fake, fake, fake, 1 << 20, null) == 1  # gamma = 0
     assert L.dspark_verify_greedy(null, fake, null, 1, 2, 10, fake, fake, fake, 1 << 20, null) == 1
     assert L.dspark_verify_greedy(fake, fake, null, 4, 8, 10, fake, fake, fake, 64, null) == 1      # workspace
+    assert L.dspark_confidence(fake, 1, fake, 1, fake, fake, fake, fake, 0.0, fake, 1, 8, 64, 100, 0,
+                               fake, fake, 256, null) == 1                                   # r = 0
+    assert L.dspark_confidence(fake, 3, fake, 1, fake, fake, fake, fake, 0.0, fake, 1, 8, 64, 100, 8,
+                               fake, fake, 256, null) == 1                                   # dtype
     assert L.dspark_schedule(fake, null, 0, 4, 4, -1, fake, fake, fake, fake, fake, 1024, null) == 1
     assert L.dspark_schedule(fake, null, 0, 2048, 1024, 5, fake, fake, fake, fake, fake, 1 << 30, null) == 1
     assert b"SPS" in L.dspark_last_error() or len(L.dspark_last_error()) > 0
