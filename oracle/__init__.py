@@ -9,11 +9,13 @@ Everything is plain numpy in float64 (integers exact), written step by step
 from the pages that define the method, each function citing its passage:
 
   * "DSpark implementation and evaluation" (ggaaooppeenngg.github.io):
-    §2.2 Sequential Markov Sampling, §3 Markov Head structure, §4 draft step.
+    §2.2 Sequential Markov Sampling, §3 Markov Head structure, §4 draft step,
+    §5 reduced draft vocabulary.
   * "Speculative decoding: from zero to DSpark" (bittide.aicompass.dev):
     §2 the loop and its lossless property, §6 scheduling by expected
     throughput and the calibrated confidence head, §7 running in a real engine.
-  * "xserv/docs/25-speculative-methods-comparison.md": §2 greedy verification.
+  * "xserv/docs/25-speculative-methods-comparison.md": §2 greedy verification,
+    §3.2 the draft-to-target id table.
 
 Where the pages are silent (the random-number counter layout, the uniform
 mapping, the fixed-point resample, the objective's exact form) the oracle
@@ -30,11 +32,12 @@ from .verify import verify, acceptance_probability_exact
 from .schedule import schedule, survival_chain
 from .greedy import verify_greedy, row_argmax
 from .confidence import confidence
+from .reduced_vocab import map_to_target, markov_sample_reduced
 
 __all__ = [
     "philox4x32_10", "philox_words", "uniform_from_word", "gumbel_from_word",
     "draft_logits", "markov_sample", "markov_bias",
     "verify", "acceptance_probability_exact",
     "schedule", "survival_chain",
-    "verify_greedy", "row_argmax", "confidence",
+    "verify_greedy", "row_argmax", "confidence", "map_to_target", "markov_sample_reduced",
 ]

@@ -95,8 +95,9 @@ def markov_sample(base_logits, anchor, w1, w2, temperature, seed: int, offset: i
     base_logits [Bs, N, V]: base logits of the requests req_ids (default 0..Bs-1);
     req_ids give the request index b used in the random-number counter, so a
     subset of a large batch can be checked alone.  anchor, temperature: [Bs].
-    The Gumbel noise of step i, request b, token v is the stream-0 Philox
-    variate of counter (v >> 2, b, i, offset), word v & 3.
+    The Gumbel noise of step i, request b, token v is the variate of the
+    split draft word of ``philox.draft_word`` (high half from stream 0, low half
+    from stream 3, counter (v >> 3, b, i, offset)).
     """
     L = np.asarray(base_logits)
     req = np.arange(L.shape[0]) if req_ids is None else np.asarray(req_ids)
