@@ -15,7 +15,7 @@ import os
 __all__ = [
     "DSparkError", "lib", "Workspace", "OP_DRAFT_LOGITS", "OP_MARKOV_SAMPLE", "OP_VERIFY",
     "OP_SCHEDULE", "OP_VERIFY_GREEDY", "OP_CONFIDENCE", "dspark_workspace_size", "dspark_verify_greedy",
-    "dspark_confidence", "dspark_draft_logits", "dspark_markov_sample",
+    "dspark_confidence", "dspark_markov_sample_reduced", "D2T_INDEX", "D2T_OFFSET", "dspark_draft_logits", "dspark_markov_sample",
     "dspark_verify", "dspark_schedule", "dspark_read_status", "dspark_status_string",
     "dspark_selftest_wait_timeout", "STATUS_TIMEOUT", "STATUS_NUMERIC", "STATUS_INPUT_RANGE",
     "STATUS_INTERNAL",
@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdspark.s
 
 OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE, OP_VERIFY_GREEDY, OP_CONFIDENCE = 0, 1, 2, 3, 4, 5
 F32, BF16 = 0, 1
+D2T_INDEX, D2T_OFFSET = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NUMERIC, ERR_INPUT_RANGE = range(7)
 STATUS_TIMEOUT, STATUS_NUMERIC, STATUS_INPUT_RANGE, STATUS_INTERNAL = 0x1, 0x2, 0x4, 0x8
 
@@ -52,6 +53,8 @@ def lib() -> ctypes.CDLL:
     L.dspark_draft_logits.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
     L.dspark_markov_sample.argtypes = [vp, vp, vp, vp, i32, vp, u64, u64, i32, i32, i32, i32,
                                        vp, vp, vp, sz, vp]
+    L.dspark_markov_sample_reduced.argtypes = [vp, vp, vp, vp, i32, vp, u64, u64, i32, i32, i32, i32,
+                                               vp, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify.argtypes = [vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_confidence.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, i32,
@@ -180,6 +183,33 @@ def dspark_markov_sample(base_logits, anchor, w1, w2, temperature, seed: int, of
                                       _ptr(temperature), seed, offset, B, N, V, r,
                                       _ptr(draft_tokens), _ptr(lse), ws.ptr, ws.nbytes,
                                       _stream(stream)), "dspark_markov_sample")
+    return draft_tokens
+
+
+def dspark_markov_sample_reduced(base_logits, anchor, w1, w2, temperature, seed: int, offset: int, d2t,
+                                 mode: int, V_target: int, draft_tokens=None, lse=None, workspace=None,
+                                 stream=None):
+    """dspark_markov_sample on a reduced draft vocabulary (V = base_logits.shape[2]); the tokens come
+    back as target-vocabulary ids through `d2t` [V] int32 (mode D2T_INDEX: d2t[d]; D2T_OFFSET:
+    d + d2t[d])."""
+    torch = _torch()
+    _need(base_logits, "base_logits", (torch.float32,), 3)
+    _need(anchor, "anchor", (torch.int32,), 1)
+    _need(w1, "w1", (torch.bfloat16, torch.float32), 2)
+    _need(w2, "w2", (w1.dtype,), 2)
+    _need(temperature, "temperature", (torch.float32,), 1)
+    _need(d2t, "d2t", (torch.int32,), 1)
+    B, N, V = base_logits.shape
+    r = w1.shape[1]
+    if tuple(w2.shape) != (V, r) or w1.shape[0] != V or d2t.shape[0] != V:
+        raise ValueError("w1 and w2 must both be [V, r] and d2t [V] over the draft vocabulary")
+    if draft_tokens is None:
+        draft_tokens = torch.empty(B, N, dtype=torch.int32, device=base_logits.device)
+    ws = _ws(workspace, OP_MARKOV_SAMPLE, B, N, V, r, base_logits.device)
+    _check(lib().dspark_markov_sample_reduced(_ptr(base_logits), _ptr(anchor), _ptr(w1), _ptr(w2), _dt(w1),
+                                              _ptr(temperature), seed, offset, B, N, V, r, _ptr(d2t), int(mode),
+                                              int(V_target), _ptr(draft_tokens), _ptr(lse), ws.ptr, ws.nbytes,
+                                              _stream(stream)), "dspark_markov_sample_reduced")
     return draft_tokens
 
 

@@ -222,7 +222,36 @@ dspark_status dspark_markov_sample(const float* base_logits, const int32_t* anch
     DeviceInfo dev;
     if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
     return launch_markov_sample(base_logits, anchor, w1, w2, wdtype, temperature, seed,
-                                static_cast<uint32_t>(offset), B, N, V, r, draft_tokens, lse, workspace,
+                                static_cast<uint32_t>(offset), B, N, V, r, draft_tokens, lse, nullptr, 0, V,
+                                workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
+dspark_status dspark_markov_sample_reduced(const float* base_logits, const int32_t* anchor, const void* w1,
+                                           const void* w2, dspark_dtype wdtype, const float* temperature,
+                                           uint64_t seed, uint64_t offset, int B, int N, int V, int r,
+                                           const int32_t* d2t, int d2t_mode, int V_target,
+                                           int32_t* draft_tokens, float* lse, void* workspace, size_t ws_bytes,
+                                           void* stream) {
+    g_error[0] = '\0';
+    DSPARK_REQUIRE(d2t != nullptr, "markov_sample_reduced: null d2t table");
+    DSPARK_REQUIRE(d2t_mode == DSPARK_D2T_INDEX || d2t_mode == DSPARK_D2T_OFFSET,
+                   "markov_sample_reduced: unknown table mode %d", d2t_mode);
+    DSPARK_REQUIRE(V_target >= 1, "markov_sample_reduced: V_target must be positive");
+    DSPARK_REQUIRE(base_logits && anchor && w1 && w2 && temperature && draft_tokens,
+                   "markov_sample: null pointer");
+    DSPARK_REQUIRE(wdtype == DSPARK_F32 || wdtype == DSPARK_BF16, "markov_sample: unknown dtype %d", (int)wdtype);
+    DSPARK_REQUIRE(B >= 1 && N >= 1 && N <= 65535 && V >= 2 && r >= 1 && r <= 1024,
+                   "markov_sample: bad sizes (B=%d N=%d V=%d r=%d)", B, N, V, r);
+    DSPARK_REQUIRE(offset < (1ull << 32), "markov_sample: offset must be below 2^32");
+    DSPARK_REQUIRE(aligned(base_logits, 4) && aligned(w1, 16) && aligned(w2, 16),
+                   "markov_sample: w1/w2 must be 16-byte aligned");
+    if (bad_ws(workspace, ws_bytes, dspark_workspace_size(DSPARK_OP_MARKOV_SAMPLE, B, N, V, r)))
+        return DSPARK_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
+    return launch_markov_sample(base_logits, anchor, w1, w2, wdtype, temperature, seed,
+                                static_cast<uint32_t>(offset), B, N, V, r, draft_tokens, lse, d2t,
+                                d2t_mode == DSPARK_D2T_OFFSET ? 1 : 0, V_target, workspace,
                                 static_cast<cudaStream_t>(stream), dev);
 }
 

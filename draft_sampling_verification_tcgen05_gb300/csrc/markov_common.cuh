@@ -63,8 +63,24 @@ struct MarkovArgs {
     int exchange;               // blocks publish per-step candidates and poll each other's
                                 // (instead of step slots and a grid barrier)
     int w2_split;               // cached w2 rows stored even rows first, then odd rows
+    const int32_t* d2t;         // [V] draft-to-target table, or null (tokens are draft ids)
+    int d2t_offset;             // 0: target = d2t[d]; 1: target = d + d2t[d]
+    int V_target;               // range of the mapped ids
     long long timeout_ns;
 };
+
+// The token written for sampled draft id d: d itself, or its target-vocabulary id through the
+// table ("DSpark implementation and evaluation" §5 index table; EAGLE-3's offset table); a
+// mapped id outside [0, V_target) is written as -1 and flagged.
+__device__ __forceinline__ int32_t output_token(const MarkovArgs& a, int d) {
+    if (a.d2t == nullptr) return d;
+    const long long t = a.d2t_offset ? static_cast<long long>(d) + a.d2t[d] : static_cast<long long>(a.d2t[d]);
+    if (t < 0 || t >= a.V_target) {
+        set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+        return -1;
+    }
+    return static_cast<int32_t>(t);
+}
 
 __device__ __forceinline__ float gumbel_at(const MarkovArgs& a, int b, int i, int v) {
     return gumbel_from_word(draft_word(a.seed, a.offset, static_cast<uint32_t>(b), static_cast<uint32_t>(i),

@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         if (a.exchange) __syncthreads();          // the last step's winners, written by other threads
         for (int idx = tid; idx < a.B * a.N; idx += kThreads) {
             const int b = idx / a.N, i = idx % a.N;
-            a.tokens[idx] = a.exchange ? s_tok[i * a.B + b] : slot_token(a, i, b);
+            a.tokens[idx] = output_token(a, a.exchange ? s_tok[i * a.B + b] : slot_token(a, i, b));
         }
     }
 }
@@ -558,8 +558,8 @@ size_t markov_workspace_bytes(int B, int N) {
 dspark_status launch_markov_sample(const float* base_logits, const int32_t* anchor, const void* w1,
                                    const void* w2, dspark_dtype wdtype, const float* temperature,
                                    uint64_t seed, uint32_t offset, int B, int N, int V, int r,
-                                   int32_t* draft_tokens, float* lse, void* ws, cudaStream_t stream,
-                                   const DeviceInfo& dev) {
+                                   int32_t* draft_tokens, float* lse, const int32_t* d2t, int d2t_offset,
+                                   int V_target, void* ws, cudaStream_t stream, const DeviceInfo& dev) {
     // clear header, slots, bounds, publication counters and the candidate entries a grid of
     // at most one block per SM uses (the lse partials need no clearing)
     const MarkovLayout lay = markov_layout(ws, B, N);
@@ -584,6 +584,9 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
     a.N = N;
     a.V = V;
     a.r = r;
+    a.d2t = d2t;
+    a.d2t_offset = d2t_offset;
+    a.V_target = V_target;
     a.timeout_ns = kDefaultTimeoutNs;
     if (markov_tc_eligible(B, N, V, r, wdtype, base_logits, lse, dev.sm_count))
         return launch_markov_tc(a, stream, dev);

@@ -520,7 +520,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         if (alive && blockIdx.x == 0) {
             for (int idx = stid; idx < a.B * a.N; idx += kStepThreads) {
                 const int b = idx / a.N, i = idx % a.N;
-                a.tokens[idx] = slot_token(a, i, b);
+                a.tokens[idx] = output_token(a, slot_token(a, i, b));
             }
         }
     }

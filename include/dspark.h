@@ -147,6 +147,38 @@ DSPARK_API dspark_status dspark_markov_sample(const float* base_logits, const in
                                    int32_t* draft_tokens, float* lse,
                                    void* workspace, size_t ws_bytes, void* stream);
 
+/* Draft-to-target id table conventions of dspark_markov_sample_reduced. */
+typedef enum {
+    DSPARK_D2T_INDEX = 0,    /* target id = d2t[draft id] (the draft logits scattered into target positions) */
+    DSPARK_D2T_OFFSET = 1    /* target id = draft id + d2t[draft id] */
+} dspark_d2t_mode;
+
+/*
+ * dspark_markov_sample on a reduced draft vocabulary: V is the draft
+ * vocabulary (base_logits [B, N, V], w1 and w2 [V, r] and the anchor are in
+ * draft ids, and the Markov chain feeds back draft ids); each sampled draft id
+ * d is written to draft_tokens as its target-vocabulary id, d2t[d]
+ * (DSPARK_D2T_INDEX: "DSpark implementation and evaluation" §5 scatters the
+ * draft logits into target positions through an index table) or d + d2t[d]
+ * (DSPARK_D2T_OFFSET: "xserv/docs/25-speculative-methods-comparison.md" §3.2,
+ * real_id = draft_id + d2t[draft_id]).  Sampling is Gumbel-max over the draft
+ * entries with noise indexed by draft id -- the same distribution as over the
+ * scattered target-size buffer.
+ *
+ *   d2t       [V] int32, device
+ *   V_target  size of the target vocabulary; a mapped id outside [0, V_target)
+ *             is written as -1 and sets INPUT_RANGE
+ * Everything else (arguments, requirements, workspace) as dspark_markov_sample;
+ * lse, when requested, is over the draft vocabulary.
+ */
+DSPARK_API dspark_status dspark_markov_sample_reduced(const float* base_logits, const int32_t* anchor,
+                                           const void* w1, const void* w2, dspark_dtype wdtype,
+                                           const float* temperature, uint64_t seed, uint64_t offset,
+                                           int B, int N, int V, int r,
+                                           const int32_t* d2t, int d2t_mode, int V_target,
+                                           int32_t* draft_tokens, float* lse,
+                                           void* workspace, size_t ws_bytes, void* stream);
+
 /*
  * Lossless speculative verification (rejection sampling) of a block of gamma
  * draft tokens per request.

@@ -29,7 +29,7 @@ def test_every_declared_symbol_is_exported(L):
     for n in names:
         assert hasattr(L, n), n
     for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule",
-               "dspark_verify_greedy", "dspark_confidence"):
+               "dspark_verify_greedy", "dspark_confidence", "dspark_markov_sample_reduced"):
         assert op in names
 
 
@@ -56,6 +56,10 @@ def test_host_validation_without_gpu(L):
     assert L.dspark_markov_sample(fake, fake, fake, fake, 1, fake, 0, 0, 1, 0, 100, 64,
                                   fake, null, fake, 1 << 20, null) == 1                   # N = 0
     assert L.dspark_verify(fake, fake, fake, null, 0, 0, 1, 0, 10, fake, fake, fake, 256, null) == 1
+    assert L.dspark_markov_sample_reduced(fake, fake, fake, fake, 1, fake, 0, 0, 1, 8, 100, 64, null, 0, 500,
+                                          fake, null, fake, 1 << 20, null) == 1                # no table
+    assert L.dspark_markov_sample_reduced(fake, fake, fake, fake, 1, fake, 0, 0, 1, 8, 100, 64, fake, 2, 500,
+                                          fake, null, fake, 1 << 20, null) == 1                # mode
     assert L.dspark_verify_greedy(fake, fake, null, 1, 0, 10, fake, fake, fake, 1 << 20, null) == 1  # gamma = 0
     assert L.dspark_verify_greedy(null, fake, null, 1, 2, 10, fake, fake, fake, 1 << 20, null) == 1
     assert L.dspark_verify_greedy(fake, fake, null, 4, 8, 10, fake, fake, fake, 64, null) == 1      # workspace
