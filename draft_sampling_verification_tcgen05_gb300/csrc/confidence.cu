@@ -9,8 +9,9 @@
 // the Markov head uses at step i).
 //
 // One warp per (request, position): 16-byte loads of the hidden row (the LM
-// head's input row) and of w_h, the r Markov features, a shuffle reduction,
-// fp32 throughout.  The output feeds dspark_schedule's cond_accept directly.
+// head's input row) and of w_h, eight in flight per lane, the r Markov
+// features, a shuffle reduction, fp32 throughout.  The output feeds
+// dspark_schedule's cond_accept directly.
 #include "device_common.cuh"
 #include "host_common.h"
 
@@ -48,6 +49,7 @@ __device__ __forceinline__ float lane_dot(const T* row, const float* w, int n, u
     int done = 0;
     if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0) {
         const int pieces = n / kPer;
+#pragma unroll 8
         for (int p = static_cast<int>(lane); p < pieces; p += 32) {
             const uint4 q = *reinterpret_cast<const uint4*>(row + p * kPer);
             const T* e = reinterpret_cast<const T*>(&q);
