@@ -33,6 +33,7 @@ from .schedule import schedule, survival_chain
 from .greedy import verify_greedy, row_argmax
 from .confidence import confidence
 from .reduced_vocab import map_to_target, markov_sample_reduced
+from .verify_logits import verify_from_logits, draft_distributions, draft_lse, residual_gumbel
 
 __all__ = [
     "philox4x32_10", "philox_words", "uniform_from_word", "gumbel_from_word",
@@ -40,4 +41,5 @@ __all__ = [
     "verify", "acceptance_probability_exact",
     "schedule", "survival_chain",
     "verify_greedy", "row_argmax", "confidence", "map_to_target", "markov_sample_reduced",
+    "verify_from_logits", "draft_distributions", "draft_lse", "residual_gumbel",
 ]

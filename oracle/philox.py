@@ -26,6 +26,7 @@ verification uses a seeded uniform ("DSpark implementation and evaluation"
   since u, and so g, is increasing in the word)
   stream 1 = verify accept uniform   (i = draft position k, j = 0, word 0)
   stream 2 = verify resample         (i = position, j = 0, words 0 and 1)
+  stream 4 = from-logits resample    (i = position, j = v >> 2, word v & 3 of element v)
 
 Uniform: u = ((w >> 9) + 1/2) * 2**-23, which lies in [2**-24, 1 - 2**-24]
 and is exactly representable in float32.  Gumbel: g = -log(-log(u)).
@@ -45,6 +46,7 @@ STREAM_GUMBEL = 0
 STREAM_ACCEPT = 1
 STREAM_RESAMPLE = 2
 STREAM_GUMBEL_LO = 3
+STREAM_RESIDUAL = 4          # Gumbel noise of the from-logits resample draw
 
 
 def philox4x32_10(c0, c1, c2, c3, k0, k1):
