@@ -420,6 +420,35 @@ def run_gpu(args):
         torch.cuda.synchronize()
         r_ms.append(e0.elapsed_time(e1))
     red_ms = float(np.median(r_ms))
+    # verification straight from logits (the draft distribution never written): target logits
+    # log p_t of the step's target rows, the step's draft base logits, tokens and sampler lse
+    lse_d = torch.empty(B, N, dtype=torch.float32, device=dev)
+    ws_m2 = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
+    ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, draft_tokens=tok,
+                            lse=lse_d, workspace=ws_m2)
+    t_logits = torch.log(p_t.clamp_min(1e-30))
+    T_t = torch.ones(B, dtype=torch.float32, device=dev)
+    ws_l = ds.Workspace(ds.OP_VERIFY_LOGITS, B, N, V, r, device=dev)
+    l_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    l_nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    vl_args = (t_logits, T_t, L_markov.view(B, N, V), anchor, w1, w2, temp, lse_d, tok, None, seed_verify, 0)
+    for _ in range(3):
+        ds.dspark_verify_logits(*vl_args, out_tokens=l_out, num_accepted=l_nacc, workspace=ws_l)
+    l_ms = []
+    for k in range(20):
+        flush_l2(k)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ds.dspark_verify_logits(*vl_args, out_tokens=l_out, num_accepted=l_nacc, workspace=ws_l)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        l_ms.append(e0.elapsed_time(e1))
+    vlog_ms = float(np.median(l_ms))
+    # bytes with every request rejected by a sampled draft: the target rows k <= gamma once for
+    # the normalisers, then per request the target row, base-logit row and bias row of k* read,
+    # the bias row written, and markov_w2 read by the bias GEMM
+    vlog_bytes = B * (N + 1) * V * 4 + 4 * B * V * 4 + V * r * w2.element_size()
+    del ws_l, ws_m2, t_logits
 
     # ---------------- roofline of the dominant kernel ----------------
     peaks = {}
@@ -476,6 +505,11 @@ def run_gpu(args):
                        "achieved": conf_bytes / (conf_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                        "frac": conf_bytes / (conf_ms / 1e3) / 1e9 / hbm_peak,
                        "note": "median of 20 launches, L2 flushed, outside the step (latency-bound at these sizes)"},
+        "verify_logits": {"ms": vlog_ms, "bound": "hbm", "algorithmic_bytes": vlog_bytes,
+                          "achieved": vlog_bytes / (vlog_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                          "frac": vlog_bytes / (vlog_ms / 1e3) / 1e9 / hbm_peak,
+                          "accepted_mean": float(l_nacc.float().mean().item()),
+                          "note": "median of 20 calls (3 kernels + bias GEMM), L2 flushed, outside the step"},
         "verify_greedy": {"ms": greedy_ms, "bound": "hbm", "algorithmic_bytes": B * (N + 1) * V * 4,
                           "achieved": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9, "peak": hbm_peak,
                           "unit": "GB/s", "frac": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9 / hbm_peak,

@@ -14,7 +14,8 @@ import os
 
 __all__ = [
     "DSparkError", "lib", "Workspace", "OP_DRAFT_LOGITS", "OP_MARKOV_SAMPLE", "OP_VERIFY",
-    "OP_SCHEDULE", "OP_VERIFY_GREEDY", "OP_CONFIDENCE", "dspark_workspace_size", "dspark_verify_greedy",
+    "OP_SCHEDULE", "OP_VERIFY_GREEDY", "OP_CONFIDENCE", "OP_VERIFY_LOGITS", "dspark_workspace_size",
+    "dspark_verify_greedy", "dspark_verify_logits",
     "dspark_confidence", "dspark_markov_sample_reduced", "D2T_INDEX", "D2T_OFFSET", "dspark_draft_logits", "dspark_markov_sample",
     "dspark_verify", "dspark_schedule", "dspark_read_status", "dspark_status_string",
     "dspark_selftest_wait_timeout", "STATUS_TIMEOUT", "STATUS_NUMERIC", "STATUS_INPUT_RANGE",
@@ -24,6 +25,7 @@ __all__ = [
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdspark.so")
 
 OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE, OP_VERIFY_GREEDY, OP_CONFIDENCE = 0, 1, 2, 3, 4, 5
+OP_VERIFY_LOGITS = 6
 F32, BF16 = 0, 1
 D2T_INDEX, D2T_OFFSET = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NUMERIC, ERR_INPUT_RANGE = range(7)
@@ -57,6 +59,8 @@ def lib() -> ctypes.CDLL:
                                                vp, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify.argtypes = [vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.dspark_verify_logits.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, u64, u64, i32, i32, i32,
+                                       vp, vp, vp, sz, vp]
     L.dspark_confidence.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, i32,
                                     vp, vp, sz, vp]
     L.dspark_schedule.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
@@ -256,6 +260,43 @@ def dspark_verify_greedy(target, draft_tokens, lengths=None, out_tokens=None, nu
     _check(lib().dspark_verify_greedy(_ptr(target), _ptr(draft_tokens), _ptr(lengths), B, gamma, V,
                                       _ptr(out_tokens), _ptr(num_accepted), ws.ptr, ws.nbytes, _stream(stream)),
            "dspark_verify_greedy")
+    return out_tokens, num_accepted
+
+
+def dspark_verify_logits(target_logits, target_temperature, base_logits, anchor, w1, w2, draft_temperature,
+                         draft_lse, draft_tokens, lengths, seed: int, offset: int, out_tokens=None,
+                         num_accepted=None, workspace=None, stream=None):
+    """Lossless verification from logits with the draft distribution recomputed;
+    returns (out_tokens [B, gamma+1], num_accepted [B])."""
+    torch = _torch()
+    _need(target_logits, "target_logits", (torch.float32,), 3)
+    _need(base_logits, "base_logits", (torch.float32,), 3)
+    _need(target_temperature, "target_temperature", (torch.float32,), 1)
+    _need(draft_temperature, "draft_temperature", (torch.float32,), 1)
+    _need(anchor, "anchor", (torch.int32,), 1)
+    _need(w1, "w1", (torch.bfloat16, torch.float32), 2)
+    _need(w2, "w2", (w1.dtype,), 2)
+    _need(draft_lse, "draft_lse", (torch.float32,), 2)
+    _need(draft_tokens, "draft_tokens", (torch.int32,), 2)
+    B, gamma, V = base_logits.shape
+    r = w1.shape[1]
+    if (tuple(target_logits.shape) != (B, gamma + 1, V) or tuple(draft_tokens.shape) != (B, gamma)
+            or tuple(draft_lse.shape) != (B, gamma) or tuple(w1.shape) != (V, r) or tuple(w2.shape) != (V, r)
+            or anchor.shape[0] != B or target_temperature.shape[0] != B or draft_temperature.shape[0] != B):
+        raise ValueError("shapes: target_logits [B, gamma+1, V], base_logits [B, gamma, V], w1/w2 [V, r], "
+                         "draft_lse / draft_tokens [B, gamma], anchor / temperatures [B]")
+    if lengths is not None:
+        _need(lengths, "lengths", (torch.int32,), 1)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=target_logits.device)
+    if num_accepted is None:
+        num_accepted = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    ws = _ws(workspace, OP_VERIFY_LOGITS, B, gamma, V, r, target_logits.device)
+    _check(lib().dspark_verify_logits(_ptr(target_logits), _ptr(target_temperature), _ptr(base_logits),
+                                      _ptr(anchor), _ptr(w1), _ptr(w2), _dt(w1), r, _ptr(draft_temperature),
+                                      _ptr(draft_lse), _ptr(draft_tokens), _ptr(lengths), seed, offset, B, gamma,
+                                      V, _ptr(out_tokens), _ptr(num_accepted), ws.ptr, ws.nbytes,
+                                      _stream(stream)), "dspark_verify_logits")
     return out_tokens, num_accepted
 
 

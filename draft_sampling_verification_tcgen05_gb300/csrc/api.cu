@@ -176,6 +176,8 @@ size_t dspark_workspace_size(int op, int B, int N, int V, int r) {
             return verify_greedy_workspace_bytes(B, N);
         case DSPARK_OP_CONFIDENCE:
             return sizeof(WsHeader);
+        case DSPARK_OP_VERIFY_LOGITS:
+            return verify_logits_workspace_bytes(B, N, V, r);
         default:
             return 0;
     }
@@ -288,6 +290,35 @@ dspark_status dspark_verify_greedy(const float* target, const int32_t* draft_tok
     DeviceInfo dev;
     if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
     return launch_verify_greedy(target, draft_tokens, lengths, B, gamma, V, out_tokens, num_accepted, workspace,
+                                static_cast<cudaStream_t>(stream), dev);
+}
+
+dspark_status dspark_verify_logits(const float* target_logits, const float* target_temperature,
+                                   const float* base_logits, const int32_t* anchor, const void* w1, const void* w2,
+                                   dspark_dtype wdtype, int r, const float* draft_temperature, const float* draft_lse,
+                                   const int32_t* draft_tokens, const int32_t* lengths, uint64_t seed,
+                                   uint64_t offset, int B, int gamma, int V, int32_t* out_tokens,
+                                   int32_t* num_accepted, void* workspace, size_t ws_bytes, void* stream) {
+    g_error[0] = '\0';
+    DSPARK_REQUIRE(target_logits && target_temperature && base_logits && anchor && w1 && w2 && draft_temperature &&
+                       draft_lse && draft_tokens && out_tokens && num_accepted,
+                   "verify_logits: null pointer");
+    DSPARK_REQUIRE(wdtype == DSPARK_F32 || wdtype == DSPARK_BF16, "verify_logits: unknown dtype %d", (int)wdtype);
+    DSPARK_REQUIRE(B >= 1 && gamma >= 1 && gamma <= 65535 && V >= 2 && r >= 1 && r <= 1024,
+                   "verify_logits: bad sizes (B=%d gamma=%d V=%d r=%d)", B, gamma, V, r);
+    const size_t esize = wdtype == DSPARK_F32 ? 4 : 2;
+    DSPARK_REQUIRE((static_cast<size_t>(r) * esize) % 16 == 0,
+                   "verify_logits: r*sizeof(wdtype) must be a multiple of 16 bytes (r=%d)", r);
+    DSPARK_REQUIRE(offset < (1ull << 32), "verify_logits: offset must be below 2^32");
+    DSPARK_REQUIRE(aligned(target_logits, 16) && aligned(base_logits, 16) && aligned(w1, 16) && aligned(w2, 16),
+                   "verify_logits: target_logits, base_logits, w1, w2 must be 16-byte aligned");
+    if (bad_ws(workspace, ws_bytes, dspark_workspace_size(DSPARK_OP_VERIFY_LOGITS, B, gamma, V, r)))
+        return DSPARK_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
+    return launch_verify_logits(target_logits, target_temperature, base_logits, anchor, w1, w2, wdtype,
+                                draft_temperature, draft_lse, draft_tokens, lengths, seed,
+                                static_cast<uint32_t>(offset), B, gamma, V, r, out_tokens, num_accepted, workspace,
                                 static_cast<cudaStream_t>(stream), dev);
 }
 

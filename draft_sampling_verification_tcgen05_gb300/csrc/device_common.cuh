@@ -208,7 +208,13 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 }
 
 // Counter layout of this library: (j, b, (stream << 16) | i, offset).
-enum : uint32_t { kStreamGumbel = 0, kStreamAccept = 1, kStreamResample = 2, kStreamGumbelLo = 3 };
+enum : uint32_t {
+    kStreamGumbel = 0,
+    kStreamAccept = 1,
+    kStreamResample = 2,
+    kStreamGumbelLo = 3,
+    kStreamResidual = 4,        // from-logits resample: word v & 3 of counter j = v >> 2
+};
 
 __device__ __forceinline__ uint4 philox_at(uint64_t seed, uint32_t offset, uint32_t j, uint32_t b,
                                            uint32_t stream, uint32_t i) {

@@ -65,6 +65,14 @@ dspark_status launch_verify(const float* p_target, const float* p_draft, const i
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
                             cudaStream_t stream, const DeviceInfo& dev);
 
+size_t verify_logits_workspace_bytes(int B, int gamma, int V, int r);
+dspark_status launch_verify_logits(const float* target_logits, const float* T_t, const float* base_logits,
+                                   const int32_t* anchor, const void* w1, const void* w2, dspark_dtype wdtype,
+                                   const float* T_d, const float* draft_lse, const int32_t* draft_tokens,
+                                   const int32_t* lengths, uint64_t seed, uint32_t offset, int B, int gamma,
+                                   int V, int r, int32_t* out_tokens, int32_t* num_accepted, void* ws,
+                                   cudaStream_t stream, const DeviceInfo& dev);
+
 size_t schedule_workspace_bytes(int B, int N);
 dspark_status launch_schedule(const float* cond_accept, const double* sps, int S, int B, int N,
                               int K_in, float* survival, int32_t* K_out, int32_t* lengths,

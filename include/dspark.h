@@ -69,7 +69,8 @@ typedef enum {
     DSPARK_OP_VERIFY = 2,
     DSPARK_OP_SCHEDULE = 3,
     DSPARK_OP_VERIFY_GREEDY = 4,
-    DSPARK_OP_CONFIDENCE = 5
+    DSPARK_OP_CONFIDENCE = 5,
+    DSPARK_OP_VERIFY_LOGITS = 6
 } dspark_op;
 
 /* Device status-word bits (OR-ed by kernels; read with dspark_read_status). */
@@ -87,6 +88,8 @@ typedef enum {
  *   DSPARK_OP_SCHEDULE      grows with B*N (radix-sort key buffers)
  *   DSPARK_OP_VERIFY_GREEDY grows with B*(N+1) (row argmax keys); N = gamma
  *   DSPARK_OP_CONFIDENCE    256 (the status word)
+ *   DSPARK_OP_VERIFY_LOGITS grows with B*V (one bias row per request) and
+ *                           B*(N+1)*V/2048 (normaliser partials); N = gamma
  * Returns 0 for an unknown op or negative sizes.
  */
 DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);
@@ -243,6 +246,65 @@ DSPARK_API dspark_status dspark_verify(const float* p_target, const float* p_dra
  */
 DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t* draft_tokens,
                                    const int32_t* lengths, int B, int gamma, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Lossless verification from logits, the draft distribution recomputed.
+ *
+ * "Speculative decoding: from zero to DSpark" §2 (the rule, as dspark_verify)
+ * with the distributions of "DSpark implementation and evaluation" §2.2 / §5:
+ *   p_t(. | row k) = softmax(target_logits[b, k] / T_t[b])
+ *   p_d(. | pos k) = softmax((base_logits[b, k] + w2 . w1[prev_k]) / T_d[b]),
+ *                    prev_0 = anchor[b], prev_k = draft_tokens[b, k-1];
+ *                    T_d = 0 (a greedy draft): the point mass at draft_tokens[b, k].
+ * No [B, gamma, V] draft probabilities are read or written: p_d(x_k) is
+ * recomputed at the drafted token from the base logit, one r-long dot product
+ * and the sampler's log-sum-exp (draft_lse = dspark_markov_sample's lse
+ * output), and the whole draft row only at the rejected position, its bias
+ * rows coming from one tcgen05 GEMM.  The target normalisers are computed here
+ * (rows k <= L_b only).
+ * Acceptance: fl32(u_k * p_d(x_k)) < p_t(x_k), u_k the stream-1 uniform as in
+ * dspark_verify.  The correction (residual max(0, p_t - p_d) at the first
+ * rejection) or bonus (p_t of row L_b) token is drawn by Gumbel-max,
+ * argmax_v ln w_v + g_v, g_v the Gumbel variate of Philox stream 4, word v & 3
+ * of counter (v >> 2, b, (4 << 16) | position, offset); ties go to the lowest
+ * id, a residual with no positive entry falls back to p_t.  Everything is fp32:
+ * a decision can differ from an exact evaluation only within rounding of its
+ * boundary (relative 1e-5 for an acceptance test, a top-2 gap of ~1e-4 for a
+ * draw).
+ *
+ *   target_logits [B, gamma+1, V] fp32, device
+ *   target_temperature [B] fp32, device, > 0
+ *   base_logits   [B, gamma, V] fp32, device: the draft's base logits of the
+ *                 drafted positions (dspark_draft_logits' output)
+ *   anchor        [B] int32, device: the token before the block
+ *   w1, w2        [V, r] wdtype (bf16 or fp32), device: markov_w1, markov_w2
+ *                 (fp32 weights: the bias rows of the rejected positions are
+ *                 computed with tf32 tensor-core products)
+ *   draft_temperature [B] fp32, device, >= 0
+ *   draft_lse     [B, gamma] fp32, device: the sampler's lse of each drafted
+ *                 position (ignored where T_d = 0)
+ *   draft_tokens  [B, gamma] int32, device
+ *   lengths       [B] int32 in [0, gamma], device, or NULL (= gamma)
+ *   out_tokens    [B, gamma+1] int32 output: accepted prefix, the correction
+ *                 or bonus token, then -1
+ *   num_accepted  [B] int32 output
+ * Requirements: B >= 1, 1 <= gamma <= 65535, 2 <= V < 2^31, 1 <= r <= 1024
+ * with r * sizeof(wdtype) a multiple of 16 bytes, offset < 2^32;
+ * target_logits, base_logits, w1, w2 16-byte aligned.
+ * Device-side: a token, anchor or length out of range or a temperature out of
+ * its range sets INPUT_RANGE, a non-finite normaliser or draft_lse sets
+ * NUMERIC; such a request outputs num_accepted 0 and -1 tokens.
+ * Launches three kernels on `stream` (captured by CUDA stream capture).
+ * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY_LOGITS, B, gamma, V, r).
+ */
+DSPARK_API dspark_status dspark_verify_logits(const float* target_logits, const float* target_temperature,
+                                   const float* base_logits, const int32_t* anchor,
+                                   const void* w1, const void* w2, dspark_dtype wdtype, int r,
+                                   const float* draft_temperature, const float* draft_lse,
+                                   const int32_t* draft_tokens, const int32_t* lengths,
+                                   uint64_t seed, uint64_t offset, int B, int gamma, int V,
                                    int32_t* out_tokens, int32_t* num_accepted,
                                    void* workspace, size_t ws_bytes, void* stream);
 

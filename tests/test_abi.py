@@ -29,7 +29,8 @@ def test_every_declared_symbol_is_exported(L):
     for n in names:
         assert hasattr(L, n), n
     for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule",
-               "dspark_verify_greedy", "dspark_confidence", "dspark_markov_sample_reduced"):
+               "dspark_verify_greedy", "dspark_confidence", "dspark_markov_sample_reduced",
+               "dspark_verify_logits"):
         assert op in names
 
 
@@ -41,6 +42,10 @@ def test_workspace_sizes(L):
     assert L.dspark_workspace_size(3, 1024, 16, 0, 0) == 256 + 2 * 8 * 1024 * 16
     assert L.dspark_workspace_size(4, 256, 8, 151936, 0) == 256 + 8 * 256 * 9 + 1024
     assert L.dspark_workspace_size(5, 64, 16, 151936, 256) == 256
+    vl = L.dspark_workspace_size(6, 256, 8, 151936, 256)
+    # keys, two counters, decisions, row selections, normaliser partials, w1 rows, bias rows
+    assert vl == 256 + 256 * (8 + 4 + 4 + 4 + 16) + 8 * 256 * 9 * 75 + 4 * 256 * 256 + 4 * 256 * 151936
+    assert L.dspark_workspace_size(6, 0, 8, 100, 8) == 0
     assert L.dspark_workspace_size(9, 1, 1, 1, 1) == 0
 
 
@@ -63,6 +68,23 @@ def test_host_validation_without_gpu(L):
     assert L.dspark_verify_greedy(fake, fake, null, 1, 0, 10, fake, fake, fake, 1 << 20, null) == 1  # gamma = 0
     assert L.dspark_verify_greedy(null, fake, null, 1, 2, 10, fake, fake, fake, 1 << 20, null) == 1
     assert L.dspark_verify_greedy(fake, fake, null, 4, 8, 10, fake, fake, fake, 64, null) == 1      # workspace
+    vl = [fake, fake, fake, fake, fake, fake, 1, 64, fake, fake, fake, null, 0, 0, 4, 8, 1000, fake, fake, fake,
+          1 << 30, null]
+
+    def vl_with(**kw):
+        args = list(vl)
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return L.dspark_verify_logits(*args)
+
+    assert vl_with(a6=2) == 1                                                # dtype
+    assert vl_with(a7=4) == 1                                                # r * 2 bytes not a multiple of 16
+    assert vl_with(a7=2048) == 1                                             # r too large
+    assert vl_with(a13=2 ** 32) == 1                                         # offset
+    assert vl_with(a15=0) == 1                                               # gamma = 0
+    assert vl_with(a9=null) == 1                                             # no draft lse
+    assert vl_with(a0=ctypes.c_void_p(4100)) == 1                            # misaligned logits
+    assert vl_with(a20=1024) == 1                                            # workspace
     assert L.dspark_confidence(fake, 1, fake, 1, fake, fake, fake, fake, 0.0, fake, 1, 8, 64, 100, 0,
                                fake, fake, 256, null) == 1                                   # r = 0
     assert L.dspark_confidence(fake, 3, fake, 1, fake, fake, fake, fake, 0.0, fake, 1, 8, 64, 100, 8,

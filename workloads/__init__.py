@@ -21,6 +21,8 @@ from zero to DSpark" §2, §5-§7):
   qwen3_8b_single    B=1,    N=8,  H=4096, V=151936, r=64,  bf16
   batched_draft      B=64,   N=16, H=4096, V=151936, r=256, bf16, T=0.8
   verify             B=256,  gamma=8,     V=151936,  fp32 probabilities
+  verify (logits)    B=256,  gamma=8,     V=151936,  r=256, bf16 Markov weights,
+                     fp32 target / draft base logits
   schedule           B=1024, N=16, SPS table over batch sizes 1..16384
 """
 from __future__ import annotations
@@ -34,7 +36,8 @@ import numpy as np
 
 __all__ = [
     "DraftConfig", "VerifyConfig", "ScheduleConfig", "DRAFT_CONFIGS",
-    "VERIFY_CONFIGS", "SCHEDULE_CONFIGS", "normal_rows", "draft_inputs",
+    "VERIFY_CONFIGS", "SCHEDULE_CONFIGS", "VerifyLogitsConfig", "VERIFY_LOGITS_CONFIGS",
+    "verify_logits_inputs", "normal_rows", "draft_inputs",
     "markov_logits", "verify_inputs", "schedule_inputs", "sps_table",
     "to_bf16_values",
 ]
@@ -44,7 +47,7 @@ _BLOCK_ROWS = 2048
 # tensor tags used in the per-block seeds
 _TAG = {"hidden": 1, "lm_head": 2, "w1": 3, "w2": 4, "anchor": 5,
         "spike_pos": 6, "base": 7, "zipf_perm": 8, "tgt": 9, "noise": 10,
-        "sigma": 11, "draft_tok": 12, "mix": 13, "conf": 14, "temp": 15}
+        "sigma": 11, "draft_tok": 12, "mix": 13, "conf": 14, "temp": 15, "vl_len": 16}
 
 
 @dataclass(frozen=True)
@@ -79,6 +82,25 @@ class VerifyConfig:
 
 
 @dataclass(frozen=True)
+class VerifyLogitsConfig:
+    name: str
+    B: int
+    gamma: int
+    V: int
+    r: int
+    dtype: str                 # storage type of markov_w1 / markov_w2
+    target_std: float
+    draft_sigmas: tuple        # per-request std of the draft's deviation from the target logits
+    draft_temps: tuple         # per-request draft temperature, drawn from this set (0 = greedy draft)
+    target_temp: float
+    data_seed: int
+    spike: bool = True
+    ragged_lengths: bool = False   # lengths drawn uniformly in [0, gamma] instead of all gamma
+    draft_seed: int = 1
+    verify_seed: int = 2
+
+
+@dataclass(frozen=True)
 class ScheduleConfig:
     name: str
     B: int
@@ -106,6 +128,12 @@ VERIFY_CONFIGS = {
     "verify": VerifyConfig("verify", B=256, gamma=8, V=151936, target_std=3.0,
                            draft_sigmas=(0.3, 1.0, 3.0), independent_draft=False,
                            data_seed=4000),
+}
+
+VERIFY_LOGITS_CONFIGS = {
+    "verify": VerifyLogitsConfig("verify", B=256, gamma=8, V=151936, r=256, dtype="bf16", target_std=3.0,
+                                 draft_sigmas=(0.3, 1.0, 3.0), draft_temps=(1.0,), target_temp=1.0,
+                                 data_seed=4000),
 }
 
 SCHEDULE_CONFIGS = {
@@ -185,18 +213,8 @@ def draft_inputs(cfg: DraftConfig, rows: slice | None = None):
         rms = np.sqrt(np.mean(X.astype(np.float64) ** 2, axis=1, keepdims=True))
         X = (X / rms).astype(np.float32)
     W = normal_rows(cfg.V, cfg.H, 1.0 / math.sqrt(cfg.H), s, "lm_head")
-    w1 = normal_rows(cfg.V, cfg.r, 1.0, s, "w1")
-    if cfg.spike:
-        rng = np.random.default_rng((s, _TAG["spike_pos"]))
-        # 8 distinct coordinates per row: argsort of uniform keys, first 8
-        keys = rng.random((cfg.V, cfg.r), dtype=np.float32)
-        pos = np.argpartition(keys, 8, axis=1)[:, :8]
-        np.multiply.at(w1, (np.arange(cfg.V)[:, None], pos), np.float32(4.0))
-    w2 = normal_rows(cfg.V, cfg.r, 1.0 / math.sqrt(cfg.r), s, "w2")
-    anchor = np.random.default_rng((s, _TAG["anchor"])).integers(
-        0, cfg.V, size=cfg.B, dtype=np.int64).astype(np.int32)
-    out = {"anchor": anchor}
-    for name, a in (("hidden", X), ("lm_head", W), ("w1", w1), ("w2", w2)):
+    out = draft_inputs_markov(cfg)
+    for name, a in (("hidden", X), ("lm_head", W)):
         t, f = _store(a, cfg.dtype)
         out[name] = t
         out[name + "_f32"] = f
@@ -280,6 +298,77 @@ def verify_inputs(cfg: VerifyConfig, B: int | None = None):
             v = int(np.searchsorted(cdf, u[b, k] * cdf[-1], side="right"))
             tokens[b, k] = min(v, V - 1)
     return {"p_t": p_t, "p_d": p_d, "draft_tokens": tokens, "sigma": sigma}
+
+
+def verify_logits_inputs(cfg: VerifyLogitsConfig, B: int | None = None, V: int | None = None):
+    """Inputs of verification from logits.
+
+    target_logits [B, gamma+1, V] ~ N(0, target_std^2) (as ``verify_inputs``); the
+    draft's base logits of the drafted positions are the target logits plus
+    N(0, sigma_b^2) noise, sigma_b drawn per request from cfg.draft_sigmas; markov
+    w1 / w2 [V, r] follow ``draft_inputs`` (w1 ~ N(0, 1) with 8 coordinates x4 per
+    row if cfg.spike, w2 ~ N(0, 1/r)); anchors uniform; draft temperatures drawn per
+    request from cfg.draft_temps; lengths all gamma or, with cfg.ragged_lengths,
+    uniform in [0, gamma].  Draft tokens: for T_d > 0 a categorical draw from
+    softmax(base_logits / T_d) (the Markov bias left out: input shaping only), for
+    T_d = 0 the argmax of the base logits, with numpy's Philox generator seeded by
+    cfg.draft_seed.
+    Returns numpy arrays plus torch CPU tensors "w1" / "w2" in storage dtype
+    ("w1_f32" / "w2_f32" hold their exact values).
+    """
+    B = cfg.B if B is None else B
+    V = cfg.V if V is None else V
+    g, s = cfg.gamma, cfg.data_seed
+    tgt = normal_rows(B * (g + 1), V, cfg.target_std, s, "tgt").reshape(B, g + 1, V)
+    sig_rng = np.random.default_rng((s, _TAG["sigma"]))
+    sigma = np.asarray(cfg.draft_sigmas, dtype=np.float32)[sig_rng.integers(0, len(cfg.draft_sigmas), size=B)]
+    base = normal_rows(B * g, V, 1.0, s, "noise").reshape(B, g, V)
+    base *= sigma[:, None, None]
+    base += tgt[:, :g]
+    dc = DraftConfig("verify_logits", B=B, N=g, H=16, V=V, r=cfg.r, dtype=cfg.dtype, temperatures=(1.0,),
+                     data_seed=s, spike=cfg.spike)
+    w = draft_inputs_markov(dc)
+    t_rng = np.random.default_rng((s, _TAG["temp"]))
+    T_d = np.asarray(cfg.draft_temps, dtype=np.float32)[t_rng.integers(0, len(cfg.draft_temps), size=B)]
+    T_t = np.full(B, cfg.target_temp, dtype=np.float32)
+    if cfg.ragged_lengths:
+        lengths = np.random.default_rng((s, _TAG["vl_len"])).integers(0, g + 1, size=B).astype(np.int32)
+    else:
+        lengths = None
+    rng = np.random.Generator(np.random.Philox(key=cfg.draft_seed))
+    u = rng.random((B, g))
+    tokens = np.empty((B, g), dtype=np.int32)
+    for b in range(B):
+        for k in range(g):
+            if T_d[b] == 0:
+                tokens[b, k] = int(np.argmax(base[b, k]))
+                continue
+            p = _softmax_rows_f32(base[b, k] / np.float32(T_d[b]))
+            cdf = np.cumsum(p, dtype=np.float64)
+            tokens[b, k] = min(int(np.searchsorted(cdf, u[b, k] * cdf[-1], side="right")), V - 1)
+    return {"target_logits": tgt, "base_logits": base, "anchor": w["anchor"], "w1": w["w1"], "w2": w["w2"],
+            "w1_f32": w["w1_f32"], "w2_f32": w["w2_f32"], "T_t": T_t, "T_d": T_d, "lengths": lengths,
+            "draft_tokens": tokens, "sigma": sigma}
+
+
+def draft_inputs_markov(cfg: DraftConfig):
+    """markov_w1, markov_w2 and the anchors of ``draft_inputs`` alone (no hidden states or LM head)."""
+    s = cfg.data_seed
+    w1 = normal_rows(cfg.V, cfg.r, 1.0, s, "w1")
+    if cfg.spike:
+        rng = np.random.default_rng((s, _TAG["spike_pos"]))
+        keys = rng.random((cfg.V, cfg.r), dtype=np.float32)
+        pos = np.argpartition(keys, 8, axis=1)[:, :8]
+        np.multiply.at(w1, (np.arange(cfg.V)[:, None], pos), np.float32(4.0))
+    w2 = normal_rows(cfg.V, cfg.r, 1.0 / math.sqrt(cfg.r), s, "w2")
+    anchor = np.random.default_rng((s, _TAG["anchor"])).integers(
+        0, cfg.V, size=cfg.B, dtype=np.int64).astype(np.int32)
+    out = {"anchor": anchor}
+    for name, a in (("w1", w1), ("w2", w2)):
+        t, f = _store(a, cfg.dtype)
+        out[name] = t
+        out[name + "_f32"] = f
+    return out
 
 
 def sps_table(n: int) -> np.ndarray:
