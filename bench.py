@@ -444,10 +444,9 @@ def run_gpu(args):
         torch.cuda.synchronize()
         l_ms.append(e0.elapsed_time(e1))
     vlog_ms = float(np.median(l_ms))
-    # bytes with every request rejected by a sampled draft: the target rows k <= gamma once for
-    # the normalisers, then per request the target row, base-logit row and bias row of k* read,
-    # the bias row written, and markov_w2 read by the bias GEMM
-    vlog_bytes = B * (N + 1) * V * 4 + 4 * B * V * 4 + V * r * w2.element_size()
+    # bytes: the target rows k <= gamma once for the normalisers, the row of k* once more for the
+    # draw (the draft's base logits and Markov rows are read only at the few candidate entries)
+    vlog_bytes = B * (N + 1) * V * 4 + B * V * 4
     del ws_l, ws_m2, t_logits
 
     # ---------------- roofline of the dominant kernel ----------------
@@ -509,7 +508,7 @@ def run_gpu(args):
                           "achieved": vlog_bytes / (vlog_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                           "frac": vlog_bytes / (vlog_ms / 1e3) / 1e9 / hbm_peak,
                           "accepted_mean": float(l_nacc.float().mean().item()),
-                          "note": "median of 20 calls (3 kernels + bias GEMM), L2 flushed, outside the step"},
+                          "note": "median of 20 calls (3 kernels), L2 flushed, outside the step"},
         "verify_greedy": {"ms": greedy_ms, "bound": "hbm", "algorithmic_bytes": B * (N + 1) * V * 4,
                           "achieved": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9, "peak": hbm_peak,
                           "unit": "GB/s", "frac": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9 / hbm_peak,

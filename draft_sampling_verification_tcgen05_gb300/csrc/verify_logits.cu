@@ -8,27 +8,31 @@
 // markov_w2 . markov_w1[prev]) / T_d), which the sampler never writes out; its
 // log-sum-exp is the sampler's lse output.  So nothing of size [B, gamma, V]
 // exists on the draft side: p_d(x_k) is recomputed at one point per tested
-// position, and the full draft row only at the rejected position.
+// position, and at the rejected position only at the entries that can still
+// win the draw.
 //
 // Three launches after the workspace clear:
 //  1. lse kernel (one block per SM, warp items of 2048 entries): per-chunk
 //     (max, sum of 2^((t - max) c)) of the target rows k <= L_b, c = log2(e)/T_t.
-//     The warp completing a request's items decides it: it merges the chunk
-//     partials into log2-normalisers row by row and runs the acceptance tests
-//     fl32(u_k p_d(x_k)) < p_t(x_k) in order (u_k from Philox stream 1, p_d(x_k)
-//     from the base logit, one r-long dot product for the bias and the sampler's
-//     lse), stopping at the first rejection k*.  It writes the decision, the
-//     normalisers of row k* and, for a rejection by a sampled draft, the row
-//     markov_w1[prev_{k*}] for step 2.
-//  2. the tcgen05 GEMM of the draft logits (same kernel) computes the bias rows
-//     markov_w2 . markov_w1[prev_{k*}] of every request, [B, V] fp32.
-//  3. draw kernel (one block per SM, warp items of 2048 entries of row k*):
-//     y_v = ln w_v + g_v with w = max(0, p_t - p_d) (rejection) or p_t (bonus),
-//     g_v the Gumbel variate of Philox stream 4; the chunk's largest key goes to
-//     the request's slot with one atomicMax, and the warp completing a request's
-//     chunks writes its tokens.  ln w_v = a_v ln 2 + log1p(-2^(b_v - a_v)) with
-//     a_v = log2 p_t(v), b_v = log2 p_d(v), so no cancellation is formed in the
-//     linear domain.
+//  2. decide kernel (programmatic dependent of 1; one block per request, one warp
+//     per position): warp k merges row k's chunk partials into its log2
+//     normaliser and, for k < L_b, runs the acceptance test
+//     fl32(u_k p_d(x_k)) < p_t(x_k) (u_k from Philox stream 1, p_d(x_k) from the
+//     base logit, one r-long dot product for the bias and the sampler's lse);
+//     k* = the smallest failing position.  Thread 0 then writes the decision and
+//     what the draw needs about row k*.
+//  3. draw kernel (warp items of 512 entries of row k*, L2-resident shared
+//     lower bound per request): y_v = ln w_v + g_v with w = max(0, p_t - p_d)
+//     (rejection) or p_t (bonus), g_v the Gumbel variate of Philox stream 4.
+//     Since w_v <= p_t(v) and g_v is increasing in its word, ln p_t(v) plus a
+//     table bound of g over the word's top byte bounds y_v; only entries whose
+//     bound reaches the best value seen so far are evaluated exactly, and only
+//     for those is the draft probability formed (the base logit and one r-long
+//     dot product for the bias, computed by the whole warp).  The chunk's
+//     largest key goes to the request's slot with one atomicMax, and the warp
+//     completing a request's chunks writes its tokens.
+//     ln w_v = a_v ln 2 + log1p(-2^(b_v - a_v)) with a_v = log2 p_t(v),
+//     b_v = log2 p_d(v), so no cancellation is formed in the linear domain.
 // A greedy draft (T_d = 0) has the point mass at its token as distribution: its
 // acceptance probability is p_t(x_k) and its residual is p_t without x_{k*}.
 #include "device_common.cuh"
@@ -39,9 +43,13 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;                        // lse kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 2048;                         // entries per warp item: 16 float4 per lane
+constexpr int kChunk = 2048;                         // lse warp item: 16 float4 per lane
+constexpr int kDrawThreads = 256;                    // draw kernel (one thread per table entry)
+constexpr int kDrawWarps = kDrawThreads / 32;
+constexpr int kDrawChunk = 512;                      // draw warp item: 4 float4 per lane
+constexpr int kDecideMaxWarps = 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -50,6 +58,9 @@ struct RowSel {                                      // what the draw of request
     float lse2_t;                                    // log2 of the target normaliser of row k*
     float c_d;                                       // log2(e) / T_d (0 for a greedy draft)
     float lse2_d;                                    // sampler lse of position k*, times log2(e)
+    int prev;                                        // the token before position k*
+    int xk;                                          // draft token at k* (rejections only)
+    int pad[2];
 };
 
 struct VLArgs {
@@ -68,28 +79,22 @@ struct VLArgs {
     WsHeader* ws;
     // workspace
     unsigned long long* keys;                        // [B] draw keys (zeroed)
-    uint32_t* done1;                                 // [B] lse items counted (zeroed)
     uint32_t* done3;                                 // [B] draw chunks counted (zeroed)
+    float* lse2;                                     // [B][g+1] log2 normalisers of the target rows
     int32_t* decision;                               // [B] see dec_kstar / dec_rejected / dec_sampled
     RowSel* sel;                                     // [B]
     float2* part;                                    // [B][g+1][n_chunk] (max t, sum)
-    void* eg;                                        // [B, r] gathered markov_w1 rows (GEMM operand)
-    const float* bias;                               // [B, V] bias rows (GEMM output)
     uint64_t seed;
     uint32_t offset;
-    int B, g, V, r, wbf16, n_chunk, warps1, warps3;
+    int B, g, V, r, wbf16, n_chunk, n_chunk3, warps1, warps3;
     long long total1;                                // B * (g+1) * n_chunk
-    long long total3;                                // B * n_chunk
+    long long total3;                                // B * n_chunk3
 };
 
 // decision encoding: -1 bad request; else (k* << 2) | (rejected << 0) | (sampled draft << 1)
 __device__ __forceinline__ int dec_kstar(int d) { return d >> 2; }
 __device__ __forceinline__ bool dec_rejected(int d) { return (d & 1) != 0; }
 __device__ __forceinline__ bool dec_sampled(int d) { return (d & 2) != 0; }
-
-__device__ __forceinline__ float wval(const void* w, bool bf16, size_t i) {
-    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(w)[i]) : static_cast<const float*>(w)[i];
-}
 
 __device__ __forceinline__ float warp_sum_f(float x) {
 #pragma unroll
@@ -155,97 +160,46 @@ __device__ float row_lse2(const VLArgs& a, int b, int k, float c) {
     return fmaf(M, c, log2f(s));
 }
 
-// Sum over j < r of w2[x, j] * w1[prev, j] (whole warp).
+// Sum over j < r of w2[x, j] * w1[prev, j] (whole warp, one 16-byte piece of each row per lane
+// per step; rows are whole multiples of 16 bytes and 16-byte aligned).  The butterfly leaves
+// the same sum in every lane.
 __device__ float point_bias(const VLArgs& a, int x, int prev) {
-    const bool bf = a.wbf16 != 0;
-    const size_t rx = static_cast<size_t>(x) * a.r, rp = static_cast<size_t>(prev) * a.r;
-    float s = 0.f;
-    for (int j = static_cast<int>(lane_id()); j < a.r; j += 32) s = fmaf(wval(a.w2, bf, rx + j), wval(a.w1, bf, rp + j), s);
-    return warp_sum_f(s);
+    float s0 = 0.f, s1 = 0.f;
+    if (a.wbf16) {
+        const uint4* rx = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w2) + static_cast<size_t>(x) * a.r);
+        const uint4* re = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w1) + static_cast<size_t>(prev) * a.r);
+        for (int p = static_cast<int>(lane_id()); p < a.r / 8; p += 32) {
+            const uint4 qx = __ldg(rx + p), qe = __ldg(re + p);
+            const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&qx);
+            const __nv_bfloat162* he = reinterpret_cast<const __nv_bfloat162*>(&qe);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 fx = __bfloat1622float2(hx[i]), fe = __bfloat1622float2(he[i]);
+                s0 = fmaf(fx.x, fe.x, s0);
+                s1 = fmaf(fx.y, fe.y, s1);
+            }
+        }
+    } else {
+        const float4* rx = reinterpret_cast<const float4*>(static_cast<const float*>(a.w2) + static_cast<size_t>(x) * a.r);
+        const float4* re = reinterpret_cast<const float4*>(static_cast<const float*>(a.w1) + static_cast<size_t>(prev) * a.r);
+        for (int p = static_cast<int>(lane_id()); p < a.r / 4; p += 32) {
+            const float4 fx = __ldg(rx + p), fe = __ldg(re + p);
+            s0 = fmaf(fx.x, fe.x, s0);
+            s1 = fmaf(fx.y, fe.y, s1);
+            s0 = fmaf(fx.z, fe.z, s0);
+            s1 = fmaf(fx.w, fe.w, s1);
+        }
+    }
+    return warp_sum_f(s0 + s1);
 }
 
-// The warp that completed request b's normaliser items decides the request.
-__device__ void decide(const VLArgs& a, int b) {
-    const uint32_t lane = lane_id();
-    const int g = a.g, V = a.V;
-    const int Lb = a.lengths != nullptr ? a.lengths[b] : g;
-    const float Tt = a.T_t[b], Td = a.T_d[b];
-    const int anc = a.anchor[b];
-    bool bad = !(Lb >= 0 && Lb <= g) || !(Tt > 0.f && Tt < INFINITY) || !(Td >= 0.f && Td < INFINITY) ||
-               anc < 0 || anc >= V;
-    const bool sampled = Td > 0.f;
-    const float c_t = kLog2e / Tt;
-    const float c_d = sampled ? kLog2e / Td : 0.f;
-    int kstar = Lb, prev_star = anc;
-    bool rejected = false, numeric = false;
-    float lse2_star = 0.f, lsed2_star = 0.f;
-    int prev = anc;
-    for (int k = 0; !bad && k <= Lb; ++k) {
-        const float lse2 = row_lse2(a, b, k, c_t);
-        if (!(fabsf(lse2) < INFINITY)) {                 // NaN in the row or no finite entry
-            numeric = bad = true;
-            break;
-        }
-        if (k == Lb) {                                  // every tested token accepted: bonus row
-            lse2_star = lse2;
-            break;
-        }
-        const int x = a.tokens[static_cast<size_t>(b) * g + k];
-        if (x < 0 || x >= V) {
-            bad = true;
-            break;
-        }
-        const float pt = exp2f(fmaf(__ldg(a.t + (static_cast<size_t>(b) * (g + 1) + k) * V + x), c_t, -lse2));
-        float pd = 1.f;
-        float lsed2 = 0.f;
-        if (sampled) {
-            const float lse_d = a.lse_d[static_cast<size_t>(b) * g + k];
-            if (!(fabsf(lse_d) < INFINITY)) {
-                numeric = bad = true;
-                break;
-            }
-            lsed2 = lse_d * kLog2e;
-            const float z = __fadd_rn(__ldg(a.L + (static_cast<size_t>(b) * g + k) * V + x), point_bias(a, x, prev));
-            pd = exp2f(fmaf(z, c_d, -lsed2));
-        }
-        const uint4 w = philox_at(a.seed, a.offset, 0u, static_cast<uint32_t>(b), kStreamAccept,
-                                  static_cast<uint32_t>(k));
-        const float u = uniform_from_word(w.x);
-        if (!(__fmul_rn(u, pd) < pt)) {
-            kstar = k;
-            rejected = true;
-            prev_star = prev;
-            lse2_star = lse2;
-            lsed2_star = lsed2;
-            break;
-        }
-        prev = x;
-    }
-    // the GEMM operand row: markov_w1[prev_{k*}] for a rejection by a sampled draft, else zeros
-    const bool gather = !bad && rejected && sampled;
-    const size_t esz = a.wbf16 ? 2 : 4;
-    const size_t row_bytes = esz * static_cast<size_t>(a.r);
-    uint8_t* dst = static_cast<uint8_t*>(a.eg) + row_bytes * static_cast<size_t>(b);
-    if (gather) {                                        // prev_star is a checked token id here
-        const uint8_t* src = static_cast<const uint8_t*>(a.w1) + row_bytes * static_cast<size_t>(prev_star);
-        for (size_t i = 4 * lane; i < row_bytes; i += 128)    // rows are whole multiples of 16 bytes
-            *reinterpret_cast<uint32_t*>(dst + i) = *reinterpret_cast<const uint32_t*>(src + i);
-    } else {
-        for (size_t i = 4 * lane; i < row_bytes; i += 128) *reinterpret_cast<uint32_t*>(dst + i) = 0u;
-    }
-    if (lane == 0) {
-        if (bad) set_status(a.ws, numeric ? DSPARK_STATUS_NUMERIC : DSPARK_STATUS_INPUT_RANGE);
-        RowSel s;
-        s.c_t = c_t;
-        s.lse2_t = lse2_star;
-        s.c_d = c_d;
-        s.lse2_d = lsed2_star;
-        a.sel[b] = s;
-        a.decision[b] = bad ? -1 : ((kstar << 2) | (sampled ? 2 : 0) | (rejected ? 1 : 0));
-    }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1) vl_lse_kernel(VLArgs a) {
+    griddep_launch_dependents();                         // the decide kernel may start launching
     const int gw = static_cast<int>(blockIdx.x) * kWarps + static_cast<int>(warp_id());
     const uint32_t lane = lane_id();
     const long long per_req = static_cast<long long>(a.g + 1) * a.n_chunk;
@@ -255,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1) vl_lse_kernel(VLArgs a) {
     while (f < f1) {
         const int b = static_cast<int>(f / per_req);
         const long long req_end = min(static_cast<long long>(b + 1) * per_req, f1);
-        const uint32_t count = static_cast<uint32_t>(req_end - f);
         const int Lb = a.lengths != nullptr ? a.lengths[b] : a.g;
         const float Tt = a.T_t[b];
         const bool ok = Lb >= 0 && Lb <= a.g && Tt > 0.f && Tt < INFINITY;
@@ -268,15 +221,84 @@ __global__ void __launch_bounds__(kThreads, 1) vl_lse_kernel(VLArgs a) {
             const float2 p = chunk_lse(row, ch * kChunk + 4 * static_cast<int>(lane), a.V, vec, c);
             if (lane == 0) a.part[(static_cast<size_t>(b) * (a.g + 1) + k) * a.n_chunk + ch] = p;
         }
-        uint32_t last = 0;
-        if (lane == 0) {
-            __threadfence();
-            last = atomicAdd(a.done1 + b, count) + count == static_cast<uint32_t>(per_req) ? 1u : 0u;
+    }
+}
+
+enum : int { kBadRange = 1, kBadNumeric = 2 };
+
+// One block per request, one warp per position (positions beyond the block's warps in rounds).
+__global__ void __launch_bounds__(32 * kDecideMaxWarps) vl_decide_kernel(VLArgs a) {
+    __shared__ int s_fail, s_bad;
+    griddep_wait();                                      // every chunk partial is written
+    const int b = static_cast<int>(blockIdx.x);
+    const int w = static_cast<int>(warp_id()), nw = static_cast<int>(blockDim.x >> 5);
+    const uint32_t lane = lane_id();
+    const int g = a.g, V = a.V;
+    const int Lb = a.lengths != nullptr ? a.lengths[b] : g;
+    const float Tt = a.T_t[b], Td = a.T_d[b];
+    const int anc = a.anchor[b];
+    const bool bad0 = !(Lb >= 0 && Lb <= g) || !(Tt > 0.f && Tt < INFINITY) || !(Td >= 0.f && Td < INFINITY) ||
+                      anc < 0 || anc >= V;
+    const bool sampled = Td > 0.f;
+    const float c_t = kLog2e / Tt;
+    const float c_d = sampled ? kLog2e / Td : 0.f;
+    if (threadIdx.x == 0) {
+        s_fail = bad0 ? 0 : Lb;
+        s_bad = bad0 ? kBadRange : 0;
+    }
+    __syncthreads();
+    for (int k0 = 0; !bad0 && k0 <= Lb; k0 += nw) {
+        const int k = k0 + w;
+        if (k > Lb) break;
+        const float lse2 = row_lse2(a, b, k, c_t);
+        if (lane == 0) a.lse2[static_cast<size_t>(b) * (g + 1) + k] = lse2;
+        if (!(fabsf(lse2) < INFINITY)) {                 // NaN in the row or no finite entry
+            if (lane == 0) atomicOr(&s_bad, kBadNumeric);
+            continue;
         }
-        if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-            __threadfence();
-            decide(a, b);
+        if (k == Lb) continue;                           // the bonus row needs no test
+        const int x = a.tokens[static_cast<size_t>(b) * g + k];
+        const int prev = k == 0 ? anc : a.tokens[static_cast<size_t>(b) * g + k - 1];
+        if (x < 0 || x >= V || prev < 0 || prev >= V) {
+            if (lane == 0) atomicOr(&s_bad, kBadRange);
+            continue;
         }
+        const float pt = exp2f(fmaf(__ldg(a.t + (static_cast<size_t>(b) * (g + 1) + k) * V + x), c_t, -lse2));
+        float pd = 1.f;
+        if (sampled) {
+            const float lse_d = a.lse_d[static_cast<size_t>(b) * g + k];
+            if (!(fabsf(lse_d) < INFINITY)) {
+                if (lane == 0) atomicOr(&s_bad, kBadNumeric);
+                continue;
+            }
+            const float z = __fadd_rn(__ldg(a.L + (static_cast<size_t>(b) * g + k) * V + x), point_bias(a, x, prev));
+            pd = exp2f(fmaf(z, c_d, -lse_d * kLog2e));
+        }
+        const uint4 wd = philox_at(a.seed, a.offset, 0u, static_cast<uint32_t>(b), kStreamAccept,
+                                   static_cast<uint32_t>(k));
+        const float u = uniform_from_word(wd.x);
+        if (!(__fmul_rn(u, pd) < pt) && lane == 0) atomicMin(&s_fail, k);
+    }
+    __syncthreads();
+    if (w != 0) return;
+    const bool bad = s_bad != 0;
+    const int kstar = s_fail;
+    const bool rejected = !bad && kstar < Lb;
+    if (lane == 0) {
+        if (bad)
+            set_status(a.ws, ((s_bad & kBadNumeric) ? DSPARK_STATUS_NUMERIC : 0u) |
+                                 ((s_bad & kBadRange) ? DSPARK_STATUS_INPUT_RANGE : 0u));
+        RowSel sl;
+        sl.c_t = c_t;
+        sl.lse2_t = bad ? 0.f : a.lse2[static_cast<size_t>(b) * (g + 1) + kstar];
+        sl.c_d = c_d;
+        sl.lse2_d = rejected && sampled ? a.lse_d[static_cast<size_t>(b) * g + kstar] * kLog2e : 0.f;
+        // every token of the tested block was checked above
+        sl.prev = bad ? 0 : (kstar == 0 ? anc : a.tokens[static_cast<size_t>(b) * g + kstar - 1]);
+        sl.xk = rejected ? a.tokens[static_cast<size_t>(b) * g + kstar] : -1;
+        sl.pad[0] = sl.pad[1] = 0;
+        a.sel[b] = sl;
+        a.decision[b] = bad ? -1 : ((kstar << 2) | (sampled ? 2 : 0) | (rejected ? 1 : 0));
     }
 }
 
@@ -285,78 +307,186 @@ __global__ void __launch_bounds__(kThreads, 1) vl_lse_kernel(VLArgs a) {
 // ---------------------------------------------------------------------------
 
 // Perturbed value ln w_v + g_v of entry v (-inf where w_v = 0), from log2 p_t = a and
-// log2 p_d = bb (bb = -inf: no draft mass to subtract).
+// log2 p_d = bb (bb = -inf: no draft mass to subtract).  Never above
+// __fadd_rn(__fmul_rn(a, ln 2), g): the log1p term is <= 0 and rounding is monotone.
 __device__ __forceinline__ float perturbed(float a, float bb, uint32_t word) {
     float lnw;
-    if (bb == -INFINITY) lnw = a * kLn2;
+    if (bb == -INFINITY) lnw = __fmul_rn(a, kLn2);
     else if (bb >= a) lnw = -INFINITY;
     else lnw = fmaf(a, kLn2, log1pf(-exp2f(bb - a)));
-    return lnw + gumbel_from_word(word);
+    return __fadd_rn(lnw, gumbel_from_word(word));
 }
 
 __device__ __forceinline__ uint32_t word_sel(uint4 w, int j) {
     return j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w;
 }
 
-// Largest key of the chunk starting at lane entry e0 (lane l: e0 + 128 q + 0..3, q < 16).
-__device__ __forceinline__ unsigned long long chunk_draw(const VLArgs& a, int b, int dec, const RowSel& s,
-                                                         int e0, bool vec, bool& nan_seen) {
-    const int V = a.V, g = a.g;
-    const int kstar = dec_kstar(dec);
-    const bool rej = dec_rejected(dec), smp = dec_sampled(dec);
-    const float* rt = a.t + (static_cast<size_t>(b) * (g + 1) + kstar) * V;
-    const float* rl = a.L + (static_cast<size_t>(b) * g + kstar) * V;
-    const float* rb = a.bias + static_cast<size_t>(b) * V;
-    const int xk = rej && !smp ? a.tokens[static_cast<size_t>(b) * g + kstar] : -1;
-    unsigned long long best = 0;
-#pragma unroll 1
-    for (int q0 = 0; q0 < 16; q0 += 4) {
-        float4 tv[4], lv[4], bv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tv[j] = load4(rt, e0 + 128 * (q0 + j), V, vec, -INFINITY);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            lv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            bv[j] = lv[j];
-        }
-        if (rej && smp) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                lv[j] = load4(rl, e0 + 128 * (q0 + j), V, vec, 0.f);
-                bv[j] = load4(rb, e0 + 128 * (q0 + j), V, vec, 0.f);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + 128 * (q0 + j);
-            if (e >= V) continue;
-            const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>(e >> 2), static_cast<uint32_t>(b),
-                                      kStreamResidual, static_cast<uint32_t>(kstar));
-            const float tt[4] = {tv[j].x, tv[j].y, tv[j].z, tv[j].w};
-            const float ll[4] = {lv[j].x, lv[j].y, lv[j].z, lv[j].w};
-            const float bb4[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
+__device__ __forceinline__ float key_value(unsigned long long key) {
+    return key == 0ull ? -INFINITY : float_from_order_bits(static_cast<uint32_t>(key >> 32));
+}
+
+// Sum over j < r of w2[v, j] * w1[prev, j] by one lane (16-byte pieces; rows are whole
+// multiples of 16 bytes and 16-byte aligned).
+__device__ __forceinline__ float lane_bias(const VLArgs& a, int v, int prev) {
+    float s0 = 0.f, s1 = 0.f;
+    if (a.wbf16) {
+        const uint4* x = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w2) + static_cast<size_t>(v) * a.r);
+        const uint4* e = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w1) + static_cast<size_t>(prev) * a.r);
+#pragma unroll 4
+        for (int p = 0; p < a.r / 8; ++p) {
+            const uint4 qx = __ldg(x + p), qe = __ldg(e + p);
+            const __nv_bfloat162* hx = reinterpret_cast<const __nv_bfloat162*>(&qx);
+            const __nv_bfloat162* he = reinterpret_cast<const __nv_bfloat162*>(&qe);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int v = e + i;
-                if (v >= V) break;
-                const float av = fmaf(tt[i], s.c_t, -s.lse2_t);
-                float bb = -INFINITY;
-                if (rej) {
-                    if (smp) bb = fmaf(__fadd_rn(ll[i], bb4[i]), s.c_d, -s.lse2_d);
-                    else bb = v == xk ? 0.f : -INFINITY;
+                const float2 fx = __bfloat1622float2(hx[i]), fe = __bfloat1622float2(he[i]);
+                s0 = fmaf(fx.x, fe.x, s0);
+                s1 = fmaf(fx.y, fe.y, s1);
+            }
+        }
+    } else {
+        const float4* x = reinterpret_cast<const float4*>(static_cast<const float*>(a.w2) + static_cast<size_t>(v) * a.r);
+        const float4* e = reinterpret_cast<const float4*>(static_cast<const float*>(a.w1) + static_cast<size_t>(prev) * a.r);
+#pragma unroll 4
+        for (int p = 0; p < a.r / 4; ++p) {
+            const float4 fx = __ldg(x + p), fe = __ldg(e + p);
+            s0 = fmaf(fx.x, fe.x, s0);
+            s1 = fmaf(fx.y, fe.y, s1);
+            s0 = fmaf(fx.z, fe.z, s0);
+            s1 = fmaf(fx.w, fe.w, s1);
+        }
+    }
+    return s0 + s1;
+}
+
+// The draft's log2 probability at entry v of row k* (one lane).
+__device__ __forceinline__ float draft_log2p(const VLArgs& a, int b, int dec, const RowSel& s, int v) {
+    if (!dec_rejected(dec)) return -INFINITY;
+    if (!dec_sampled(dec)) return v == s.xk ? 0.f : -INFINITY;
+    const int kstar = dec_kstar(dec);
+    const float l = __ldg(a.L + (static_cast<size_t>(b) * a.g + kstar) * a.V + v);
+    return fmaf(__fadd_rn(l, lane_bias(a, v, s.prev)), s.c_d, -s.lse2_d);
+}
+
+// The draft's log2 probability at entry v of row k* (whole warp; v uniform).
+__device__ __forceinline__ float draft_log2p_warp(const VLArgs& a, int b, int dec, const RowSel& s, int v) {
+    if (!dec_rejected(dec)) return -INFINITY;
+    if (!dec_sampled(dec)) return v == s.xk ? 0.f : -INFINITY;
+    const int kstar = dec_kstar(dec);
+    const float l = __ldg(a.L + (static_cast<size_t>(b) * a.g + kstar) * a.V + v);
+    return fmaf(__fadd_rn(l, point_bias(a, v, s.prev)), s.c_d, -s.lse2_d);
+}
+
+// Bound of the Gumbel variate of `word`: by its top byte, and for top byte 255 (where the
+// variate ranges up to its maximum) by its second byte.
+__device__ __forceinline__ float gumbel_bound(const float* gtab, uint32_t word) {
+    const uint32_t hi = word >> 24;
+    return hi != 255u ? gtab[hi] : gtab[256 + ((word >> 16) & 255u)];
+}
+
+__device__ __forceinline__ float comp(const float4& f, int i) { return i == 0 ? f.x : i == 1 ? f.y : i == 2 ? f.z : f.w; }
+
+// Entry q (= 4 j + i) of a lane's 16 loaded target logits, q not a compile-time constant.
+__device__ __forceinline__ float entry_of(const float4 (&tv)[4], int q) {
+    float x = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        if (k == q) x = comp(tv[k >> 2], k & 3);
+    return x;
+}
+
+__device__ __forceinline__ uint32_t residual_word(const VLArgs& a, int b, int kstar, int v) {
+    return word_sel(philox_at(a.seed, a.offset, static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(b),
+                              kStreamResidual, static_cast<uint32_t>(kstar)),
+                    v & 3);
+}
+
+// One 512-entry chunk of row k* whose target logits tv the lane holds (lane l: entries
+// e0 + 128 j + 0..3, j < 4).  best / LB are warp-uniform: the largest key found so far and its
+// value, which every exact value must reach to matter.
+__device__ __forceinline__ void chunk_draw(const VLArgs& a, int b, int dec, const RowSel& s, int e0,
+                                           const float4 (&tv)[4], const float* gtab, unsigned long long& best,
+                                           float& LB, bool& nan_seen) {
+    const int V = a.V;
+    const int kstar = dec_kstar(dec);
+    float bnd[16];
+    uint32_t cand = 0;                                   // bit 4 j + i: entry e0 + 128 j + i may win
+    int pick = -1;                                       // the lane's candidate of largest bound
+    float pb = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float av[4];
+        float hi = -INFINITY;
+        bool odd = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            av[i] = fmaf(comp(tv[j], i), s.c_t, -s.lse2_t);
+            hi = fmaxf(hi, av[i]);
+            odd |= av[i] != av[i];
+            bnd[4 * j + i] = -INFINITY;
+        }
+        const int e = e0 + 128 * j;
+        // no word can lift this group to LB: skip its Philox call (NaN entries are kept)
+        if (e >= V || (!odd && __fadd_rn(__fmul_rn(hi, kLn2), kGumbelMax) < LB)) continue;
+        const uint4 w = philox_at(a.seed, a.offset, static_cast<uint32_t>(e >> 2), static_cast<uint32_t>(b),
+                                  kStreamResidual, static_cast<uint32_t>(kstar));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float bound = __fadd_rn(__fmul_rn(av[i], kLn2), gumbel_bound(gtab, word_sel(w, i)));
+            bnd[4 * j + i] = bound;
+            if (e + i < V && !(bound < LB)) {
+                cand |= 1u << (4 * j + i);
+                if (pick < 0 || bound > pb) {
+                    pick = 4 * j + i;
+                    pb = bound;
                 }
-                const float y = perturbed(av, bb, word_sel(w, i));
-                if (y != y) {
-                    nan_seen = true;
-                    continue;
-                }
-                if (y == -INFINITY) continue;
-                const unsigned long long key = argmax_key(y, static_cast<uint32_t>(v));
-                best = key > best ? key : best;
             }
         }
     }
-    return best;
+    if (LB == -INFINITY) {
+        // nothing known yet: every lane evaluates its candidate of largest bound, at once
+        unsigned long long mine = 0;
+        if (pick >= 0) {
+            cand &= ~(1u << pick);
+            const int v = e0 + 128 * (pick >> 2) + (pick & 3);
+            const float y = perturbed(fmaf(entry_of(tv, pick), s.c_t, -s.lse2_t), draft_log2p(a, b, dec, s, v),
+                                      residual_word(a, b, kstar, v));
+            if (y != y) nan_seen = true;
+            else if (y > -INFINITY) mine = argmax_key(y, static_cast<uint32_t>(v));
+        }
+        mine = warp_max_u64(mine);
+        if (mine > best) {
+            best = mine;
+            LB = key_value(best);
+        }
+    }
+    // drop what LB now excludes, then the rest one at a time across the warp
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        if (bnd[q] < LB) cand &= ~(1u << q);
+    uint32_t m = __ballot_sync(0xFFFFFFFFu, cand != 0u);
+    while (m != 0u) {
+        const int src = __ffs(m) - 1;
+        const int bit = __ffs(__shfl_sync(0xFFFFFFFFu, cand, src)) - 1;
+        const float tc = __shfl_sync(0xFFFFFFFFu, entry_of(tv, bit), src);
+        const int v = e0 - 4 * static_cast<int>(lane_id()) + 4 * src + 128 * (bit >> 2) + (bit & 3);
+        const float y = perturbed(fmaf(tc, s.c_t, -s.lse2_t), draft_log2p_warp(a, b, dec, s, v),
+                                  residual_word(a, b, kstar, v));
+        if (static_cast<int>(lane_id()) == src) cand &= cand - 1u;
+        if (y != y) {
+            nan_seen = true;
+        } else if (y > -INFINITY) {
+            const unsigned long long key = argmax_key(y, static_cast<uint32_t>(v));
+            if (key > best) {
+                best = key;
+                LB = y;
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    if (bnd[q] < LB) cand &= ~(1u << q);
+            }
+        }
+        m = __ballot_sync(0xFFFFFFFFu, cand != 0u);
+    }
 }
 
 // Fallback of a residual without positive mass (float32 rounding only): the bonus form over row
@@ -404,35 +534,61 @@ __device__ void finish(const VLArgs& a, int b, int dec) {
     if (lane == 0) a.n_acc[b] = kstar;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) vl_draw_kernel(VLArgs a) {
-    const int gw = static_cast<int>(blockIdx.x) * kWarps + static_cast<int>(warp_id());
+__global__ void __launch_bounds__(kDrawThreads, 2) vl_draw_kernel(VLArgs a) {
+    __shared__ float gtab[512];
+    {
+        // bound of the Gumbel variate over the words with top byte k (entry k) and over those with
+        // top bytes 255, k (entry 256 + k): the value at the largest such word, plus a margin for
+        // the rounding of the two logarithms (the variate increases with the word)
+        const uint32_t k = threadIdx.x;                  // blockDim.x == 256
+        gtab[k] = __fadd_rn(gumbel_from_word(((k + 1u) << 24) - 1u), 1e-3f);
+        gtab[256 + k] = __fadd_rn(gumbel_from_word(((0xFF00u + k + 1u) << 16) - 1u), 1e-3f);
+    }
+    __syncthreads();
+    const int gw = static_cast<int>(blockIdx.x) * kDrawWarps + static_cast<int>(warp_id());
     const uint32_t lane = lane_id();
     const bool vec = (a.V & 3) == 0;
     long long f = a.total3 * gw / a.warps3;
     const long long f1 = a.total3 * (gw + 1) / a.warps3;
     bool nan_seen = false;
     while (f < f1) {
-        const int b = static_cast<int>(f / a.n_chunk);
-        const long long req_end = min(static_cast<long long>(b + 1) * a.n_chunk, f1);
+        const int b = static_cast<int>(f / a.n_chunk3);
+        const long long req_end = min(static_cast<long long>(b + 1) * a.n_chunk3, f1);
         const uint32_t count = static_cast<uint32_t>(req_end - f);
         const int dec = a.decision[b];
         if (dec >= 0) {
             const RowSel s = a.sel[b];
-            unsigned long long best = 0;
+            const float* rt = a.t + (static_cast<size_t>(b) * (a.g + 1) + dec_kstar(dec)) * a.V;
+            unsigned long long best = 0, published = 0;
+            float4 cur[4], nxt[4];
+            int e0 = static_cast<int>(f - static_cast<long long>(b) * a.n_chunk3) * kDrawChunk + 4 * static_cast<int>(lane);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cur[j] = load4(rt, e0 + 128 * j, a.V, vec, -INFINITY);
             for (; f < req_end; ++f) {
-                const int ch = static_cast<int>(f - static_cast<long long>(b) * a.n_chunk);
-                const unsigned long long k =
-                    chunk_draw(a, b, dec, s, ch * kChunk + 4 * static_cast<int>(lane), vec, nan_seen);
-                best = k > best ? k : best;
+                // the next chunk's loads are in flight while this one is processed
+                const bool more = f + 1 < req_end;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    nxt[j] = more ? load4(rt, e0 + kDrawChunk + 128 * j, a.V, vec, -INFINITY) : cur[j];
+                // the request's best so far (any warp's) bounds what can still win
+                const unsigned long long shared_best = __ldcg(a.keys + b);
+                if (shared_best > best) best = shared_best;
+                float LB = key_value(best);
+                chunk_draw(a, b, dec, s, e0, cur, gtab, best, LB, nan_seen);
+                if (best > published && best > shared_best) {
+                    if (lane == 0) atomicMax(a.keys + b, best);
+                    published = best;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cur[j] = nxt[j];
+                e0 += kDrawChunk;
             }
-            best = warp_max_u64(best);
-            if (lane == 0 && best != 0ull) atomicMax(a.keys + b, best);
         }
         f = req_end;
         uint32_t last = 0;
         if (lane == 0) {
             __threadfence();
-            last = atomicAdd(a.done3 + b, count) + count == static_cast<uint32_t>(a.n_chunk) ? 1u : 0u;
+            last = atomicAdd(a.done3 + b, count) + count == static_cast<uint32_t>(a.n_chunk3) ? 1u : 0u;
         }
         if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
             __threadfence();
@@ -445,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) vl_draw_kernel(VLArgs a) {
 size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct VLLayout {
-    size_t keys, done1, done3, clear_end, decision, sel, part, eg, bias, total;
+    size_t keys, done3, clear_end, decision, sel, lse2, part, total;
 };
 
 VLLayout vl_layout(int B, int gamma, int V, int r) {
@@ -454,8 +610,6 @@ VLLayout vl_layout(int B, int gamma, int V, int r) {
     size_t p = sizeof(WsHeader);
     l.keys = p;
     p = al(p + sizeof(unsigned long long) * B);
-    l.done1 = p;
-    p = al(p + sizeof(uint32_t) * B);
     l.done3 = p;
     p = al(p + sizeof(uint32_t) * B);
     l.clear_end = p;
@@ -463,12 +617,10 @@ VLLayout vl_layout(int B, int gamma, int V, int r) {
     p = al(p + sizeof(int32_t) * B);
     l.sel = p;
     p = al(p + sizeof(RowSel) * B);
+    l.lse2 = p;
+    p = al(p + sizeof(float) * static_cast<size_t>(B) * (gamma + 1));
     l.part = p;
     p = al(p + sizeof(float2) * static_cast<size_t>(B) * (gamma + 1) * n_chunk);
-    l.eg = p;
-    p = al(p + sizeof(float) * static_cast<size_t>(B) * r);          // sized for fp32 weights
-    l.bias = p;
-    p = al(p + sizeof(float) * static_cast<size_t>(B) * V);
     l.total = p;
     return l;
 }
@@ -505,14 +657,11 @@ dspark_status launch_verify_logits(const float* target_logits, const float* T_t,
     a.n_acc = num_accepted;
     a.ws = static_cast<WsHeader*>(ws);
     a.keys = reinterpret_cast<unsigned long long*>(base + l.keys);
-    a.done1 = reinterpret_cast<uint32_t*>(base + l.done1);
     a.done3 = reinterpret_cast<uint32_t*>(base + l.done3);
     a.decision = reinterpret_cast<int32_t*>(base + l.decision);
     a.sel = reinterpret_cast<RowSel*>(base + l.sel);
+    a.lse2 = reinterpret_cast<float*>(base + l.lse2);
     a.part = reinterpret_cast<float2*>(base + l.part);
-    a.eg = base + l.eg;
-    float* bias = reinterpret_cast<float*>(base + l.bias);
-    a.bias = bias;
     a.seed = seed;
     a.offset = offset;
     a.B = B;
@@ -521,23 +670,36 @@ dspark_status launch_verify_logits(const float* target_logits, const float* T_t,
     a.r = r;
     a.wbf16 = wdtype == DSPARK_BF16 ? 1 : 0;
     a.n_chunk = (V + kChunk - 1) / kChunk;
+    a.n_chunk3 = (V + kDrawChunk - 1) / kDrawChunk;
     a.total1 = static_cast<long long>(B) * (gamma + 1) * a.n_chunk;
-    a.total3 = static_cast<long long>(B) * a.n_chunk;
-    auto blocks_for = [&](long long items) {
-        const long long want = (items + 3) / 4;                      // at least 4 chunks a warp
-        return static_cast<int>(std::max(1LL, std::min(static_cast<long long>(dev.sm_count),
-                                                        (want + kWarps - 1) / kWarps)));
-    };
-    const int blocks1 = blocks_for(a.total1), blocks3 = blocks_for(a.total3);
+    a.total3 = static_cast<long long>(B) * a.n_chunk3;
+    // lse: one 512-thread block per SM at most, each warp at least one 2048-entry chunk;
+    // draw: up to two 256-thread blocks per SM, each warp at least one 512-entry chunk
+    const int blocks1 = static_cast<int>(std::max(1LL, std::min(static_cast<long long>(dev.sm_count),
+                                                                 (a.total1 + kWarps - 1) / kWarps)));
+    const int blocks3 = static_cast<int>(std::max(1LL, std::min(2LL * dev.sm_count,
+                                                                 (a.total3 + kDrawWarps - 1) / kDrawWarps)));
     a.warps1 = blocks1 * kWarps;
-    a.warps3 = blocks3 * kWarps;
+    a.warps3 = blocks3 * kDrawWarps;
 
     vl_lse_kernel<<<blocks1, kThreads, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "launch(verify_logits lse)");
-    st = launch_draft_logits(a.eg, w2, wdtype, B, r, V, bias, ws, stream, dev);
-    if (st != DSPARK_OK) return st;
-    vl_draw_kernel<<<blocks3, kThreads, 0, stream>>>(a);
+    // programmatic dependent launch: the decide blocks become resident while the lse kernel runs
+    // and wait (griddepcontrol.wait) for its partials
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B));
+    cfg.blockDim = dim3(32u * static_cast<unsigned>(std::min(gamma + 1, kDecideMaxWarps)));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, vl_decide_kernel, a);
+    if (e != cudaSuccess) return cuda_error(e, "launch(verify_logits decide)");
+    vl_draw_kernel<<<blocks3, kDrawThreads, 0, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "launch(verify_logits draw)");
     return DSPARK_OK;

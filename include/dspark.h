@@ -88,8 +88,8 @@ typedef enum {
  *   DSPARK_OP_SCHEDULE      grows with B*N (radix-sort key buffers)
  *   DSPARK_OP_VERIFY_GREEDY grows with B*(N+1) (row argmax keys); N = gamma
  *   DSPARK_OP_CONFIDENCE    256 (the status word)
- *   DSPARK_OP_VERIFY_LOGITS grows with B*V (one bias row per request) and
- *                           B*(N+1)*V/2048 (normaliser partials); N = gamma
+ *   DSPARK_OP_VERIFY_LOGITS grows with B*(N+1)*V/2048 (normaliser partials);
+ *                           N = gamma
  * Returns 0 for an unknown op or negative sizes.
  */
 DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);
@@ -261,9 +261,10 @@ DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t
  * No [B, gamma, V] draft probabilities are read or written: p_d(x_k) is
  * recomputed at the drafted token from the base logit, one r-long dot product
  * and the sampler's log-sum-exp (draft_lse = dspark_markov_sample's lse
- * output), and the whole draft row only at the rejected position, its bias
- * rows coming from one tcgen05 GEMM.  The target normalisers are computed here
- * (rows k <= L_b only).
+ * output), and at the rejected position only at the entries whose perturbed
+ * value can still win the draw (the draw is bounded through p_t, which the
+ * residual never exceeds).  The target normalisers are computed here (rows
+ * k <= L_b only).
  * Acceptance: fl32(u_k * p_d(x_k)) < p_t(x_k), u_k the stream-1 uniform as in
  * dspark_verify.  The correction (residual max(0, p_t - p_d) at the first
  * rejection) or bonus (p_t of row L_b) token is drawn by Gumbel-max,
@@ -280,8 +281,6 @@ DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t
  *                 drafted positions (dspark_draft_logits' output)
  *   anchor        [B] int32, device: the token before the block
  *   w1, w2        [V, r] wdtype (bf16 or fp32), device: markov_w1, markov_w2
- *                 (fp32 weights: the bias rows of the rejected positions are
- *                 computed with tf32 tensor-core products)
  *   draft_temperature [B] fp32, device, >= 0
  *   draft_lse     [B, gamma] fp32, device: the sampler's lse of each drafted
  *                 position (ignored where T_d = 0)
@@ -296,7 +295,8 @@ DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t
  * Device-side: a token, anchor or length out of range or a temperature out of
  * its range sets INPUT_RANGE, a non-finite normaliser or draft_lse sets
  * NUMERIC; such a request outputs num_accepted 0 and -1 tokens.
- * Launches three kernels on `stream` (captured by CUDA stream capture).
+ * Launches three kernels on `stream`, the second as a programmatic dependent
+ * launch of the first (all captured by CUDA stream capture).
  * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY_LOGITS, B, gamma, V, r).
  */
 DSPARK_API dspark_status dspark_verify_logits(const float* target_logits, const float* target_temperature,
