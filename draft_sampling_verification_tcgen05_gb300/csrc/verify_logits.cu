@@ -11,17 +11,19 @@
 // position, and at the rejected position only at the entries that can still
 // win the draw.
 //
-// Three launches after the workspace clear:
-//  1. lse kernel (one block per SM, warp items of 2048 entries): per-chunk
-//     (max, sum of 2^((t - max) c)) of the target rows k <= L_b, c = log2(e)/T_t.
-//  2. decide kernel (programmatic dependent of 1; one block per request, one warp
-//     per position): warp k merges row k's chunk partials into its log2
-//     normaliser and, for k < L_b, runs the acceptance test
-//     fl32(u_k p_d(x_k)) < p_t(x_k) (u_k from Philox stream 1, p_d(x_k) from the
-//     base logit, one r-long dot product for the bias and the sampler's lse);
-//     k* = the smallest failing position.  Thread 0 then writes the decision and
-//     what the draw needs about row k*.
-//  3. draw kernel (warp items of 512 entries of row k*, L2-resident shared
+// Two launches after the workspace clear:
+//  1. rounds kernel (persistent, cooperative, one block per SM): round j streams
+//     target row j of every request still undecided, as warp items of 2048
+//     entries giving (max, sum of 2^((t - max) c)), c = log2(e)/T_t; the warp
+//     completing a request's row merges the partials into the row's log2
+//     normaliser and runs the acceptance test fl32(u_j p_d(x_j)) < p_t(x_j)
+//     (u_j from Philox stream 1, p_d(x_j) from the base logit, one r-long dot
+//     product for the bias and the sampler's lse).  A rejection fixes k* = j, an
+//     acceptance of position L_b - 1 fixes k* = L_b (bonus), otherwise the
+//     request joins the next round; a grid barrier separates the rounds.  Only
+//     the rows k <= k* are read (a bonus row needs no normaliser: the draw is
+//     invariant to a constant shift).
+//  2. draw kernel (warp items of 512 entries of row k*, L2-resident shared
 //     lower bound per request): y_v = ln w_v + g_v with w = max(0, p_t - p_d)
 //     (rejection) or p_t (bonus), g_v the Gumbel variate of Philox stream 4.
 //     Since w_v <= p_t(v) and g_v is increasing in its word, ln p_t(v) plus a
@@ -43,13 +45,12 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 512;                        // lse kernel
+constexpr int kThreads = 512;                        // rounds kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 2048;                         // lse warp item: 16 float4 per lane
+constexpr int kChunk = 2048;                         // rounds warp item: 16 float4 per lane
 constexpr int kDrawThreads = 256;                    // draw kernel (one thread per table entry)
 constexpr int kDrawWarps = kDrawThreads / 32;
 constexpr int kDrawChunk = 512;                      // draw warp item: 4 float4 per lane
-constexpr int kDecideMaxWarps = 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -80,14 +81,21 @@ struct VLArgs {
     // workspace
     unsigned long long* keys;                        // [B] draw keys (zeroed)
     uint32_t* done3;                                 // [B] draw chunks counted (zeroed)
-    float* lse2;                                     // [B][g+1] log2 normalisers of the target rows
-    int32_t* decision;                               // [B] see dec_kstar / dec_rejected / dec_sampled
+    uint32_t* done;                                  // [B] chunk items counted over all rounds (zeroed)
+    uint32_t* rowcnt;                                // [B][g] chunks counted per row (zeroed)
+    uint32_t* rejm;                                  // [B] window positions rejected (zeroed)
+    uint32_t* badm;                                  // [B] window positions with non-finite inputs (zeroed)
+    uint32_t* count;                                 // [rounds + 1] requests entering each round (zeroed)
+    int32_t* list;                                   // [2][B] requests of the current / next round
+    float* lse2w;                                    // [B][R] log2 normalisers of the window's rows
+    int32_t* decision;                               // [B] 2 + decision (see write_decision; zeroed)
     RowSel* sel;                                     // [B]
-    float2* part;                                    // [B][g+1][n_chunk] (max t, sum)
+    float2* part;                                    // [B][R][n_chunk] (max t, sum) of the window's rows
     uint64_t seed;
     uint32_t offset;
+    long long timeout_ns;
     int B, g, V, r, wbf16, n_chunk, n_chunk3, warps1, warps3;
-    long long total1;                                // B * (g+1) * n_chunk
+    int R;                                           // rows per round (window), <= 32
     long long total3;                                // B * n_chunk3
 };
 
@@ -144,9 +152,9 @@ __device__ __forceinline__ float2 chunk_lse(const float* row, int e0, int V, boo
     return make_float2(M, warp_sum_f(s));
 }
 
-// log2 of the normaliser of target row k of request b from its chunk partials (whole warp).
-__device__ float row_lse2(const VLArgs& a, int b, int k, float c) {
-    const float2* p = a.part + (static_cast<size_t>(b) * (a.g + 1) + k) * a.n_chunk;
+// log2 of the normaliser of window row `slot` of request b from its chunk partials (whole warp).
+__device__ float row_lse2(const VLArgs& a, int b, int slot, float c) {
+    const float2* p = a.part + (static_cast<size_t>(b) * a.R + slot) * a.n_chunk;
     float m = -INFINITY;
     for (int i = static_cast<int>(lane_id()); i < a.n_chunk; i += 32) m = fmaxf(m, __ldcg(&p[i].x));
     const float M = warp_max_f(m);
@@ -193,112 +201,199 @@ __device__ float point_bias(const VLArgs& a, int x, int prev) {
     return warp_sum_f(s0 + s1);
 }
 
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__global__ void __launch_bounds__(kThreads, 1) vl_lse_kernel(VLArgs a) {
-    griddep_launch_dependents();                         // the decide kernel may start launching
-    const int gw = static_cast<int>(blockIdx.x) * kWarps + static_cast<int>(warp_id());
-    const uint32_t lane = lane_id();
-    const long long per_req = static_cast<long long>(a.g + 1) * a.n_chunk;
-    const bool vec = (a.V & 3) == 0;
-    long long f = a.total1 * gw / a.warps1;
-    const long long f1 = a.total1 * (gw + 1) / a.warps1;
-    while (f < f1) {
-        const int b = static_cast<int>(f / per_req);
-        const long long req_end = min(static_cast<long long>(b + 1) * per_req, f1);
-        const int Lb = a.lengths != nullptr ? a.lengths[b] : a.g;
-        const float Tt = a.T_t[b];
-        const bool ok = Lb >= 0 && Lb <= a.g && Tt > 0.f && Tt < INFINITY;
-        const float c = kLog2e / Tt;
-        for (; f < req_end; ++f) {
-            const long long rem = f - static_cast<long long>(b) * per_req;
-            const int k = static_cast<int>(rem / a.n_chunk), ch = static_cast<int>(rem % a.n_chunk);
-            if (!ok || k > Lb) continue;                     // rows past L_b are not needed
-            const float* row = a.t + (static_cast<size_t>(b) * (a.g + 1) + k) * a.V;
-            const float2 p = chunk_lse(row, ch * kChunk + 4 * static_cast<int>(lane), a.V, vec, c);
-            if (lane == 0) a.part[(static_cast<size_t>(b) * (a.g + 1) + k) * a.n_chunk + ch] = p;
-        }
-    }
-}
-
 enum : int { kBadRange = 1, kBadNumeric = 2 };
 
-// One block per request, one warp per position (positions beyond the block's warps in rounds).
-__global__ void __launch_bounds__(32 * kDecideMaxWarps) vl_decide_kernel(VLArgs a) {
-    __shared__ int s_fail, s_bad;
-    griddep_wait();                                      // every chunk partial is written
-    const int b = static_cast<int>(blockIdx.x);
-    const int w = static_cast<int>(warp_id()), nw = static_cast<int>(blockDim.x >> 5);
-    const uint32_t lane = lane_id();
-    const int g = a.g, V = a.V;
-    const int Lb = a.lengths != nullptr ? a.lengths[b] : g;
+// Decisions are stored plus 2, so that the cleared value 0 reads as "never decided" (only after
+// a grid barrier gave up).
+__device__ void write_decision(const VLArgs& a, int b, int dec, const RowSel& sl) {
+    if (lane_id() == 0) {
+        a.sel[b] = sl;
+        a.decision[b] = dec + 2;
+    }
+}
+
+__device__ __forceinline__ int read_decision(const VLArgs& a, int b) {
+    const int d = a.decision[b] - 2;
+    if (d == -2) {                                       // undecided: treated as a bad request
+        set_status(a.ws, DSPARK_STATUS_INTERNAL);
+        return -1;
+    }
+    return d;
+}
+
+__device__ void write_bad(const VLArgs& a, int b, int bad) {
+    if (lane_id() == 0) {
+        set_status(a.ws, ((bad & kBadNumeric) ? DSPARK_STATUS_NUMERIC : 0u) |
+                             ((bad & kBadRange) ? DSPARK_STATUS_INPUT_RANGE : 0u));
+        a.decision[b] = -1 + 2;
+    }
+}
+
+// Lengths, temperatures and anchor of request b usable (its rows can be streamed).
+__device__ __forceinline__ bool request_ok(const VLArgs& a, int b) {
+    const int Lb = a.lengths != nullptr ? a.lengths[b] : a.g;
     const float Tt = a.T_t[b], Td = a.T_d[b];
     const int anc = a.anchor[b];
-    const bool bad0 = !(Lb >= 0 && Lb <= g) || !(Tt > 0.f && Tt < INFINITY) || !(Td >= 0.f && Td < INFINITY) ||
-                      anc < 0 || anc >= V;
+    return Lb >= 0 && Lb <= a.g && Tt > 0.f && Tt < INFINITY && Td >= 0.f && Td < INFINITY && anc >= 0 &&
+           anc < a.V;
+}
+
+// The warp that completed row k (window slot k - k0) of request b: its normaliser and the
+// acceptance test of position k (whole warp).  The previous token is known, so every row of a
+// window is tested independently; the first rejection is chosen once the window is complete.
+__device__ void decide_row(const VLArgs& a, int b, int k, int k0) {
+    const int g = a.g, V = a.V;
+    const float Td = a.T_d[b];
     const bool sampled = Td > 0.f;
-    const float c_t = kLog2e / Tt;
-    const float c_d = sampled ? kLog2e / Td : 0.f;
-    if (threadIdx.x == 0) {
-        s_fail = bad0 ? 0 : Lb;
-        s_bad = bad0 ? kBadRange : 0;
+    const float c_t = kLog2e / a.T_t[b];
+    const float lse2 = row_lse2(a, b, k - k0, c_t);
+    const uint32_t bit = 1u << (k - k0);
+    if (lane_id() == 0) a.lse2w[static_cast<size_t>(b) * a.R + (k - k0)] = lse2;
+    if (!(fabsf(lse2) < INFINITY)) {                     // NaN in the row or no finite entry
+        if (lane_id() == 0) atomicOr(a.badm + b, bit);
+        return;
     }
-    __syncthreads();
-    for (int k0 = 0; !bad0 && k0 <= Lb; k0 += nw) {
-        const int k = k0 + w;
-        if (k > Lb) break;
-        const float lse2 = row_lse2(a, b, k, c_t);
-        if (lane == 0) a.lse2[static_cast<size_t>(b) * (g + 1) + k] = lse2;
-        if (!(fabsf(lse2) < INFINITY)) {                 // NaN in the row or no finite entry
-            if (lane == 0) atomicOr(&s_bad, kBadNumeric);
-            continue;
+    const int x = a.tokens[static_cast<size_t>(b) * g + k];
+    const int prev = k == 0 ? a.anchor[b] : a.tokens[static_cast<size_t>(b) * g + k - 1];
+    if (x < 0 || x >= V || prev < 0 || prev >= V) {     // the request is voided when its window ends
+        if (lane_id() == 0) atomicOr(a.badm + b, bit);
+        return;
+    }
+    const float pt = exp2f(fmaf(__ldg(a.t + (static_cast<size_t>(b) * (g + 1) + k) * V + x), c_t, -lse2));
+    float pd = 1.f;
+    if (sampled) {
+        const float lse_d = a.lse_d[static_cast<size_t>(b) * g + k];
+        if (!(fabsf(lse_d) < INFINITY)) {
+            if (lane_id() == 0) atomicOr(a.badm + b, bit);
+            return;
         }
-        if (k == Lb) continue;                           // the bonus row needs no test
-        const int x = a.tokens[static_cast<size_t>(b) * g + k];
-        const int prev = k == 0 ? anc : a.tokens[static_cast<size_t>(b) * g + k - 1];
-        if (x < 0 || x >= V || prev < 0 || prev >= V) {
-            if (lane == 0) atomicOr(&s_bad, kBadRange);
-            continue;
+        const float z = __fadd_rn(__ldg(a.L + (static_cast<size_t>(b) * g + k) * V + x), point_bias(a, x, prev));
+        pd = exp2f(fmaf(z, kLog2e / Td, -lse_d * kLog2e));
+    }
+    const uint4 wd = philox_at(a.seed, a.offset, 0u, static_cast<uint32_t>(b), kStreamAccept,
+                               static_cast<uint32_t>(k));
+    const float u = uniform_from_word(wd.x);
+    if (!(__fmul_rn(u, pd) < pt) && lane_id() == 0) atomicOr(a.rejm + b, bit);
+}
+
+// The warp that completed request b's window [k0, k0 + R) decides what comes next (whole warp).
+__device__ void decide_request(const VLArgs& a, int b, int j, int next_slot_base) {
+    const uint32_t lane = lane_id();
+    const int g = a.g;
+    const int Lb = a.lengths != nullptr ? a.lengths[b] : g;
+    const float Td = a.T_d[b];
+    const int anc = a.anchor[b];
+    const bool sampled = Td > 0.f;
+    const int k0 = j * a.R;
+    RowSel sl;
+    sl.c_t = kLog2e / a.T_t[b];
+    sl.c_d = sampled ? kLog2e / Td : 0.f;
+    sl.lse2_t = 0.f;
+    sl.lse2_d = 0.f;
+    sl.prev = anc;
+    sl.xk = -1;
+    sl.pad[0] = sl.pad[1] = 0;
+    if (j == 0) {
+        // the first round checks the whole request: lengths, temperatures, anchor, every token
+        bool bad = !request_ok(a, b);
+        for (int k = static_cast<int>(lane); !bad && k < Lb; k += 32) {
+            const int x = a.tokens[static_cast<size_t>(b) * g + k];
+            bad = x < 0 || x >= a.V;
         }
-        const float pt = exp2f(fmaf(__ldg(a.t + (static_cast<size_t>(b) * (g + 1) + k) * V + x), c_t, -lse2));
-        float pd = 1.f;
-        if (sampled) {
-            const float lse_d = a.lse_d[static_cast<size_t>(b) * g + k];
-            if (!(fabsf(lse_d) < INFINITY)) {
-                if (lane == 0) atomicOr(&s_bad, kBadNumeric);
-                continue;
+        if (__any_sync(0xFFFFFFFFu, bad)) {
+            write_bad(a, b, kBadRange);
+            return;
+        }
+        if (Lb == 0) {                                   // nothing to test: a bonus draw from row 0
+            write_decision(a, b, (0 << 2) | (sampled ? 2 : 0), sl);
+            return;
+        }
+    }
+    const uint32_t rej = __ldcg(a.rejm + b), bad = __ldcg(a.badm + b);
+    const uint32_t stop = rej | bad;
+    if (stop != 0u) {
+        const int p = __ffs(stop) - 1;                   // the first position that ends the block
+        if (bad & (1u << p)) {
+            write_bad(a, b, kBadNumeric);
+            return;
+        }
+        const int kstar = k0 + p;
+        sl.lse2_t = __ldcg(a.lse2w + static_cast<size_t>(b) * a.R + p);
+        sl.lse2_d = sampled ? a.lse_d[static_cast<size_t>(b) * g + kstar] * kLog2e : 0.f;
+        sl.prev = kstar == 0 ? anc : a.tokens[static_cast<size_t>(b) * g + kstar - 1];
+        sl.xk = a.tokens[static_cast<size_t>(b) * g + kstar];
+        write_decision(a, b, (kstar << 2) | (sampled ? 2 : 0) | 1, sl);
+    } else if (k0 + a.R >= Lb) {                         // all accepted: the bonus row L_b
+        write_decision(a, b, (Lb << 2) | (sampled ? 2 : 0), sl);
+    } else if (lane == 0) {                              // on to the next window
+        const uint32_t slot = atomicAdd(a.count + j + 1, 1u);
+        a.list[next_slot_base + static_cast<int>(slot)] = b;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) vl_rounds_kernel(VLArgs a) {
+    const int gw = static_cast<int>(blockIdx.x) * kWarps + static_cast<int>(warp_id());
+    const uint32_t lane = lane_id();
+    const bool vec = (a.V & 3) == 0;
+    const int per_req = a.R * a.n_chunk;                 // chunk items of one request per round
+    const int rounds = (a.g + a.R - 1) / a.R;
+    for (int j = 0; j < rounds; ++j) {
+        // round j: rows [j R, j R + R) of the requests undecided after round j - 1 (all in round 0)
+        const int k0 = j * a.R;
+        const int n_active = j == 0 ? a.B : static_cast<int>(__ldcg(a.count + j));
+        if (n_active == 0) break;
+        const int32_t* list = a.list + (j & 1) * a.B;
+        const int next_base = ((j + 1) & 1) * a.B;
+        const long long total = static_cast<long long>(n_active) * per_req;
+        long long f = total * gw / a.warps1;
+        const long long f1 = total * (gw + 1) / a.warps1;
+        while (f < f1) {
+            const int li = static_cast<int>(f / per_req);
+            const int b = j == 0 ? li : __ldcg(list + li);
+            const long long req_end = min(static_cast<long long>(li + 1) * per_req, f1);
+            const uint32_t count = static_cast<uint32_t>(req_end - f);
+            const int Lb = a.lengths != nullptr ? a.lengths[b] : a.g;
+            const bool ok = j > 0 || (request_ok(a, b) && Lb > 0);
+            const float c = kLog2e / a.T_t[b];
+            while (f < req_end) {
+                // the part of this row that falls in the warp's range
+                const int rem = static_cast<int>(f - static_cast<long long>(li) * per_req);
+                const int kk = rem / a.n_chunk, k = k0 + kk;
+                const long long row_end = min(static_cast<long long>(li) * per_req + (kk + 1) * a.n_chunk, req_end);
+                const uint32_t rcount = static_cast<uint32_t>(row_end - f);
+                const bool live = ok && k < Lb;
+                const float* row = a.t + (static_cast<size_t>(b) * (a.g + 1) + k) * a.V;
+                for (; f < row_end; ++f) {
+                    if (!live) continue;
+                    const int ch = static_cast<int>(f - static_cast<long long>(li) * per_req) - kk * a.n_chunk;
+                    const float2 p = chunk_lse(row, ch * kChunk + 4 * static_cast<int>(lane), a.V, vec, c);
+                    if (lane == 0) a.part[(static_cast<size_t>(b) * a.R + kk) * a.n_chunk + ch] = p;
+                }
+                if (live) {
+                    uint32_t last = 0;
+                    if (lane == 0) {
+                        __threadfence();
+                        last = atomicAdd(a.rowcnt + static_cast<size_t>(b) * a.g + k, rcount) + rcount ==
+                                       static_cast<uint32_t>(a.n_chunk) ? 1u : 0u;
+                    }
+                    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+                        __threadfence();
+                        decide_row(a, b, k, k0);
+                    }
+                }
             }
-            const float z = __fadd_rn(__ldg(a.L + (static_cast<size_t>(b) * g + k) * V + x), point_bias(a, x, prev));
-            pd = exp2f(fmaf(z, c_d, -lse_d * kLog2e));
+            uint32_t last = 0;
+            if (lane == 0) {
+                __threadfence();
+                last = atomicAdd(a.done + b, count) + count == static_cast<uint32_t>((j + 1) * per_req) ? 1u : 0u;
+            }
+            if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+                __threadfence();
+                decide_request(a, b, j, next_base);
+            }
         }
-        const uint4 wd = philox_at(a.seed, a.offset, 0u, static_cast<uint32_t>(b), kStreamAccept,
-                                   static_cast<uint32_t>(k));
-        const float u = uniform_from_word(wd.x);
-        if (!(__fmul_rn(u, pd) < pt) && lane == 0) atomicMin(&s_fail, k);
-    }
-    __syncthreads();
-    if (w != 0) return;
-    const bool bad = s_bad != 0;
-    const int kstar = s_fail;
-    const bool rejected = !bad && kstar < Lb;
-    if (lane == 0) {
-        if (bad)
-            set_status(a.ws, ((s_bad & kBadNumeric) ? DSPARK_STATUS_NUMERIC : 0u) |
-                                 ((s_bad & kBadRange) ? DSPARK_STATUS_INPUT_RANGE : 0u));
-        RowSel sl;
-        sl.c_t = c_t;
-        sl.lse2_t = bad ? 0.f : a.lse2[static_cast<size_t>(b) * (g + 1) + kstar];
-        sl.c_d = c_d;
-        sl.lse2_d = rejected && sampled ? a.lse_d[static_cast<size_t>(b) * g + kstar] * kLog2e : 0.f;
-        // every token of the tested block was checked above
-        sl.prev = bad ? 0 : (kstar == 0 ? anc : a.tokens[static_cast<size_t>(b) * g + kstar - 1]);
-        sl.xk = rejected ? a.tokens[static_cast<size_t>(b) * g + kstar] : -1;
-        sl.pad[0] = sl.pad[1] = 0;
-        a.sel[b] = sl;
-        a.decision[b] = bad ? -1 : ((kstar << 2) | (sampled ? 2 : 0) | (rejected ? 1 : 0));
+        if (j + 1 == rounds) break;
+        if (!grid_barrier(a.ws, static_cast<uint32_t>(j), a.timeout_ns, 0x5600u + static_cast<uint32_t>(j))) return;
     }
 }
 
@@ -555,7 +650,7 @@ __global__ void __launch_bounds__(kDrawThreads, 2) vl_draw_kernel(VLArgs a) {
         const int b = static_cast<int>(f / a.n_chunk3);
         const long long req_end = min(static_cast<long long>(b + 1) * a.n_chunk3, f1);
         const uint32_t count = static_cast<uint32_t>(req_end - f);
-        const int dec = a.decision[b];
+        const int dec = read_decision(a, b);
         if (dec >= 0) {
             const RowSel s = a.sel[b];
             const float* rt = a.t + (static_cast<size_t>(b) * (a.g + 1) + dec_kstar(dec)) * a.V;
@@ -601,26 +696,47 @@ __global__ void __launch_bounds__(kDrawThreads, 2) vl_draw_kernel(VLArgs a) {
 size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct VLLayout {
-    size_t keys, done3, clear_end, decision, sel, lse2, part, total;
+    size_t keys, done3, done, rowcnt, rejm, badm, count, decision, clear_end, sel, list, lse2w, part, total;
 };
 
-VLLayout vl_layout(int B, int gamma, int V, int r) {
+// Rows per round: all drafted rows at once while they are few (their bytes cost less than the
+// extra rounds would), else one row per round so that only rows k <= k* are streamed.
+int rows_per_round(int B, int gamma, int V) {
+    const double all_rows = 4.0 * B * static_cast<double>(gamma) * V;
+    return all_rows <= 64.0 * (1 << 20) ? std::min(gamma, 32) : 1;
+}
+
+VLLayout vl_layout(int B, int gamma, int V) {
     const size_t n_chunk = (static_cast<size_t>(V) + kChunk - 1) / kChunk;
+    const int R = rows_per_round(B, gamma, V);
+    const int rounds = (gamma + R - 1) / R;
     VLLayout l;
     size_t p = sizeof(WsHeader);
     l.keys = p;
     p = al(p + sizeof(unsigned long long) * B);
     l.done3 = p;
     p = al(p + sizeof(uint32_t) * B);
-    l.clear_end = p;
+    l.done = p;
+    p = al(p + sizeof(uint32_t) * B);
+    l.rowcnt = p;
+    p = al(p + sizeof(uint32_t) * static_cast<size_t>(B) * gamma);
+    l.rejm = p;
+    p = al(p + sizeof(uint32_t) * B);
+    l.badm = p;
+    p = al(p + sizeof(uint32_t) * B);
+    l.count = p;
+    p = al(p + sizeof(uint32_t) * (static_cast<size_t>(rounds) + 1));
     l.decision = p;
     p = al(p + sizeof(int32_t) * B);
+    l.clear_end = p;
     l.sel = p;
     p = al(p + sizeof(RowSel) * B);
-    l.lse2 = p;
-    p = al(p + sizeof(float) * static_cast<size_t>(B) * (gamma + 1));
+    l.list = p;
+    p = al(p + sizeof(int32_t) * 2 * static_cast<size_t>(B));
+    l.lse2w = p;
+    p = al(p + sizeof(float) * static_cast<size_t>(B) * R);
     l.part = p;
-    p = al(p + sizeof(float2) * static_cast<size_t>(B) * (gamma + 1) * n_chunk);
+    p = al(p + sizeof(float2) * static_cast<size_t>(B) * R * n_chunk);
     l.total = p;
     return l;
 }
@@ -629,7 +745,8 @@ VLLayout vl_layout(int B, int gamma, int V, int r) {
 
 size_t verify_logits_workspace_bytes(int B, int gamma, int V, int r) {
     if (B < 1 || gamma < 1 || V < 1 || r < 1) return 0;
-    return vl_layout(B, gamma, V, r).total;
+    (void)r;
+    return vl_layout(B, gamma, V).total;
 }
 
 dspark_status launch_verify_logits(const float* target_logits, const float* T_t, const float* base_logits,
@@ -638,7 +755,7 @@ dspark_status launch_verify_logits(const float* target_logits, const float* T_t,
                                    const int32_t* lengths, uint64_t seed, uint32_t offset, int B, int gamma,
                                    int V, int r, int32_t* out_tokens, int32_t* num_accepted, void* ws,
                                    cudaStream_t stream, const DeviceInfo& dev) {
-    const VLLayout l = vl_layout(B, gamma, V, r);
+    const VLLayout l = vl_layout(B, gamma, V);
     dspark_status st = clear_workspace(ws, l.clear_end, stream);
     if (st != DSPARK_OK) return st;
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -660,45 +777,54 @@ dspark_status launch_verify_logits(const float* target_logits, const float* T_t,
     a.done3 = reinterpret_cast<uint32_t*>(base + l.done3);
     a.decision = reinterpret_cast<int32_t*>(base + l.decision);
     a.sel = reinterpret_cast<RowSel*>(base + l.sel);
-    a.lse2 = reinterpret_cast<float*>(base + l.lse2);
+    a.done = reinterpret_cast<uint32_t*>(base + l.done);
+    a.rowcnt = reinterpret_cast<uint32_t*>(base + l.rowcnt);
+    a.rejm = reinterpret_cast<uint32_t*>(base + l.rejm);
+    a.badm = reinterpret_cast<uint32_t*>(base + l.badm);
+    a.count = reinterpret_cast<uint32_t*>(base + l.count);
+    a.list = reinterpret_cast<int32_t*>(base + l.list);
+    a.lse2w = reinterpret_cast<float*>(base + l.lse2w);
     a.part = reinterpret_cast<float2*>(base + l.part);
     a.seed = seed;
     a.offset = offset;
+    a.timeout_ns = kDefaultTimeoutNs;
     a.B = B;
     a.g = gamma;
     a.V = V;
     a.r = r;
     a.wbf16 = wdtype == DSPARK_BF16 ? 1 : 0;
     a.n_chunk = (V + kChunk - 1) / kChunk;
+    a.R = rows_per_round(B, gamma, V);
     a.n_chunk3 = (V + kDrawChunk - 1) / kDrawChunk;
-    a.total1 = static_cast<long long>(B) * (gamma + 1) * a.n_chunk;
     a.total3 = static_cast<long long>(B) * a.n_chunk3;
-    // lse: one 512-thread block per SM at most, each warp at least one 2048-entry chunk;
-    // draw: up to two 256-thread blocks per SM, each warp at least one 512-entry chunk
-    const int blocks1 = static_cast<int>(std::max(1LL, std::min(static_cast<long long>(dev.sm_count),
-                                                                 (a.total1 + kWarps - 1) / kWarps)));
+    // rounds: one co-resident 512-thread block per SM at most; draw: up to two 256-thread
+    // blocks per SM, each warp at least one 512-entry chunk
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vl_rounds_kernel, kThreads, 0);
+    if (e != cudaSuccess) return cuda_error(e, "occupancy(verify_logits rounds)");
+    if (per_sm < 1) {
+        set_error("verify_logits: the rounds kernel does not fit on an SM");
+        return DSPARK_ERR_UNSUPPORTED;
+    }
+    const long long want1 = (static_cast<long long>(B) * a.R * a.n_chunk + kWarps - 1) / kWarps;
+    const int blocks1 = static_cast<int>(std::max(1LL, std::min(static_cast<long long>(dev.sm_count), want1)));
     const int blocks3 = static_cast<int>(std::max(1LL, std::min(2LL * dev.sm_count,
                                                                  (a.total3 + kDrawWarps - 1) / kDrawWarps)));
     a.warps1 = blocks1 * kWarps;
     a.warps3 = blocks3 * kDrawWarps;
 
-    vl_lse_kernel<<<blocks1, kThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "launch(verify_logits lse)");
-    // programmatic dependent launch: the decide blocks become resident while the lse kernel runs
-    // and wait (griddepcontrol.wait) for its partials
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(B));
-    cfg.blockDim = dim3(32u * static_cast<unsigned>(std::min(gamma + 1, kDecideMaxWarps)));
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks1));
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;          // the rounds meet at grid barriers
+    attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, vl_decide_kernel, a);
-    if (e != cudaSuccess) return cuda_error(e, "launch(verify_logits decide)");
+    e = cudaLaunchKernelEx(&cfg, vl_rounds_kernel, a);
+    if (e != cudaSuccess) return cuda_error(e, "launch(verify_logits rounds)");
     vl_draw_kernel<<<blocks3, kDrawThreads, 0, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "launch(verify_logits draw)");

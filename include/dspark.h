@@ -88,8 +88,7 @@ typedef enum {
  *   DSPARK_OP_SCHEDULE      grows with B*N (radix-sort key buffers)
  *   DSPARK_OP_VERIFY_GREEDY grows with B*(N+1) (row argmax keys); N = gamma
  *   DSPARK_OP_CONFIDENCE    256 (the status word)
- *   DSPARK_OP_VERIFY_LOGITS grows with B*(N+1)*V/2048 (normaliser partials);
- *                           N = gamma
+ *   DSPARK_OP_VERIFY_LOGITS grows with B*V/2048 (normaliser partials); N = gamma
  * Returns 0 for an unknown op or negative sizes.
  */
 DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);
@@ -263,8 +262,9 @@ DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t
  * and the sampler's log-sum-exp (draft_lse = dspark_markov_sample's lse
  * output), and at the rejected position only at the entries whose perturbed
  * value can still win the draw (the draw is bounded through p_t, which the
- * residual never exceeds).  The target normalisers are computed here (rows
- * k <= L_b only).
+ * residual never exceeds).  The target normalisers are computed here, lazily:
+ * row k is read only if every earlier drafted token was accepted, so only the
+ * rows k <= k* are streamed.
  * Acceptance: fl32(u_k * p_d(x_k)) < p_t(x_k), u_k the stream-1 uniform as in
  * dspark_verify.  The correction (residual max(0, p_t - p_d) at the first
  * rejection) or bonus (p_t of row L_b) token is drawn by Gumbel-max,
@@ -295,8 +295,9 @@ DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t
  * Device-side: a token, anchor or length out of range or a temperature out of
  * its range sets INPUT_RANGE, a non-finite normaliser or draft_lse sets
  * NUMERIC; such a request outputs num_accepted 0 and -1 tokens.
- * Launches three kernels on `stream`, the second as a programmatic dependent
- * launch of the first (all captured by CUDA stream capture).
+ * Launches two kernels on `stream` (captured by CUDA stream capture), the first
+ * a cooperative persistent kernel whose rounds meet at bounded grid barriers
+ * (a barrier that gives up sets TIMEOUT).
  * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY_LOGITS, B, gamma, V, r).
  */
 DSPARK_API dspark_status dspark_verify_logits(const float* target_logits, const float* target_temperature,

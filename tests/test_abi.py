@@ -43,8 +43,10 @@ def test_workspace_sizes(L):
     assert L.dspark_workspace_size(4, 256, 8, 151936, 0) == 256 + 8 * 256 * 9 + 1024
     assert L.dspark_workspace_size(5, 64, 16, 151936, 256) == 256
     vl = L.dspark_workspace_size(6, 256, 8, 151936, 256)
-    # keys, counters, decisions, row selections, row normalisers, their chunk partials
-    assert vl == 256 + 256 * (8 + 4 + 4 + 32) + 4 * 256 * 9 + 8 * 256 * 9 * 75
+    # keys, per-request and per-row counters, window masks, per-round counts, decisions, row
+    # selections, two request lists, the window's normalisers and chunk partials (one row per
+    # round at this size)
+    assert vl == 256 + 2048 + 1024 + 1024 + 8192 + 1024 + 1024 + 256 + 1024 + 8192 + 2048 + 1024 + 8 * 256 * 75
     assert L.dspark_workspace_size(6, 0, 8, 100, 8) == 0
     assert L.dspark_workspace_size(9, 1, 1, 1, 1) == 0
 

@@ -170,11 +170,13 @@ def test_bonus_only_and_all_greedy(cuda_lib):
             assert np.all(nacc.cpu().numpy() == 0)
 
 
-def test_invalid_requests_set_status(cuda_lib):
+@pytest.mark.parametrize("B,gamma,V", [(12, 4, 1500), (64, 4, 70001)])
+def test_invalid_requests_set_status(cuda_lib, B, gamma, V):
     """Out-of-range token, anchor or length, a non-positive target temperature, a negative draft
     temperature and a NaN draft lse each void their request (num_accepted 0, tokens -1) and set
-    the status; the other requests still match the oracle."""
-    cfg = _small_cfg("bf16", 1500, 8, temps=(1.0,), B=12)
+    the status; the other requests still match the oracle.  The two sizes take the two row
+    schedules (every drafted row in one round; one row per round)."""
+    cfg = _small_cfg("bf16", V, 8, temps=(1.0,), B=B, gamma=gamma)
     inp = verify_logits_inputs(cfg)
     inp["lengths"] = np.full(cfg.B, cfg.gamma, np.int32)
     lse = oracle.draft_lse(inp["base_logits"], inp["anchor"], inp["w1_f32"], inp["w2_f32"], inp["T_d"],
