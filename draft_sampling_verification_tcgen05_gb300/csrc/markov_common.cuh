@@ -104,18 +104,24 @@ __device__ __forceinline__ int slot_token(const MarkovArgs& a, int i, int b) {
     return static_cast<int>(key_index(k));
 }
 
-// Combine the lse partials of step i for the requests this block finalises.
-// `tid`/`nthreads`: this thread's index among the block's participating threads.
+// Combine the lse partials of step i: one warp per request, the lanes over the blocks' partials,
+// then a butterfly merge.  `tid`/`nthreads`: this thread's index among the block's participating
+// threads (whole warps).
 __device__ inline void finish_lse(const MarkovArgs& a, int i, int tid, int nthreads) {
     if (a.lse == nullptr) return;
     const float2* part = a.lay.lse_part + static_cast<size_t>(i & 1) * kMaxGrid * a.B;
-    for (int b = blockIdx.x * nthreads + tid; b < a.B; b += gridDim.x * nthreads) {
+    const int lane = tid & 31, warps = nthreads >> 5;
+    for (int b = static_cast<int>(blockIdx.x) * warps + (tid >> 5); b < a.B; b += static_cast<int>(gridDim.x) * warps) {
         float2 m = make_float2(0.f, 0.f);
-        for (int c = 0; c < static_cast<int>(gridDim.x); ++c) {
-            const float2 p = __ldcg(part + static_cast<size_t>(c) * a.B + b);
-            m = lse_merge(m, p);
+        for (int c = lane; c < static_cast<int>(gridDim.x); c += 32) m = lse_merge(m, __ldcg(part + static_cast<size_t>(c) * a.B + b));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float2 other;
+            other.x = __shfl_xor_sync(0xFFFFFFFFu, m.x, o);
+            other.y = __shfl_xor_sync(0xFFFFFFFFu, m.y, o);
+            m = lse_merge(m, other);
         }
-        a.lse[static_cast<size_t>(b) * a.N + i] = m.y > 0.f ? m.x + logf(m.y) : -INFINITY;
+        if (lane == 0) a.lse[static_cast<size_t>(b) * a.N + i] = m.y > 0.f ? m.x + logf(m.y) : -INFINITY;
     }
 }
 

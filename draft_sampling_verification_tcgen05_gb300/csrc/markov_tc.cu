@@ -24,7 +24,10 @@
 //                          per-request argmax of z -> one real perturbed value
 //                          published as the lower bound LB (atomicMax)
 //                 pass 2   z from TMEM; Gumbel noise only where z + G_max >= LB;
-//                          block argmax -> one atomicMax per (block, request)
+//                          block argmax -> one atomicMax per (block, request);
+//                          with an lse output, also the block's sum of
+//                          exp(z - block max z) per request, merged over the
+//                          blocks at the start of the next step
 //   then a grid barrier among warps 1..9; the producer keeps streaming.
 // No [B, V] row is written to device memory.
 #include "device_common.cuh"
@@ -57,6 +60,7 @@ constexpr uint32_t kBarGroup0 = 2;
 constexpr uint32_t kBarEpi = kBarGroup0 + kGroups;   // all epilogue warps
 constexpr uint32_t kWaitProducer = 0x301, kWaitMma = 0x302, kWaitEpi = 0x303;
 constexpr size_t kEMaxBytes = 64 * 1024;
+constexpr float kLog2eF = 1.4426950408889634f;
 
 struct TcArgs {
     int w2_stages;        // depth of the w2 ring
@@ -139,6 +143,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ float s_lb[kGroups][kChunk];
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
     __shared__ unsigned long long s_best[kGroups][kChunk];
+    __shared__ float s_zmax[256];                                      // block max of z per request
+    __shared__ float s_lsum[kGroups][4][kChunk];                       // per-warp sums of exp(z - zmax)
     __shared__ __align__(16) float s_zt[kEpiWarps][8 * kZtPitch];      // z of 8 requests x 32 rows, transposed
     __shared__ int s_ok;
 
@@ -290,6 +296,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         const int chunks16 = a.r / 8;                         // 16-byte pieces of a w1 row
 
         for (int i = 0; i < a.N && alive; ++i) {
+            if (i > 0) finish_lse(a, i - 1, stid, static_cast<int>(kStepThreads));
             // ---- previous tokens, then E = w1[prev] in the swizzled K-major operand layout ----
             for (int b = stid; b < a.B; b += kStepThreads) {
                 int p;
@@ -393,6 +400,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                         const int b = c * kChunk + static_cast<int>(lane);
                         unsigned long long k = 0;
                         for (int q = 0; q < 4; ++q) k = s_part[grp][q][lane] > k ? s_part[grp][q][lane] : k;
+                        if (b < a.B) s_zmax[b] = k != 0ull ? float_from_order_bits(static_cast<uint32_t>(k >> 32)) : -INFINITY;
                         if (b < a.B && k != 0ull) {
                             const uint32_t vb = key_index(k);
                             if (s_invT[b] > 0.f) {
@@ -444,13 +452,17 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                     bool any = false;
 #pragma unroll
                     for (int j = 0; j < kChunk; ++j) any |= s_lb[grp][j] < INFINITY;
-                    if (any && !dead) {
+                    const bool want_lse = a.lse != nullptr;
+                    const int jj = static_cast<int>(lane >> 2), q = static_cast<int>(lane & 3u);
+                    const int b0 = c * kChunk + jj, b1 = b0 + 8;
+                    float ls0 = 0.f, ls1 = 0.f;               // sums of exp(z - block max z)
+                    if ((any || want_lse) && !dead) {
                         // lane (jj, q) takes rows 8q..8q+7 of requests jj and 8 + jj: one Philox
                         // block each, both drawn (independent chains, interleaved) as soon as one
                         // of the 16 entries passes the z test
-                        const int jj = static_cast<int>(lane >> 2), q = static_cast<int>(lane & 3u);
                         const float lb0 = s_lb[grp][jj], lb1 = s_lb[grp][8 + jj];
-                        const int b0 = c * kChunk + jj, b1 = b0 + 8;
+                        const float m0 = want_lse && b0 < a.B ? s_zmax[b0] : -INFINITY;
+                        const float m1 = want_lse && b1 < a.B ? s_zmax[b1] : -INFINITY;
                         for (int tl = 0; tl < nt; ++tl) {
                             const int v0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32) + 8 * q;
                             const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
@@ -460,6 +472,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             float z0[8], z1[8];
                             transpose_half(s_zt[epi], r, 0, lane, z0);
                             transpose_half(s_zt[epi], r, 1, lane, z1);
+                            if (want_lse) {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    if (v0 + k < a.V) {
+                                        if (m0 > -INFINITY) ls0 += exp2f(__fmul_rn(__fsub_rn(z0[k], m0), kLog2eF));
+                                        if (m1 > -INFINITY) ls1 += exp2f(__fmul_rn(__fsub_rn(z1[k], m1), kLog2eF));
+                                    }
+                                }
+                            }
                             uint32_t p0 = 0, p1 = 0;
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
@@ -497,9 +518,26 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             }
                         }
                     }
+                    if (a.lse != nullptr) {
+                        // the four lanes of a request pair, then the four warps of the group (fixed order)
+                        ls0 += __shfl_xor_sync(0xFFFFFFFFu, ls0, 1);
+                        ls0 += __shfl_xor_sync(0xFFFFFFFFu, ls0, 2);
+                        ls1 += __shfl_xor_sync(0xFFFFFFFFu, ls1, 1);
+                        ls1 += __shfl_xor_sync(0xFFFFFFFFu, ls1, 2);
+                        if (q == 0) {
+                            s_lsum[grp][quad][jj] = ls0;
+                            s_lsum[grp][quad][8 + jj] = ls1;
+                        }
+                    }
                     named_bar_sync(kBarGroup0 + grp, 128);
                     if (grp_lead && lane < kChunk) {
                         const int b = c * kChunk + static_cast<int>(lane);
+                        if (a.lse != nullptr && b < a.B) {
+                            const float S = ((s_lsum[grp][0][lane] + s_lsum[grp][1][lane]) + s_lsum[grp][2][lane]) +
+                                            s_lsum[grp][3][lane];
+                            a.lay.lse_part[(static_cast<size_t>(i & 1) * kMaxGrid + blockIdx.x) * a.B + b] =
+                                make_float2(s_zmax[b], s_zmax[b] > -INFINITY ? S : 0.f);
+                        }
                         const unsigned long long k = s_best[grp][lane];
                         if (b < a.B && k != 0ull) {
                             atomicMax(slot + b, k);
@@ -517,6 +555,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
             tc_fence_after();
         }
         if (nan_seen) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+        if (alive) finish_lse(a, a.N - 1, stid, static_cast<int>(kStepThreads));
         if (alive && blockIdx.x == 0) {
             for (int idx = stid; idx < a.B * a.N; idx += kStepThreads) {
                 const int b = idx / a.N, i = idx % a.N;
@@ -552,7 +591,8 @@ size_t tc_smem_bytes(int B_pad, int r) {
 
 bool markov_tc_eligible(int B, int N, int V, int r, dspark_dtype wdtype, const float* base, const float* lse,
                         int sm_count) {
-    if (wdtype != DSPARK_BF16 || lse != nullptr) return false;
+    (void)lse;
+    if (wdtype != DSPARK_BF16) return false;
     if (B < 16 || B > 256 || r % 64 != 0 || r > 256 || V % 4 != 0 || V < kTileV || V >= (1 << 27))
         return false;
     if (N > 65535 || !aligned(base, 16)) return false;
