@@ -233,28 +233,69 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t w) {
     return -logf(-logf(u));
 }
 
-// Draft noise of element v: a 16-bit high half from stream 0 and a 16-bit low
-// half from stream 3, both from counter j = v >> 3, word (v & 7) >> 1, bits 0-15
-// for even v and 16-31 for odd v.  The uniform, and so the Gumbel variate, is
-// increasing in the 32-bit word (high << 16) | low, so the high half alone
-// bounds the variate.
-__device__ __forceinline__ uint32_t draft_half(uint4 w, uint32_t v) {
-    const uint32_t sel = (v & 7u) >> 1;
-    const uint32_t word = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
-    return (word >> (16u * (v & 1u))) & 0xFFFFu;
+// Draft noise, in groups of 16 entries (group G = v >> 4, position k = v & 15).
+// The group word is word G & 3 of stream-0 counter G >> 2: its bits 0-3 give
+// the position p of the group's largest variate and its uniform u0 the
+// group's smallest exponential E_min = -log(u0) / 16.  Entry k != p adds its
+// own exponential: E_k = E_min - log(u_k), u_k from word k & 3 of stream-3
+// counter (G << 2) | (k >> 2); E_p = E_min; g = -log(E).  The 16 E's are
+// independent Exp(1) variates (the smallest of 16 is Exp(16), at a uniform
+// position, and the rest exceed it by independent Exp(1) amounts), so the g's
+// are independent standard Gumbels, and -log(E_min) bounds the whole group.
+__device__ __forceinline__ uint32_t word_of(const uint4& w, uint32_t s) {
+    return s == 0 ? w.x : s == 1 ? w.y : s == 2 ? w.z : w.w;
 }
 
-__device__ __forceinline__ uint32_t draft_word(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i,
-                                               uint32_t v) {
-    const uint32_t hi = draft_half(philox_at(seed, offset, v >> 3, b, kStreamGumbel, i), v);
-    const uint32_t lo = draft_half(philox_at(seed, offset, v >> 3, b, kStreamGumbelLo, i), v);
-    return (hi << 16) | lo;
+__device__ __forceinline__ uint32_t draft_group_word(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i,
+                                                     uint32_t G) {
+    return word_of(philox_at(seed, offset, G >> 2, b, kStreamGumbel, i), G & 3u);
 }
 
-// Every Gumbel variate produced above is below this bound: the largest u is
-// 1 - 2^-24, for which -log(-log(u)) = 16.6355..; logf is accurate to a few
-// ulp, so 16.75 leaves a wide margin.  Used only to skip elements that can
-// not win the argmax.
+// E_min of a group word (the scaling by 1/16 is exact).
+__device__ __forceinline__ float group_e_min(uint32_t W) {
+    return __fmul_rn(-logf(uniform_from_word(W)), 0.0625f);
+}
+
+// Gumbel variate of an entry other than the group's largest, from its element word.
+__device__ __forceinline__ float draft_gumbel_of_entry(float e_min, uint32_t w) {
+    return -logf(__fadd_rn(e_min, -logf(uniform_from_word(w))));
+}
+
+// Gumbel variate of entry k of group G whose group word is W (E_min = group_e_min(W)).
+__device__ __forceinline__ float draft_gumbel_in_group(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i,
+                                                       uint32_t G, uint32_t k, uint32_t W, float e_min) {
+    if (k == (W & 15u)) return -logf(e_min);
+    return draft_gumbel_of_entry(e_min, word_of(philox_at(seed, offset, (G << 2) | (k >> 2), b, kStreamGumbelLo, i),
+                                                k & 3u));
+}
+
+__device__ __forceinline__ float draft_gumbel(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i, uint32_t v) {
+    const uint32_t G = v >> 4;
+    const uint32_t W = draft_group_word(seed, offset, b, i, G);
+    return draft_gumbel_in_group(seed, offset, b, i, G, v & 15u, W, group_e_min(W));
+}
+
+// Draft variates of the adjacent entries v and v + 1 (v even: one group word and one
+// element counter serve both).
+__device__ __forceinline__ void draft_gumbel_pair(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i,
+                                                  uint32_t v, float& g0, float& g1) {
+    const uint32_t G = v >> 4, k = v & 15u;
+    const uint32_t W = draft_group_word(seed, offset, b, i, G);
+    const float e_min = group_e_min(W);
+    const uint4 w = philox_at(seed, offset, (G << 2) | (k >> 2), b, kStreamGumbelLo, i);
+    const uint32_t p = W & 15u;
+    g0 = k == p ? -logf(e_min) : draft_gumbel_of_entry(e_min, word_of(w, k & 3u));
+    g1 = k + 1u == p ? -logf(e_min) : draft_gumbel_of_entry(e_min, word_of(w, (k + 1u) & 3u));
+}
+
+// Bound on every draft variate: E_min >= -log(1 - 2^-24) / 16, so g <= 19.41; logf is
+// accurate to a few ulp, so 19.5 leaves a wide margin.
+constexpr float kDraftGumbelMax = 19.5f;
+
+// Every standard Gumbel variate of one word (gumbel_from_word) is below this
+// bound: the largest u is 1 - 2^-24, for which -log(-log(u)) = 16.6355..; logf
+// is accurate to a few ulp, so 16.75 leaves a wide margin.  Used only to skip
+// elements that can not win an argmax.
 constexpr float kGumbelMax = 16.75f;
 
 // ---------------------------------------------------------------------------
@@ -481,6 +522,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+// 32 lanes x 32 bits, one column: thread t of the warp gets lane (quadrant*32 + t) of column col.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {

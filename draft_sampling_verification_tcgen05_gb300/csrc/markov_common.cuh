@@ -83,8 +83,7 @@ __device__ __forceinline__ int32_t output_token(const MarkovArgs& a, int d) {
 }
 
 __device__ __forceinline__ float gumbel_at(const MarkovArgs& a, int b, int i, int v) {
-    return gumbel_from_word(draft_word(a.seed, a.offset, static_cast<uint32_t>(b), static_cast<uint32_t>(i),
-                                       static_cast<uint32_t>(v)));
+    return draft_gumbel(a.seed, a.offset, static_cast<uint32_t>(b), static_cast<uint32_t>(i), static_cast<uint32_t>(v));
 }
 
 __device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {

@@ -264,14 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         const float* lr = a.base + static_cast<size_t>(j) * a.V;
         l0 = __ldcs(lr + v);
         l1 = two ? __ldcs(lr + v + 1) : 0.f;
-        const uint4 wh = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, 0u, kStreamGumbel,
-                                   static_cast<uint32_t>(j));
-        const uint4 wl = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, 0u, kStreamGumbelLo,
-                                   static_cast<uint32_t>(j));
-        g0 = gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v)) << 16) | draft_half(wl, static_cast<uint32_t>(v)));
-        g1 = two ? gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v + 1)) << 16) |
-                                    draft_half(wl, static_cast<uint32_t>(v + 1)))
-                 : 0.f;
+        draft_gumbel_pair(a.seed, a.offset, 0u, static_cast<uint32_t>(j), static_cast<uint32_t>(v), g0, g1);
+        if (!two) g1 = 0.f;
     };
     if (fast) prepare(0, pl0, pl1, pg0, pg1);
     bool alive = true;
@@ -326,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             bool bad = false;
             if (hot && a.single_pass && a.lse == nullptr) {
                 // one pass with noise on every entry; each thread takes two adjacent entries,
-                // which share their noise counter (v >> 3) and interleave for ILP
+                // which share their group word and element counter and interleave for ILP
                 for (int t = 2 * tid; t < n_local; t += 2 * kThreads) {
                     const int v = v_lo + t;
                     const bool two = t + 1 < n_local;
@@ -342,15 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                     } else {
                         l0 = __ldcs(lrow + v);
                         l1 = two ? __ldcs(lrow + v + 1) : 0.f;
-                        const uint4 wh = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
-                                                   kStreamGumbel, static_cast<uint32_t>(i));
-                        const uint4 wl = philox_at(a.seed, a.offset, static_cast<uint32_t>(v) >> 3, static_cast<uint32_t>(b),
-                                                   kStreamGumbelLo, static_cast<uint32_t>(i));
-                        g0 = gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v)) << 16) |
-                                              draft_half(wl, static_cast<uint32_t>(v)));
-                        g1 = two ? gumbel_from_word((draft_half(wh, static_cast<uint32_t>(v + 1)) << 16) |
-                                                    draft_half(wl, static_cast<uint32_t>(v + 1)))
-                                 : 0.f;
+                        draft_gumbel_pair(a.seed, a.offset, static_cast<uint32_t>(b), static_cast<uint32_t>(i),
+                                          static_cast<uint32_t>(v), g0, g1);
+                        if (!two) g1 = 0.f;
                     }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -422,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                                                       : static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v) * row_bytes;
                     z = __fmul_rn(__fadd_rn(__ldg(lrow + v), bias_dot<WT>(wrow, e, a.r)), invT);
                 }
-                if (!(__fadd_rn(z, kGumbelMax) >= lb)) continue;      // cannot win (or NaN)
+                if (!(__fadd_rn(z, kDraftGumbelMax) >= lb)) continue;  // cannot win (or NaN)
                 const float y = __fadd_rn(z, gumbel_at(a, b, i, v));
                 if (y != y) continue;
                 const unsigned long long k = argmax_key(y, static_cast<uint32_t>(v));

@@ -23,8 +23,11 @@
 //                          block's whole [tiles x 128, B] slab of z for the step;
 //                          per-request argmax of z -> one real perturbed value
 //                          published as the lower bound LB (atomicMax)
-//                 pass 2   z from TMEM; Gumbel noise only where z + G_max >= LB;
-//                          block argmax -> one atomicMax per (block, request);
+//                 pass 2   z from TMEM; per 16-entry noise group one group word
+//                          (its top byte bounds the group's largest variate by a
+//                          table); only groups whose largest z plus that bound
+//                          reaches LB draw exact variates (rare); block argmax ->
+//                          one atomicMax per (block, request);
 //                          with an lse output, also the block's sum of
 //                          exp(z - block max z) per request, merged over the
 //                          blocks at the start of the next step
@@ -54,7 +57,7 @@ constexpr int kMaxLocalTiles = 32;
 constexpr int kZtPitch = 36;                     // floats per request row of the transpose buffer (no bank conflicts)
 constexpr uint32_t kW2StageBytes = kTileV * 128;             // 128 rows x 64 bf16
 constexpr uint32_t kLStageBytes = kTileV * kChunk * 4;       // 16 requests x 128 fp32
-constexpr uint32_t kGtabBytes = 256 * 32 * 4;                // bound table, one copy per bank
+constexpr uint32_t kGtabBytes = 256 * 4;                     // bound table of the group words
 constexpr uint32_t kBarStep = 1;
 constexpr uint32_t kBarGroup0 = 2;
 constexpr uint32_t kBarEpi = kBarGroup0 + kGroups;   // all epilogue warps
@@ -75,27 +78,41 @@ __device__ __forceinline__ void tile_range(const TcArgs& t, int& lo, int& hi) {
     hi = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * t.n_tiles) / gridDim.x);
 }
 
-// Can an element whose noise word has high half `hi` reach a perturbed value
-// d above its scaled logit?  Its uniform is below u_max = (hi + 1) / 2^16 and g
-// increases with u, so if u_max < exp(-exp(-(d - 1e-3))) then g < d - 1e-3 and
-// the element stays strictly below the bound.  The fast exponentials carry a
-// relative error far below the 1e-5 slack, and 1e-3 covers the rounding of g
-// and of z + g, so a "no" is always right.
-__device__ __forceinline__ bool high_half_can_reach(uint32_t hi, float d) {
-    if (d < 2.0f) return true;                               // too close to the bound: draw exactly
-    const float thr = __expf(-__expf(-(d - 1e-3f))) * (1.0f - 1e-5f);
-    const float u_max = static_cast<float>(hi + 1u) * 0x1p-16f;
-    return u_max >= thr;
+// Stream-0 counter of the two noise groups of local tile `tile` that TMEM lane quadrant `quad`
+// holds (rows quad * 32 .. quad * 32 + 31 of the tile: groups 8 tile + 2 quad and + 1).
+__device__ __forceinline__ uint32_t group_counter(int tile, uint32_t quad) {
+    return static_cast<uint32_t>((tile * kTileV + static_cast<int>(quad * 32u)) >> 6);
 }
 
-// Full noise of one element that its high half could not rule out (rare):
-// draws the low half, returns the argmax key of z + g (0 for NaN).  Kept out
-// of line so the unrolled test loop stays small.
-__device__ __noinline__ unsigned long long rare_candidate(uint64_t seed, uint32_t offset, uint32_t b, uint32_t i,
-                                                          uint32_t v, float z, uint32_t hi) {
-    const uint32_t lo = draft_half(philox_at(seed, offset, v >> 3, b, kStreamGumbelLo, i), v);
-    const float y = __fadd_rn(z, gumbel_from_word((hi << 16) | lo));
-    return (y == y) ? argmax_key(y, v) : 0ull;
+// Exact candidates of one noise group that the table test could not rule out (rare), drawn by
+// the whole warp: one TMEM column load gives lane l the z of row quad * 32 + l for the request,
+// so each of the group's 16 lanes (half `gsel` of the warp) tests its own entry.  The group's
+// largest variate -log(E_min) is exact for the entry at position p and bounds every other one,
+// so an entry is drawn only when z + that variate still reaches lb (the 1e-3 covers the rounding
+// of z + g and of logf).  The best key goes to `best_slot`.  Called by the whole warp.
+__device__ __forceinline__ void group_candidates(const MarkovArgs& a, int b, int i, uint32_t taddr, int v_row0,
+                                                 uint32_t gsel, uint32_t W, float lb, unsigned long long* best_slot) {
+    const uint32_t lane = lane_id();
+    const float z = __uint_as_float(tmem_ld1(taddr));
+    tmem_wait_ld();
+    const int v = v_row0 + static_cast<int>(lane);
+    const uint32_t k = lane & 15u;
+    const float e_min = group_e_min(W);
+    const float g_top = -logf(e_min);
+    unsigned long long key = 0ull;
+    if ((lane >> 4) == gsel && v < a.V && __fadd_rn(__fadd_rn(z, g_top), 1e-3f) >= lb) {
+        float g = g_top;
+        if (k != (W & 15u)) {
+            const uint32_t G = static_cast<uint32_t>(v) >> 4;
+            g = draft_gumbel_of_entry(e_min, word_of(philox_at(a.seed, a.offset, (G << 2) | (k >> 2),
+                                                               static_cast<uint32_t>(b), kStreamGumbelLo,
+                                                               static_cast<uint32_t>(i)), k & 3u));
+        }
+        const float y = __fadd_rn(z, g);
+        if (y == y) key = argmax_key(y, static_cast<uint32_t>(v));
+    }
+    key = warp_max_u64(key);
+    if (lane == 0 && key != 0ull) atomicMax(best_slot, key);
 }
 
 // Half h of a tile-chunk seen transposed: the warp holds z for its 32 rows (one per lane) and 16
@@ -114,13 +131,6 @@ __device__ __forceinline__ void transpose_half(float* zt, const uint32_t (&r)[16
     zz[4] = b.x; zz[5] = b.y; zz[6] = b.z; zz[7] = b.w;
 }
 
-// High half (16 bits) of entry k (0..7) of a Philox block of 8 entries: even entries in the low
-// 16 bits of word k/2.
-__device__ __forceinline__ uint32_t half_of(const uint4& w, int k) {
-    const uint32_t word = (k >> 1) == 0 ? w.x : (k >> 1) == 1 ? w.y : (k >> 1) == 2 ? w.z : w.w;
-    return (word >> (16 * (k & 1))) & 0xFFFFu;
-}
-
 __global__ void __launch_bounds__(kThreadsTC, 1)
 markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmL,
                  MarkovArgs a, TcArgs t) {
@@ -129,8 +139,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* w2s = base;
     uint8_t* Ls = w2s + t.w2_stages * kW2StageBytes;
-    // gtab[k][lane]: bound on g for a noise word with top byte k, replicated across the 32 banks
-    // so that a warp's lookups with random k never conflict
+    // gtab[k]: bound on the largest variate of a noise group whose group word has top byte k
     float* gtab = reinterpret_cast<float*>(Ls + kGroups * t.l_stages * kLStageBytes);
     uint8_t* Es = Ls + kGroups * t.l_stages * kLStageBytes + kGtabBytes;
 
@@ -188,12 +197,13 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         s_invT[b] = inv;
     }
     if (bad_t) set_status(a.ws, DSPARK_STATUS_NUMERIC);
-    // gtab[k][.] bounds the variate of every word whose top byte is k: the variate of
-    // the largest such word (it increases with the word) plus a margin for logf's
+    // gtab[k][.] bounds the largest variate -log(E_min) of a noise group whose group word has top
+    // byte k: that of the largest such word (it increases with the word) plus a margin for logf's
     // rounding; the top bin is capped by the global bound
     for (int k = threadIdx.x; k < 256; k += kThreadsTC) {
-        const float g = k == 255 ? kGumbelMax : gumbel_from_word((static_cast<uint32_t>(k + 1) << 24) - 1u) + 1e-3f;
-        for (int l = 0; l < 32; ++l) gtab[k * 32 + l] = g;
+        const float g = k == 255 ? kDraftGumbelMax
+                                 : -logf(group_e_min((static_cast<uint32_t>(k + 1) << 24) - 1u)) + 1e-3f;
+        gtab[k] = g;
     }
     {   // zero E once: padding rows (b >= B) stay zero for the whole call
         uint4* e4 = reinterpret_cast<uint4*>(Es);
@@ -434,11 +444,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 named_bar_sync(kBarEpi, 32 * kEpiWarps);
 
                 // ---- pass 2 over this group's chunks: noise only where z can still beat the
-                //      bound.  The high halves of the noise words come 8 per Philox call (lane
-                //      l draws the counter of 8 consecutive entries for two requests); a table
-                //      bound on g from the top byte, then the exact bound from the 16-bit
-                //      high half, rule out almost every element; only the rest draw their
-                //      low half and the exact variate ----
+                //      bound.  One group word per 16 entries bounds the group's largest variate
+                //      (a table on its top byte); a group whose largest z plus that bound
+                //      reaches LB is drawn exactly by the whole warp (rare) ----
                 for (int ro = 0; ro < rounds; ++ro) {
                     const int c = ro * kGroups + grp;
                     if (c >= n_chunks) continue;
@@ -457,12 +465,17 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                     const int b0 = c * kChunk + jj, b1 = b0 + 8;
                     float ls0 = 0.f, ls1 = 0.f;               // sums of exp(z - block max z)
                     if ((any || want_lse) && !dead) {
-                        // lane (jj, q) takes rows 8q..8q+7 of requests jj and 8 + jj: one Philox
-                        // block each, both drawn (independent chains, interleaved) as soon as one
-                        // of the 16 entries passes the z test
+                        // lane (jj, q) takes rows 8q..8q+7 of requests jj and 8 + jj; lanes q and
+                        // q ^ 1 hold the two halves of one 16-entry noise group, whose group word
+                        // bounds every variate of the group.  Lane l draws the stream-0 counter of
+                        // the warp's two groups for request l & 15 of the chunk and passes the
+                        // two group words to the lanes that hold those groups.
                         const float lb0 = s_lb[grp][jj], lb1 = s_lb[grp][8 + jj];
                         const float m0 = want_lse && b0 < a.B ? s_zmax[b0] : -INFINITY;
                         const float m1 = want_lse && b1 < a.B ? s_zmax[b1] : -INFINITY;
+                        const uint32_t pw = (quad * 2u) & 3u;            // word of the warp's first group
+                        const int bsrc = c * kChunk + static_cast<int>(lane & 15u);
+                        const bool draw = any && s_lb[grp][lane & 15u] < INFINITY;
                         for (int tl = 0; tl < nt; ++tl) {
                             const int v0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32) + 8 * q;
                             const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
@@ -481,40 +494,42 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                     }
                                 }
                             }
-                            uint32_t p0 = 0, p1 = 0;
+                            uint32_t wa = 0, wb = 0;
+                            if (draw) {
+                                const uint4 w = philox_at(a.seed, a.offset, group_counter(tile_lo + tl, quad),
+                                                          static_cast<uint32_t>(bsrc), kStreamGumbel, static_cast<uint32_t>(i));
+                                wa = word_of(w, pw);
+                                wb = word_of(w, pw + 1u);
+                            }
+                            const uint32_t a0 = __shfl_sync(0xFFFFFFFFu, wa, jj), c0 = __shfl_sync(0xFFFFFFFFu, wb, jj);
+                            const uint32_t a1 = __shfl_sync(0xFFFFFFFFu, wa, 8 + jj), c1 = __shfl_sync(0xFFFFFFFFu, wb, 8 + jj);
+                            const uint32_t W0 = (q >> 1) ? c0 : a0, W1 = (q >> 1) ? c1 : a1;
+                            // the group's largest z (entries past V left out), from both halves
+                            float gm0 = -INFINITY, gm1 = -INFINITY;
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
-                                const bool in = v0 + k < a.V;
-                                p0 |= (in && __fadd_rn(z0[k], kGumbelMax) >= lb0 ? 1u : 0u) << k;
-                                p1 |= (in && __fadd_rn(z1[k], kGumbelMax) >= lb1 ? 1u : 0u) << k;
+                                if (v0 + k < a.V) {
+                                    gm0 = fmaxf(gm0, z0[k]);
+                                    gm1 = fmaxf(gm1, z1[k]);
+                                }
                             }
-                            if ((p0 | p1) == 0u) continue;
-                            const uint4 w0 = philox_at(a.seed, a.offset, static_cast<uint32_t>(v0 >> 3),
-                                                       static_cast<uint32_t>(b0), kStreamGumbel, static_cast<uint32_t>(i));
-                            const uint4 w1 = philox_at(a.seed, a.offset, static_cast<uint32_t>(v0 >> 3),
-                                                       static_cast<uint32_t>(b1), kStreamGumbel, static_cast<uint32_t>(i));
-                            // straight-line: the table bound on g from the top byte of each high half
-                            uint32_t need = 0;
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                need |= (((p0 >> k) & 1u) && __fadd_rn(z0[k], gtab[(half_of(w0, k) >> 8) * 32 + lane]) >= lb0 ? 1u : 0u) << k;
-                                need |= (((p1 >> k) & 1u) && __fadd_rn(z1[k], gtab[(half_of(w1, k) >> 8) * 32 + lane]) >= lb1 ? 1u : 0u) << (8 + k);
-                            }
-                            // rare: the exact 16-bit bound, then the full draw (compact loop over set bits)
-                            while (need != 0u) {
-                                const int e = __ffs(need) - 1;
-                                need &= need - 1u;
-                                const int hh = e >> 3, k = e & 7;
-                                float z = 0.f;                       // register select, no local array
-#pragma unroll
-                                for (int kk = 0; kk < 8; ++kk) z = kk == k ? (hh ? z1[kk] : z0[kk]) : z;
-                                const float lb = hh ? lb1 : lb0;
-                                const uint32_t hi = half_of(hh ? w1 : w0, k);
-                                if (!high_half_can_reach(hi, __fsub_rn(lb, z))) continue;
-                                const unsigned long long key =
-                                    rare_candidate(a.seed, a.offset, static_cast<uint32_t>(hh ? b1 : b0),
-                                                   static_cast<uint32_t>(i), static_cast<uint32_t>(v0 + k), z, hi);
-                                if (key != 0ull) atomicMax(&s_best[grp][8 * hh + jj], key);
+                            gm0 = fmaxf(gm0, __shfl_xor_sync(0xFFFFFFFFu, gm0, 1));
+                            gm1 = fmaxf(gm1, __shfl_xor_sync(0xFFFFFFFFu, gm1, 1));
+                            // the table bounds the group's largest variate by the top byte of its word
+                            const bool T0 = lb0 < INFINITY && __fadd_rn(gm0, gtab[W0 >> 24]) >= lb0;
+                            const bool T1 = lb1 < INFINITY && __fadd_rn(gm1, gtab[W1 >> 24]) >= lb1;
+                            // the even lane of each pair reports its group; the warp draws them one by one
+                            uint32_t m0 = __ballot_sync(0xFFFFFFFFu, T0 && (q & 1) == 0);
+                            uint32_t m1 = __ballot_sync(0xFFFFFFFFu, T1 && (q & 1) == 0);
+                            const int row0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32);
+                            while ((m0 | m1) != 0u) {
+                                const bool second = m0 == 0u;
+                                const int src = __ffs(second ? m1 : m0) - 1;
+                                if (second) m1 &= m1 - 1u; else m0 &= m0 - 1u;
+                                const int j = (src >> 2) + (second ? 8 : 0);           // request in the chunk
+                                const uint32_t Wg = __shfl_sync(0xFFFFFFFFu, second ? W1 : W0, src);
+                                group_candidates(a, c * kChunk + j, i, taddr + static_cast<uint32_t>(j), row0,
+                                                 static_cast<uint32_t>(src >> 1) & 1u, Wg, s_lb[grp][j], &s_best[grp][j]);
                             }
                         }
                     }

@@ -17,13 +17,20 @@ verification uses a seeded uniform ("DSpark implementation and evaluation"
 
   key      = (lo32(seed), hi32(seed))
   counter  = (j, b, (stream << 16) | i, offset)       offset < 2**32
-  stream 0 = draft noise, high halves (b = request, i = draft step)
-  stream 3 = draft noise, low halves  (same counters)
-             element v takes 16 bits from each stream, from counter j = v >> 3:
-             word (v & 7) >> 1, bits 0-15 for even v and 16-31 for odd v;
-             its 32-bit word is (high half << 16) | low half
-  (the split lets a sampler rule an element out from its high half alone,
-  since u, and so g, is increasing in the word)
+  stream 0 = draft noise, group words (b = request, i = draft step)
+  stream 3 = draft noise, element words (same b, i)
+             entries come in groups of 16 (G = v >> 4, position k = v & 15);
+             the group word is word G & 3 of counter j = G >> 2 of stream 0:
+             its bits 0-3 give the position p of the group's largest variate,
+             its uniform u0 the group's smallest exponential E_min = -log(u0) / 16;
+             entry k != p takes word k & 3 of counter j = (G << 2) | (k >> 2)
+             of stream 3 and E_k = E_min - log(u_k); E_p = E_min; g = -log(E).
+             The smallest of 16 independent Exp(1) variates is Exp(16)
+             distributed, its position uniform, and the others exceed it by
+             independent Exp(1) amounts, so the 16 E's are independent Exp(1)
+             and the g's independent standard Gumbels; -log(E_min), which is
+             u0's Gumbel variate + log 16, bounds every g of the group, so a
+             sampler can rule a whole group out from one word
   stream 1 = verify accept uniform   (i = draft position k, j = 0, word 0)
   stream 2 = verify resample         (i = position, j = 0, words 0 and 1)
   stream 4 = from-logits resample    (i = position, j = v >> 2, word v & 3 of element v)
@@ -95,26 +102,41 @@ def gumbel_from_word(w) -> np.ndarray:
     return -np.log(-np.log(u))
 
 
-def draft_halfword(seed: int, offset: int, b, i, v, stream: int) -> np.ndarray:
-    """16-bit piece of element v's draft word from `stream` (0: high half, 3: low half)."""
-    v = np.asarray(v, dtype=np.uint64)
-    words = philox_words(seed, offset, v >> np.uint64(3), b, stream, i)
-    sel = ((v & np.uint64(7)) >> np.uint64(1)).astype(np.int64)
-    w = np.where(sel == 0, words[0], np.where(sel == 1, words[1],
-                 np.where(sel == 2, words[2], words[3])))
-    shift = (v & np.uint64(1)) * np.uint64(16)
-    return (w >> shift) & np.uint64(0xFFFF)
+GROUP = 16                   # draft-noise entries per group word
 
 
-def draft_word(seed: int, offset: int, b, i, v) -> np.ndarray:
-    """32-bit draft-noise word of element v: (high half << 16) | low half."""
-    hi = draft_halfword(seed, offset, b, i, v, STREAM_GUMBEL)
-    lo = draft_halfword(seed, offset, b, i, v, STREAM_GUMBEL_LO)
-    return (hi << np.uint64(16)) | lo
+def _select_word(words, idx):
+    """words: the 4 output arrays of philox_words; idx: which word (0..3), broadcastable."""
+    idx = np.asarray(idx)
+    return np.where(idx == 0, words[0], np.where(idx == 1, words[1], np.where(idx == 2, words[2], words[3])))
+
+
+def draft_group_words(seed: int, offset: int, b, i, G) -> np.ndarray:
+    """Group word of draft-noise group G: word G & 3 of counter (G >> 2, b, (0 << 16) | i, offset)."""
+    G = np.asarray(G, dtype=np.uint64)
+    words = philox_words(seed, offset, G >> np.uint64(2), b, STREAM_GUMBEL, i)
+    return _select_word(words, (G & np.uint64(3)).astype(np.int64))
 
 
 def draft_gumbel(seed: int, offset: int, b, i, V: int) -> np.ndarray:
-    """Gumbel noise g[b, v] (float64) of draft step i for requests b (array) over v in [0, V)."""
+    """Gumbel noise g[b, v] (float64) of draft step i for requests b (array) over v in [0, V).
+
+    Groups of 16 entries: the group word gives the position p of the group's largest variate
+    (its bits 0-3) and the group's smallest exponential E_min = -log(u0) / 16; every other
+    entry k adds its own exponential, E_k = E_min - log(u_k), from word k & 3 of the stream-3
+    counter (G << 2) | (k >> 2); g = -log(E).
+    """
     b = np.asarray(b, dtype=np.uint64).reshape(-1, 1)
-    v = np.arange(V, dtype=np.uint64).reshape(1, -1)
-    return gumbel_from_word(draft_word(seed, offset, b, i, v))
+    n_groups = (V + GROUP - 1) // GROUP
+    G = np.arange(n_groups, dtype=np.uint64).reshape(1, -1)
+    W = draft_group_words(seed, offset, b, i, G)                           # [nb, n_groups]
+    p = (W & np.uint64(15)).astype(np.int64)
+    e_min = -np.log(uniform_from_word(W)) / GROUP
+    v = np.arange(n_groups * GROUP, dtype=np.uint64).reshape(1, -1)
+    k = v & np.uint64(15)
+    Gv = (v >> np.uint64(4)).astype(np.int64).ravel()
+    ew = _select_word(philox_words(seed, offset, ((v >> np.uint64(4)) << np.uint64(2)) | (k >> np.uint64(2)),
+                                   b, STREAM_GUMBEL_LO, i), (k & np.uint64(3)).astype(np.int64))
+    E = e_min[:, Gv] - np.log(uniform_from_word(ew))
+    E = np.where(k.astype(np.int64) == p[:, Gv], e_min[:, Gv], E)
+    return -np.log(E)[:, :V]

@@ -128,30 +128,63 @@ def test_gumbel_distribution_and_bounds():
     assert 16.63 < gmax < 16.64 and -2.82 < gmin < -2.81
 
 
-def test_draft_gumbel_word_layout():
-    # element v: high half from stream 0 and low half from stream 3, both from counter
-    # v >> 3, word (v & 7) >> 1, bits 0-15 (even v) or 16-31 (odd v)
-    g = draft_gumbel(3, 4, np.array([2]), 5, 20)
-    for v in range(20):
-        hw = philox_words(3, 4, v >> 3, 2, 0, 5)[(v & 7) >> 1]
-        lw = philox_words(3, 4, v >> 3, 2, 3, 5)[(v & 7) >> 1]
-        sh = 16 * (v & 1)
-        word = (((int(hw) >> sh) & 0xFFFF) << 16) | ((int(lw) >> sh) & 0xFFFF)
-        assert g[0, v] == gumbel_from_word(np.uint64(word))
+def test_draft_gumbel_layout_of_a_few_entries():
+    # entry v of group G = v >> 4 at position k = v & 15: group word G & 3 of stream-0 counter
+    # G >> 2 (position p in bits 0-3, E_min = -log(u0) / 16); k != p adds -log(u) of word k & 3
+    # of stream-3 counter (G << 2) | (k >> 2)
+    g = draft_gumbel(3, 4, np.array([2]), 5, 70)
+    for v in (0, 1, 15, 16, 37, 63, 64, 69):
+        G, k = v >> 4, v & 15
+        W = int(philox_words(3, 4, G >> 2, 2, 0, 5)[G & 3])
+        e_min = -np.log(uniform_from_word(np.uint64(W))) / 16
+        if k == (W & 15):
+            E = e_min
+        else:
+            w = philox_words(3, 4, (G << 2) | (k >> 2), 2, 3, 5)[k & 3]
+            E = e_min - np.log(uniform_from_word(w))
+        assert g[0, v] == -np.log(E)
 
 
-def test_draft_words_uniform_and_halves_independent():
-    from oracle.philox import draft_word, draft_halfword
-    v = np.arange(200_000, dtype=np.uint64)
-    w = draft_word(9, 1, 4, 2, v)
-    counts, _ = np.histogram((w >> np.uint64(16)).astype(np.float64), bins=64, range=(0, 65536))
+def _noise(n_req=8, V=16 * 4096, seed=9, i=2):
+    return draft_gumbel(seed, 1, np.arange(n_req), i, V)
+
+
+def test_draft_noise_marginal_is_standard_gumbel():
+    g = _noise().ravel()
+    assert stats.kstest(g, stats.gumbel_r.cdf).pvalue > 0.01
+    # every entry lies below the largest group variate: E_min >= -log(1 - 2^-24) / 16
+    assert g.max() <= -np.log(-np.log(1.0 - 2.0 ** -24) / 16)
+
+
+def test_draft_noise_group_maximum_is_gumbel_plus_log16_at_a_uniform_position():
+    # the largest of 16 independent standard Gumbels is distributed as Gumbel + log 16, and
+    # falls on each of the 16 positions with probability 1/16
+    g = _noise().reshape(-1, 16)
+    top = g.max(axis=1)
+    assert stats.kstest(top - np.log(16.0), stats.gumbel_r.cdf).pvalue > 0.01
+    counts = np.bincount(g.argmax(axis=1), minlength=16)
     assert stats.chisquare(counts).pvalue > 0.01
-    counts, _ = np.histogram((w & np.uint64(0xFFFF)).astype(np.float64), bins=64, range=(0, 65536))
-    assert stats.chisquare(counts).pvalue > 0.01
-    hi = draft_halfword(9, 1, 4, 2, v, 0)
-    lo = draft_halfword(9, 1, 4, 2, v, 3)
-    joint = np.histogram2d((hi >> np.uint64(13)).astype(float), (lo >> np.uint64(13)).astype(float),
-                           bins=8, range=[[0, 8], [0, 8]])[0].ravel()
+    # the smallest is distributed as the smallest of 16 Gumbels: P(min <= x) = 1 - (1 - F(x))^16
+    low = g.min(axis=1)
+    assert stats.kstest(low, lambda x: 1.0 - (1.0 - stats.gumbel_r.cdf(x)) ** 16).pvalue > 0.01
+
+
+@pytest.mark.parametrize("k1,k2", [(0, 1), (3, 11), (0, 15), (15, 16)])
+def test_draft_noise_entries_are_independent(k1, k2):
+    # entries of one group, and the last entry of a group with the first of the next: the joint
+    # law of (F(g1), F(g2)) is uniform on the unit square (F = standard Gumbel cdf)
+    g = _noise(n_req=16)
+    a = stats.gumbel_r.cdf(g[:, k1::32].ravel())
+    b = stats.gumbel_r.cdf(g[:, k2::32].ravel())
+    joint = np.histogram2d(a, b, bins=8, range=[[0, 1], [0, 1]])[0].ravel()
     assert stats.chisquare(joint).pvalue > 0.01
-    # neighbouring elements get different words (no sharing of halves)
-    assert len(np.unique(w[:4096])) == 4096
+    assert abs(np.corrcoef(a, b)[0, 1]) < 0.01
+
+
+def test_draft_noise_depends_on_request_step_and_offset():
+    base = draft_gumbel(9, 1, np.array([4]), 2, 256)
+    for other in (draft_gumbel(9, 1, np.array([5]), 2, 256), draft_gumbel(9, 1, np.array([4]), 3, 256),
+                  draft_gumbel(9, 2, np.array([4]), 2, 256), draft_gumbel(10, 1, np.array([4]), 2, 256)):
+        assert np.mean(base == other) < 0.01
+    # a prefix of the vocabulary draws the same values
+    np.testing.assert_array_equal(draft_gumbel(9, 1, np.array([4]), 2, 100), base[:, :100])
