@@ -468,14 +468,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                         // lane (jj, q) takes rows 8q..8q+7 of requests jj and 8 + jj; lanes q and
                         // q ^ 1 hold the two halves of one 16-entry noise group, whose group word
                         // bounds every variate of the group.  Lane l draws the stream-0 counter of
-                        // the warp's two groups for request l & 15 of the chunk and passes the
-                        // two group words to the lanes that hold those groups.
+                        // the warp's two groups for request l & 15 of the chunk (lanes 16-31 one
+                        // tile ahead) and passes the group words to the lanes that hold them.
                         const float lb0 = s_lb[grp][jj], lb1 = s_lb[grp][8 + jj];
                         const float m0 = want_lse && b0 < a.B ? s_zmax[b0] : -INFINITY;
                         const float m1 = want_lse && b1 < a.B ? s_zmax[b1] : -INFINITY;
                         const uint32_t pw = (quad * 2u) & 3u;            // word of the warp's first group
                         const int bsrc = c * kChunk + static_cast<int>(lane & 15u);
                         const bool draw = any && s_lb[grp][lane & 15u] < INFINITY;
+                        uint32_t wa = 0, wb = 0;
                         for (int tl = 0; tl < nt; ++tl) {
                             const int v0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32) + 8 * q;
                             const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
@@ -494,15 +495,22 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                     }
                                 }
                             }
-                            uint32_t wa = 0, wb = 0;
-                            if (draw) {
-                                const uint4 w = philox_at(a.seed, a.offset, group_counter(tile_lo + tl, quad),
-                                                          static_cast<uint32_t>(bsrc), kStreamGumbel, static_cast<uint32_t>(i));
-                                wa = word_of(w, pw);
-                                wb = word_of(w, pw + 1u);
+                            if ((tl & 1) == 0) {
+                                // one Philox round serves two tiles: lanes 0-15 draw this tile's group
+                                // words, lanes 16-31 the next tile's
+                                const int td = tl + static_cast<int>(lane >> 4);
+                                wa = 0;
+                                wb = 0;
+                                if (draw && td < nt) {
+                                    const uint4 w = philox_at(a.seed, a.offset, group_counter(tile_lo + td, quad),
+                                                              static_cast<uint32_t>(bsrc), kStreamGumbel, static_cast<uint32_t>(i));
+                                    wa = word_of(w, pw);
+                                    wb = word_of(w, pw + 1u);
+                                }
                             }
-                            const uint32_t a0 = __shfl_sync(0xFFFFFFFFu, wa, jj), c0 = __shfl_sync(0xFFFFFFFFu, wb, jj);
-                            const uint32_t a1 = __shfl_sync(0xFFFFFFFFu, wa, 8 + jj), c1 = __shfl_sync(0xFFFFFFFFu, wb, 8 + jj);
+                            const int wo = (tl & 1) ? 16 : 0;
+                            const uint32_t a0 = __shfl_sync(0xFFFFFFFFu, wa, wo + jj), c0 = __shfl_sync(0xFFFFFFFFu, wb, wo + jj);
+                            const uint32_t a1 = __shfl_sync(0xFFFFFFFFu, wa, wo + 8 + jj), c1 = __shfl_sync(0xFFFFFFFFu, wb, wo + 8 + jj);
                             const uint32_t W0 = (q >> 1) ? c0 : a0, W1 = (q >> 1) ? c1 : a1;
                             // the group's largest z (entries past V left out), from both halves
                             float gm0 = -INFINITY, gm1 = -INFINITY;
@@ -588,10 +596,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     }
 }
 
-// Ring depths: the w2 ring gets what the E operand leaves (deeper rings measured no faster).
+// Ring depths: the w2 ring gets what the E operand leaves (the w2 stream from L2 is bound by the
+// bytes in flight, and a deeper ring lets the next step's first tiles land during pass 2).
 void tc_rings(int B_pad, int r, int* w2_stages, int* l_stages) {
     const bool small_e = static_cast<size_t>(B_pad) * r * 2 <= 32 * 1024;
-    *w2_stages = small_e ? 4 : 2;
+    *w2_stages = small_e ? 6 : 4;
     *l_stages = 2;
 }
 
