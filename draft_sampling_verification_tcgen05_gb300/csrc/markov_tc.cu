@@ -53,9 +53,12 @@ constexpr int kW2Stages = 6;                    // upper bound of the w2 ring (t
 constexpr int kLStages = 3;                      // upper bound per epilogue group; the launcher picks 2 or 3
 constexpr int kTileV = 128;
 constexpr int kChunk = 16;                       // requests per epilogue chunk
+constexpr int kInterleave = 1;                   // tiles whose bias MMAs are issued k-block by k-block together
+constexpr int kKbPerStage = 2;                   // 64-wide K blocks of w2 per ring stage
 constexpr int kMaxLocalTiles = 32;
 constexpr int kZtPitch = 36;                     // floats per request row of the transpose buffer (no bank conflicts)
-constexpr uint32_t kW2StageBytes = kTileV * 128;             // 128 rows x 64 bf16
+constexpr uint32_t kW2BoxBytes = kTileV * 128;               // 128 rows x 64 bf16
+constexpr uint32_t kW2StageBytes = kKbPerStage * kW2BoxBytes;
 constexpr uint32_t kLStageBytes = kTileV * kChunk * 4;       // 16 requests x 128 fp32
 constexpr uint32_t kGtabBytes = 256 * 4;                     // bound table of the group words
 constexpr uint32_t kBarStep = 1;
@@ -162,6 +165,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     const int n_chunks = Bp / kChunk;
     const int rounds = (n_chunks + kGroups - 1) / kGroups;
     const int kblocks = a.r / 64;
+    const int kstages = (kblocks + kKbPerStage - 1) / kKbPerStage;      // ring stages per tile
     const uint32_t e_kb_bytes = static_cast<uint32_t>(Bp) * 128u;
     int tile_lo, tile_hi;
     tile_range(t, tile_lo, tile_hi);
@@ -226,17 +230,24 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
             int ws = 0;
             uint32_t wph = 0;
             bool ok = true;
+            // (in the order the MMA warp consumes them: k-block by k-block across each group
+            // of kInterleave tiles)
             for (int i = 0; i < a.N && ok; ++i) {
-                for (int tl = 0; tl < nt && ok; ++tl) {
-                    const int v0 = (tile_lo + tl) * kTileV;
-                    for (int kb = 0; kb < kblocks; ++kb) {
-                        if (!mbar_wait(&bar_w2_empty[ws], wph ^ 1u, a.ws, a.timeout_ns, kWaitProducer)) {
-                            ok = false;
-                            break;
+                for (int t0 = 0; t0 < nt && ok; t0 += kInterleave) {
+                    const int gsz = min(kInterleave, nt - t0);
+                    for (int ks = 0; ks < kstages && ok; ++ks) {
+                        const int nkb = min(kKbPerStage, kblocks - ks * kKbPerStage);
+                        for (int u = 0; u < gsz; ++u) {
+                            if (!mbar_wait(&bar_w2_empty[ws], wph ^ 1u, a.ws, a.timeout_ns, kWaitProducer)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&bar_w2_full[ws], static_cast<uint32_t>(nkb) * kW2BoxBytes);
+                            for (int j = 0; j < nkb; ++j)
+                                tma_load_2d(w2s + ws * kW2StageBytes + j * kW2BoxBytes, &tmW2, (ks * kKbPerStage + j) * 64,
+                                            (tile_lo + t0 + u) * kTileV, &bar_w2_full[ws], pol_keep);
+                            if (++ws == t.w2_stages) { ws = 0; wph ^= 1u; }
                         }
-                        mbar_arrive_expect_tx(&bar_w2_full[ws], kW2StageBytes);
-                        tma_load_2d(w2s + ws * kW2StageBytes, &tmW2, kb * 64, v0, &bar_w2_full[ws], pol_keep);
-                        if (++ws == t.w2_stages) { ws = 0; wph ^= 1u; }
                     }
                 }
             }
@@ -337,24 +348,34 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 // ---- bias for every local tile: D[tile] = w2_tile (128 x r) . E^T (r x Bp) ----
                 if (lane == 0 && !dead) {
                     tc_fence_after();
-                    for (int tl = 0; tl < nt && !dead; ++tl) {
-                        const uint32_t d = tmem + static_cast<uint32_t>(tl * Bp);
-                        for (int kb = 0; kb < kblocks; ++kb) {
-                            if (!mbar_wait(&bar_w2_full[w2st], w2ph, a.ws, a.timeout_ns, kWaitMma)) {
-                                dead = true;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t a_addr = smem_u32(w2s + w2st * kW2StageBytes);
-                            const uint32_t b_addr = smem_u32(Es + kb * e_kb_bytes);
+                    // the k-blocks of kInterleave tiles alternate, so their accumulation chains
+                    // (independent TMEM columns) overlap in the tensor pipe
+                    for (int t0 = 0; t0 < nt && !dead; t0 += kInterleave) {
+                        const int gsz = min(kInterleave, nt - t0);
+                        for (int ks = 0; ks < kstages && !dead; ++ks) {
+                            const int nkb = min(kKbPerStage, kblocks - ks * kKbPerStage);
+                            for (int u = 0; u < gsz; ++u) {
+                                if (!mbar_wait(&bar_w2_full[w2st], w2ph, a.ws, a.timeout_ns, kWaitMma)) {
+                                    dead = true;
+                                    break;
+                                }
+                                tc_fence_after();
+                                const uint32_t d = tmem + static_cast<uint32_t>((t0 + u) * Bp);
+                                for (int j = 0; j < nkb; ++j) {
+                                    const int kb = ks * kKbPerStage + j;
+                                    const uint32_t a_addr = smem_u32(w2s + w2st * kW2StageBytes + j * kW2BoxBytes);
+                                    const uint32_t b_addr = smem_u32(Es + kb * e_kb_bytes);
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                mma_issue<false>(d, sw128_kmajor_desc(a_addr + 32 * k),
-                                                 sw128_kmajor_desc(b_addr + 32 * k), idesc, (kb | k) != 0 ? 1u : 0u);
-                            mma_commit(&bar_w2_empty[w2st]);
-                            if (++w2st == t.w2_stages) { w2st = 0; w2ph ^= 1u; }
+                                    for (int k = 0; k < 4; ++k)
+                                        mma_issue<false>(d, sw128_kmajor_desc(a_addr + 32 * k),
+                                                         sw128_kmajor_desc(b_addr + 32 * k), idesc, (kb | k) != 0 ? 1u : 0u);
+                                }
+                                mma_commit(&bar_w2_empty[w2st]);
+                                if (++w2st == t.w2_stages) { w2st = 0; w2ph ^= 1u; }
+                            }
                         }
-                        if (!dead) mma_commit(&bar_tile[tl]);
+                        if (!dead)
+                            for (int u = 0; u < gsz; ++u) mma_commit(&bar_tile[t0 + u]);
                     }
                 }
                 __syncwarp();
@@ -600,7 +621,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
 // bytes in flight, and a deeper ring lets the next step's first tiles land during pass 2).
 void tc_rings(int B_pad, int r, int* w2_stages, int* l_stages) {
     const bool small_e = static_cast<size_t>(B_pad) * r * 2 <= 32 * 1024;
-    *w2_stages = small_e ? 6 : 4;
+    *w2_stages = (small_e ? 6 : 4) / kKbPerStage;
     *l_stages = 2;
 }
 
