@@ -314,6 +314,8 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         // one MMA covers all B_pad requests: measured on sm_103a, a tcgen05.mma of
         // M=128, K=16 costs about the same time for N=32, 64 or 256, so the widest N wins
         const uint32_t idesc = mma_idesc(128, Bp, false);
+        const uint64_t dw2 = sw128_kmajor_desc(smem_u32(w2s));    // ring base (every offset keeps it below 256 KB)
+        const uint64_t dE = sw128_kmajor_desc(smem_u32(Es));
         const int chunks16 = a.r / 8;                         // 16-byte pieces of a w1 row
 
         for (int i = 0; i < a.N && alive; ++i) {
@@ -361,14 +363,15 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 }
                                 tc_fence_after();
                                 const uint32_t d = tmem + static_cast<uint32_t>((t0 + u) * Bp);
+                                // descriptors differ only in the start-address field (address >> 4)
+                                const uint64_t da = dw2 + ((static_cast<uint32_t>(w2st) * kW2StageBytes) >> 4);
                                 for (int j = 0; j < nkb; ++j) {
                                     const int kb = ks * kKbPerStage + j;
-                                    const uint32_t a_addr = smem_u32(w2s + w2st * kW2StageBytes + j * kW2BoxBytes);
-                                    const uint32_t b_addr = smem_u32(Es + kb * e_kb_bytes);
+                                    const uint64_t dja = da + (static_cast<uint32_t>(j) * kW2BoxBytes >> 4);
+                                    const uint64_t djb = dE + (static_cast<uint32_t>(kb) * e_kb_bytes >> 4);
 #pragma unroll
                                     for (int k = 0; k < 4; ++k)
-                                        mma_issue<false>(d, sw128_kmajor_desc(a_addr + 32 * k),
-                                                         sw128_kmajor_desc(b_addr + 32 * k), idesc, (kb | k) != 0 ? 1u : 0u);
+                                        mma_issue<false>(d, dja + 2 * k, djb + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
                                 }
                                 mma_commit(&bar_w2_empty[w2st]);
                                 if (++w2st == t.w2_stages) { w2st = 0; w2ph ^= 1u; }
