@@ -10,7 +10,7 @@ from the pages that define the method, each function citing its passage:
 
   * "DSpark implementation and evaluation" (ggaaooppeenngg.github.io):
     §2.2 Sequential Markov Sampling, §3 Markov Head structure, §4 draft step,
-    §5 reduced draft vocabulary.
+    §5 reduced draft vocabulary and verification with the draft's Gumbel noise.
   * "Speculative decoding: from zero to DSpark" (bittide.aicompass.dev):
     §2 the loop and its lossless property, §6 scheduling by expected
     throughput and the calibrated confidence head, §7 running in a real engine.
@@ -34,6 +34,7 @@ from .greedy import verify_greedy, row_argmax
 from .confidence import confidence
 from .reduced_vocab import map_to_target, markov_sample_reduced
 from .verify_logits import verify_from_logits, draft_distributions, draft_lse, residual_gumbel
+from .verify_gumbel import verify_gumbel, target_gumbel_tokens
 
 __all__ = [
     "philox4x32_10", "philox_words", "uniform_from_word", "gumbel_from_word",
@@ -42,4 +43,5 @@ __all__ = [
     "schedule", "survival_chain",
     "verify_greedy", "row_argmax", "confidence", "map_to_target", "markov_sample_reduced",
     "verify_from_logits", "draft_distributions", "draft_lse", "residual_gumbel",
+    "verify_gumbel", "target_gumbel_tokens",
 ]
