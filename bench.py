@@ -360,7 +360,7 @@ def run_gpu(args):
         e2e = {"value": job_throughput(M, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
 
-    # ---------------- kernels beyond the step, timed on their own ----------------
+    # ---------------- the library's other entry points, timed on their own ----------------
     # greedy verification of the step's draft tokens against the same target rows (all rows
     # k <= gamma are read)
     ws_g2 = ds.Workspace(ds.OP_VERIFY_GREEDY, B, N, device=dev)
@@ -457,6 +457,25 @@ def run_gpu(args):
     # and Markov rows are read only at the few candidate entries
     vlog_rows = int((l_nacc.long() + 2).sum().item())
     vlog_bytes = vlog_rows * V * 4
+    # verification with the draft's own Gumbel noise on the same target logits (the draft's
+    # temperature for the target, the sampler's seed and offset); all rows k <= gamma are read
+    ws_gu = ds.Workspace(ds.OP_VERIFY_GUMBEL, B, N, device=dev)
+    gu_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    gu_nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    gu_args = (t_logits, temp, tok, None, seed_draft, 0)
+    for _ in range(3):
+        ds.dspark_verify_gumbel(*gu_args, out_tokens=gu_out, num_accepted=gu_nacc, workspace=ws_gu)
+    gu_ms = []
+    for k in range(20):
+        flush_l2(k)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ds.dspark_verify_gumbel(*gu_args, out_tokens=gu_out, num_accepted=gu_nacc, workspace=ws_gu)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        gu_ms.append(e0.elapsed_time(e1))
+    gumbel_ms = float(np.median(gu_ms))
+    gumbel_bytes = B * (N + 1) * V * 4
     del ws_l, ws_m2, t_logits
 
     # ---------------- roofline of the dominant kernel ----------------
@@ -521,6 +540,12 @@ def run_gpu(args):
                           "target": "the draft's base-logit rows + N(0, s^2), s in {0.3, 1, 3} per request",
                           "note": "median of 20 calls (2 kernels), L2 flushed, outside the step; bytes = "
                                   "target rows k <= k* plus row k* again, from the measured k*"},
+        "verify_gumbel": {"ms": gumbel_ms, "bound": "hbm", "algorithmic_bytes": gumbel_bytes,
+                          "achieved": gumbel_bytes / (gumbel_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                          "frac": gumbel_bytes / (gumbel_ms / 1e3) / 1e9 / hbm_peak,
+                          "accepted_mean": float(gu_nacc.float().mean().item()),
+                          "note": "median of 20 launches, L2 flushed, outside the step; target logits as for "
+                                  "verify_logits, the draft's temperature and noise"},
         "verify_greedy": {"ms": greedy_ms, "bound": "hbm", "algorithmic_bytes": B * (N + 1) * V * 4,
                           "achieved": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9, "peak": hbm_peak,
                           "unit": "GB/s", "frac": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9 / hbm_peak,
@@ -529,7 +554,7 @@ def run_gpu(args):
                             "achieved": markov_bytes / (kernel_ms[1] / 1e3) / 1e9, "peak": hbm_peak,
                             "unit": "GB/s", "frac": markov_bytes / (kernel_ms[1] / 1e3) / 1e9 / hbm_peak},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,           # GEMM, Markov sampler, verify decide + stream, schedule
         "step_launch": "one CUDA graph replay per step" if graph is not None else "four eager calls per step",
         "kernel_ms_note": "per-kernel CUDA-event times from an eager pass over the same K steps",
         "clocks": clk.summary(),

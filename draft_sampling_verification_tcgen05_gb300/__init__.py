@@ -14,7 +14,8 @@ import os
 
 __all__ = [
     "DSparkError", "lib", "Workspace", "OP_DRAFT_LOGITS", "OP_MARKOV_SAMPLE", "OP_VERIFY",
-    "OP_SCHEDULE", "OP_VERIFY_GREEDY", "OP_CONFIDENCE", "OP_VERIFY_LOGITS", "dspark_workspace_size",
+    "OP_SCHEDULE", "OP_VERIFY_GREEDY", "OP_CONFIDENCE", "OP_VERIFY_LOGITS", "OP_VERIFY_GUMBEL",
+    "dspark_workspace_size", "dspark_verify_gumbel",
     "dspark_verify_greedy", "dspark_verify_logits",
     "dspark_confidence", "dspark_markov_sample_reduced", "D2T_INDEX", "D2T_OFFSET", "dspark_draft_logits", "dspark_markov_sample",
     "dspark_verify", "dspark_schedule", "dspark_read_status", "dspark_status_string",
@@ -26,6 +27,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdspark.s
 
 OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE, OP_VERIFY_GREEDY, OP_CONFIDENCE = 0, 1, 2, 3, 4, 5
 OP_VERIFY_LOGITS = 6
+OP_VERIFY_GUMBEL = 7
 F32, BF16 = 0, 1
 D2T_INDEX, D2T_OFFSET = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NUMERIC, ERR_INPUT_RANGE = range(7)
@@ -59,6 +61,7 @@ def lib() -> ctypes.CDLL:
                                                vp, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify.argtypes = [vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify_greedy.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.dspark_verify_gumbel.argtypes = [vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify_logits.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, u64, u64, i32, i32, i32,
                                        vp, vp, vp, sz, vp]
     L.dspark_confidence.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, ctypes.c_float, vp, i32, i32, i32, i32, i32,
@@ -237,6 +240,32 @@ def dspark_verify(p_target, p_draft, draft_tokens, lengths, seed: int, offset: i
     _check(lib().dspark_verify(_ptr(p_target), _ptr(p_draft), _ptr(draft_tokens), _ptr(lengths),
                                seed, offset, B, gamma, V, _ptr(out_tokens), _ptr(num_accepted),
                                ws.ptr, ws.nbytes, _stream(stream)), "dspark_verify")
+    return out_tokens, num_accepted
+
+
+def dspark_verify_gumbel(target_logits, temperature, draft_tokens, lengths, seed: int, offset: int,
+                         out_tokens=None, num_accepted=None, workspace=None, stream=None):
+    """Verification with the draft's Gumbel noise (the draft sampler's seed and offset); returns
+    (out_tokens [B, gamma+1], num_accepted [B])."""
+    torch = _torch()
+    _need(target_logits, "target_logits", (torch.float32,), 3)
+    _need(temperature, "temperature", (torch.float32,), 1)
+    _need(draft_tokens, "draft_tokens", (torch.int32,), 2)
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    if tuple(draft_tokens.shape) != (B, gamma) or temperature.shape[0] != B:
+        raise ValueError("shapes must be target_logits [B, gamma+1, V], temperature [B], tokens [B, gamma]")
+    if lengths is not None:
+        _need(lengths, "lengths", (torch.int32,), 1)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=target_logits.device)
+    if num_accepted is None:
+        num_accepted = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    ws = _ws(workspace, OP_VERIFY_GUMBEL, B, gamma, 0, 0, target_logits.device)
+    _check(lib().dspark_verify_gumbel(_ptr(target_logits), _ptr(temperature), _ptr(draft_tokens), _ptr(lengths),
+                                      seed, offset, B, gamma, V, _ptr(out_tokens), _ptr(num_accepted), ws.ptr,
+                                      ws.nbytes, _stream(stream)),
+           "dspark_verify_gumbel")
     return out_tokens, num_accepted
 
 

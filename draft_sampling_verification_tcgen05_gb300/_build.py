@@ -15,7 +15,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libdspark.so")
-SOURCES = ["api.cu", "draft_logits.cu", "markov_sample.cu", "markov_tc.cu", "verify.cu", "verify_greedy.cu", "verify_logits.cu", "confidence.cu", "schedule.cu"]
+SOURCES = ["api.cu", "draft_logits.cu", "markov_sample.cu", "markov_tc.cu", "verify.cu", "verify_greedy.cu", "verify_gumbel.cu", "verify_logits.cu", "confidence.cu", "schedule.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

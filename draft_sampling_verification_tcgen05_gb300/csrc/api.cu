@@ -178,6 +178,8 @@ size_t dspark_workspace_size(int op, int B, int N, int V, int r) {
             return sizeof(WsHeader);
         case DSPARK_OP_VERIFY_LOGITS:
             return verify_logits_workspace_bytes(B, N, V, r);
+        case DSPARK_OP_VERIFY_GUMBEL:
+            return verify_gumbel_workspace_bytes(B, N);
         default:
             return 0;
     }
@@ -291,6 +293,26 @@ dspark_status dspark_verify_greedy(const float* target, const int32_t* draft_tok
     if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
     return launch_verify_greedy(target, draft_tokens, lengths, B, gamma, V, out_tokens, num_accepted, workspace,
                                 static_cast<cudaStream_t>(stream), dev);
+}
+
+dspark_status dspark_verify_gumbel(const float* target_logits, const float* temperature,
+                                   const int32_t* draft_tokens, const int32_t* lengths, uint64_t seed,
+                                   uint64_t offset, int B, int gamma, int V, int32_t* out_tokens,
+                                   int32_t* num_accepted, void* workspace, size_t ws_bytes, void* stream) {
+    g_error[0] = '\0';
+    DSPARK_REQUIRE(target_logits && temperature && draft_tokens && out_tokens && num_accepted,
+                   "verify_gumbel: null pointer");
+    DSPARK_REQUIRE(B >= 1 && B <= 65535 && gamma >= 1 && gamma <= 65535 && V >= 1 && V < (1 << 27),
+                   "verify_gumbel: bad sizes (B=%d gamma=%d V=%d)", B, gamma, V);
+    DSPARK_REQUIRE(offset < (1ull << 32), "verify_gumbel: offset must be below 2^32");
+    DSPARK_REQUIRE(aligned(target_logits, 16), "verify_gumbel: target_logits must be 16-byte aligned");
+    if (bad_ws(workspace, ws_bytes, dspark_workspace_size(DSPARK_OP_VERIFY_GUMBEL, B, gamma, 0, 0)))
+        return DSPARK_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
+    return launch_verify_gumbel(target_logits, temperature, draft_tokens, lengths, seed, static_cast<uint32_t>(offset),
+                                B, gamma, V, out_tokens, num_accepted, workspace, static_cast<cudaStream_t>(stream),
+                                dev);
 }
 
 dspark_status dspark_verify_logits(const float* target_logits, const float* target_temperature,

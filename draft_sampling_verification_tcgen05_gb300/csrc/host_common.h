@@ -53,6 +53,11 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
 
 size_t verify_workspace_bytes(int B, int V);
 size_t verify_greedy_workspace_bytes(int B, int gamma);
+size_t verify_gumbel_workspace_bytes(int B, int gamma);
+dspark_status launch_verify_gumbel(const float* target_logits, const float* temperature, const int32_t* draft_tokens,
+                                   const int32_t* lengths, uint64_t seed, uint32_t offset, int B, int gamma, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted, void* ws, cudaStream_t stream,
+                                   const DeviceInfo& dev);
 dspark_status launch_confidence(const void* hidden, dspark_dtype hdtype, const void* w1, dspark_dtype wdtype,
                                 const int32_t* anchor, const int32_t* draft_tokens, const float* w_h,
                                 const float* w_e, float beta, const float* tau, int B, int N, int H, int V, int r,

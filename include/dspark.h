@@ -70,7 +70,8 @@ typedef enum {
     DSPARK_OP_SCHEDULE = 3,
     DSPARK_OP_VERIFY_GREEDY = 4,
     DSPARK_OP_CONFIDENCE = 5,
-    DSPARK_OP_VERIFY_LOGITS = 6
+    DSPARK_OP_VERIFY_LOGITS = 6,
+    DSPARK_OP_VERIFY_GUMBEL = 7
 } dspark_op;
 
 /* Device status-word bits (OR-ed by kernels; read with dspark_read_status). */
@@ -89,6 +90,7 @@ typedef enum {
  *   DSPARK_OP_VERIFY_GREEDY grows with B*(N+1) (row argmax keys); N = gamma
  *   DSPARK_OP_CONFIDENCE    256 (the status word)
  *   DSPARK_OP_VERIFY_LOGITS grows with B*V/2048 (normaliser partials); N = gamma
+ *   DSPARK_OP_VERIFY_GUMBEL grows with B*(N+1) (row keys); N = gamma
  * Returns 0 for an unknown op or negative sizes.
  */
 DSPARK_API size_t dspark_workspace_size(int op, int B, int N, int V, int r);
@@ -245,6 +247,46 @@ DSPARK_API dspark_status dspark_verify(const float* p_target, const float* p_dra
  */
 DSPARK_API dspark_status dspark_verify_greedy(const float* target, const int32_t* draft_tokens,
                                    const int32_t* lengths, int B, int gamma, int V,
+                                   int32_t* out_tokens, int32_t* num_accepted,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Verification with the draft's own Gumbel noise ("probabilistic" drafting).
+ *
+ * "DSpark implementation and evaluation" §5: the draft samples with the
+ * Gumbel-max trick and the target verifies with the same Gumbel seed, which
+ * keeps the output distribution.  The target draws its own token at each
+ * position with the noise the draft drew at that step,
+ *   y_k = argmax_v (target_logits[b, k, v] / T[b] + g(b, k, v)),
+ * g the draft noise of dspark_markov_sample step k for request b (its seed and
+ * offset, the group-of-16 layout of the header of that function); T[b] = 0
+ * scores the plain argmax.  Drafted tokens are accepted while x_k = y_k; y at
+ * the first mismatch (at L_b when every tested token matches) is appended.
+ * The output is the target's own Gumbel-max sample sequence, so its law is the
+ * target's whatever the draft; the draft only decides how many of the tokens
+ * come from one target pass.  b is the request's row in both calls.  Ties go
+ * to the lowest id; NaN entries never win (a row without one gives token 0
+ * and sets NUMERIC); a NaN, negative or infinite T is scored greedily and
+ * sets NUMERIC.  Scores are fp32 (t * (1/T) + g): a token can differ from an
+ * exact evaluation only where the row's top-2 gap is within rounding.
+ *
+ *   target_logits [B, gamma+1, V] fp32, device: row k scores position k
+ *   temperature   [B] fp32, device (the target's; 0 = greedy)
+ *   draft_tokens  [B, gamma] int32, device
+ *   lengths       [B] int32 in [0, gamma], device, or NULL (= gamma)
+ *   seed, offset  the draft sampler's (offset < 2^32)
+ *   out_tokens    [B, gamma+1] int32 output: accepted prefix, the target's
+ *                 token, then -1
+ *   num_accepted  [B] int32 output
+ * Requirements: B >= 1, 1 <= gamma <= 65535, 1 <= V < 2^27, B <= 65535;
+ * target_logits 16-byte aligned.  Device-side: a token or length out of range
+ * sets INPUT_RANGE (the request outputs num_accepted 0 and -1 tokens).  Only
+ * rows k <= L_b are read.
+ * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY_GUMBEL, B, gamma, 0, 0).
+ */
+DSPARK_API dspark_status dspark_verify_gumbel(const float* target_logits, const float* temperature,
+                                   const int32_t* draft_tokens, const int32_t* lengths,
+                                   uint64_t seed, uint64_t offset, int B, int gamma, int V,
                                    int32_t* out_tokens, int32_t* num_accepted,
                                    void* workspace, size_t ws_bytes, void* stream);
 

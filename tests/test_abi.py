@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
     for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule",
                "dspark_verify_greedy", "dspark_confidence", "dspark_markov_sample_reduced",
-               "dspark_verify_logits"):
+               "dspark_verify_logits", "dspark_verify_gumbel"):
         assert op in names
 
 
@@ -48,6 +48,7 @@ def test_workspace_sizes(L):
     # round at this size)
     assert vl == 256 + 2048 + 1024 + 1024 + 8192 + 1024 + 1024 + 256 + 1024 + 8192 + 2048 + 1024 + 8 * 256 * 75
     assert L.dspark_workspace_size(6, 0, 8, 100, 8) == 0
+    assert L.dspark_workspace_size(7, 256, 8, 151936, 0) == 256 + 8 * 256 * 9 + 1024
     assert L.dspark_workspace_size(9, 1, 1, 1, 1) == 0
 
 
@@ -87,6 +88,20 @@ def test_host_validation_without_gpu(L):
     assert vl_with(a9=null) == 1                                             # no draft lse
     assert vl_with(a0=ctypes.c_void_p(4100)) == 1                            # misaligned logits
     assert vl_with(a20=1024) == 1                                            # workspace
+    vg = [fake, fake, fake, null, 0, 0, 4, 8, 1000, fake, fake, fake, 1 << 20, null]
+
+    def vg_with(**kw):
+        args = list(vg)
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return L.dspark_verify_gumbel(*args)
+
+    assert vg_with(a1=null) == 1                                             # no temperature
+    assert vg_with(a5=2 ** 32) == 1                                          # offset
+    assert vg_with(a7=0) == 1                                                # gamma = 0
+    assert vg_with(a8=1 << 27) == 1                                          # V too large
+    assert vg_with(a0=ctypes.c_void_p(4100)) == 1                            # misaligned logits
+    assert vg_with(a12=64) == 1                                              # workspace
     assert L.dspark_confidence(fake, 1, fake, 1, fake, fake, fake, fake, 0.0, fake, 1, 8, 64, 100, 0,
                                fake, fake, 256, null) == 1                                   # r = 0
     assert L.dspark_confidence(fake, 3, fake, 1, fake, fake, fake, fake, 0.0, fake, 1, 8, 64, 100, 8,
