@@ -57,20 +57,127 @@ __device__ __forceinline__ void take(unsigned long long& best, float y, int v) {
     }
 }
 
+// Running argmax of one lane over entries it sees in increasing index order: a strict comparison
+// keeps the lowest index, NaN never wins.
+__device__ __forceinline__ void argmax_take(float x, int e, float& best, int& idx) {
+    const bool take_it = (x == x) & ((idx < 0) | (x > best));
+    best = take_it ? x : best;
+    idx = take_it ? e : idx;
+}
+
+struct Running {
+    float lb;                                        // best exact score the row has reached
+    unsigned long long best;                         // this lane's best key
+};
+
+// The groups of one step of the chunk loop that the table could not rule out (rare; out of line
+// so the unrolled loop stays small): the exact largest variate first (exact for the entry at
+// position p, which becomes a candidate), the bound raised to the best of them over the warp,
+// then the lane's entries that can still reach it draw their own variate.  Called by the whole
+// warp.
+__device__ __noinline__ Running draw_groups(const GumbelArgs& a, int b, int k, int e, uint32_t W, float z0, float z1,
+                                            float z2, float z3, bool pass, Running run) {
+    const uint32_t lane = lane_id();
+    const float z[4] = {z0, z1, z2, z3};
+    const float e_min = group_e_min(W);
+    const float g_top = -logf(e_min);
+    const uint32_t p = W & 15u;
+    const uint32_t kpos0 = 4u * (lane & 3u);                    // this lane's first position in the group
+    if (pass && p - kpos0 < 4u) {
+        const int q = static_cast<int>(p - kpos0);
+        take(run.best, __fadd_rn(z[q], g_top), e + q);
+    }
+    const unsigned long long top = warp_max_u64(run.best);
+    if (top != 0ull) run.lb = fmaxf(run.lb, float_from_order_bits(static_cast<uint32_t>(top >> 32)));
+    if (pass) {
+        const uint32_t G = static_cast<uint32_t>(e) >> 4;
+        uint4 ew = make_uint4(0, 0, 0, 0);
+        bool have = false;
+        for (int q = 0; q < 4; ++q) {
+            if (kpos0 + static_cast<uint32_t>(q) == p) continue;
+            if (!(__fadd_rn(__fadd_rn(z[q], g_top), 1e-3f) >= run.lb)) continue;    // can not reach it (or NaN)
+            if (!have) {
+                ew = philox_at(a.seed, a.offset, (G << 2) | (lane & 3u), static_cast<uint32_t>(b), kStreamGumbelLo,
+                               static_cast<uint32_t>(k));
+                have = true;
+            }
+            take(run.best, __fadd_rn(z[q], draft_gumbel_of_entry(e_min, word_of(ew, static_cast<uint32_t>(q)))), e + q);
+        }
+    }
+    return run;
+}
+
 // Best key of one chunk of row (b, k) scored by z = t * invT plus the draft noise of step k.
 // Lane l holds entries e0 + 128 j + 4 l .. + 3 (j = 0..15); the four lanes 4m..4m+3 hold one
 // noise group for every j.
 __device__ unsigned long long chunk_gumbel(const GumbelArgs& a, const float* row, int b, int k, int c, float invT,
-                                           float lb, const float* gtab) {
+                                           float lb, const float* gtab, uint4* wbuf) {
     const uint32_t lane = lane_id();
     const int e0 = c * kChunk + 4 * static_cast<int>(lane);
     const bool whole = (a.V & 3) == 0 && c * kChunk + kChunk <= a.V;
     // group words of the chunk's 128 groups: lane l draws groups 4l .. 4l+3
     const uint4 gw = philox_at(a.seed, a.offset, static_cast<uint32_t>(c * 32) + lane, static_cast<uint32_t>(b),
                                kStreamGumbel, static_cast<uint32_t>(k));
-    const uint32_t widx = (lane >> 2) & 3u;
-    unsigned long long best = 0ull;
+    // through the warp's 512-byte buffer: lane l later reads word (l >> 2) & 3 of lane 2 jj + (l >> 4)
+    __syncwarp();
+    wbuf[lane] = gw;
+    __syncwarp();
+    const uint32_t* wsrc = reinterpret_cast<const uint32_t*>(wbuf) + 4 * (lane >> 4) + ((lane >> 2) & 3u);
+    Running run = {lb, 0ull};
 #pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        float4 f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = e0 + 128 * (8 * half + j);
+            if (whole) {
+                f[j] = __ldcs(reinterpret_cast<const float4*>(row + e));
+            } else {
+                const float nan = __int_as_float(0x7FC00000);
+                f[j].x = e + 0 < a.V ? __ldcs(row + e + 0) : nan;
+                f[j].y = e + 1 < a.V ? __ldcs(row + e + 1) : nan;
+                f[j].z = e + 2 < a.V ? __ldcs(row + e + 2) : nan;
+                f[j].w = e + 3 < a.V ? __ldcs(row + e + 3) : nan;
+            }
+        }
+        // the eight group tests of this half first (independent of each other), against the
+        // bound reached before the half; then the rare groups that pass are drawn in order
+        uint32_t Ws[8];
+        uint32_t passm = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int jj = 8 * half + j;
+            f[j].x = __fmul_rn(f[j].x, invT);
+            f[j].y = __fmul_rn(f[j].y, invT);
+            f[j].z = __fmul_rn(f[j].z, invT);
+            f[j].w = __fmul_rn(f[j].w, invT);
+            Ws[j] = wsrc[8 * jj];                        // the group word of this lane's group
+            float gm = fmaxf(fmaxf(f[j].x, f[j].y), fmaxf(f[j].z, f[j].w));   // NaN (and past-V) never win
+            gm = fmaxf(gm, __shfl_xor_sync(0xFFFFFFFFu, gm, 1));
+            gm = fmaxf(gm, __shfl_xor_sync(0xFFFFFFFFu, gm, 2));
+            const bool pass = __fadd_rn(gm, gtab[Ws[j] >> 24]) >= run.lb;
+            passm |= (pass ? 1u : 0u) << j;
+        }
+        const uint32_t warpm = __reduce_or_sync(0xFFFFFFFFu, passm);
+        if (warpm == 0u) continue;                                        // uniform over the warp
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if ((warpm >> j) & 1u)
+                run = draw_groups(a, b, k, e0 + 128 * (8 * half + j), Ws[j], f[j].x, f[j].y, f[j].z, f[j].w,
+                                  ((passm >> j) & 1u) != 0u, run);
+    }
+    return warp_max_u64(run.best);
+}
+
+// Plain argmax of one chunk (a greedy request): lowest index on ties, NaN never wins.  The loads
+// of each half are all issued before any is compared.
+__device__ unsigned long long chunk_argmax(const GumbelArgs& a, const float* row, int c) {
+    const uint32_t lane = lane_id();
+    const int e0 = c * kChunk + 4 * static_cast<int>(lane);
+    const bool whole = (a.V & 3) == 0 && c * kChunk + kChunk <= a.V;
+    float bv = 0.f;
+    int bi = -1;
+#pragma unroll
     for (int half = 0; half < 2; ++half) {
         float4 f[8];
 #pragma unroll
@@ -88,65 +195,14 @@ __device__ unsigned long long chunk_gumbel(const GumbelArgs& a, const float* row
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int jj = 8 * half + j;
-            const int e = e0 + 128 * jj;
-            float z[4] = {__fmul_rn(f[j].x, invT), __fmul_rn(f[j].y, invT), __fmul_rn(f[j].z, invT),
-                          __fmul_rn(f[j].w, invT)};
-            // the group word of this lane's group: word (l >> 2) & 3 of lane 2 jj + (l >> 4)'s draw
-            const int src = 2 * jj + static_cast<int>(lane >> 4);
-            const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, gw.x, src), w1 = __shfl_sync(0xFFFFFFFFu, gw.y, src);
-            const uint32_t w2 = __shfl_sync(0xFFFFFFFFu, gw.z, src), w3 = __shfl_sync(0xFFFFFFFFu, gw.w, src);
-            const uint32_t W = widx == 0 ? w0 : widx == 1 ? w1 : widx == 2 ? w2 : w3;
-            float gm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));          // NaN (and past-V) never win
-            gm = fmaxf(gm, __shfl_xor_sync(0xFFFFFFFFu, gm, 1));
-            gm = fmaxf(gm, __shfl_xor_sync(0xFFFFFFFFu, gm, 2));
-            const bool pass = __fadd_rn(gm, gtab[W >> 24]) >= lb;
-            if (__ballot_sync(0xFFFFFFFFu, pass) == 0u) continue;
-            // the groups that pass: the exact largest variate first (exact for the entry at
-            // position p, which becomes a candidate), the bound raised to the best of them,
-            // then the entries that can still reach it draw their own variate
-            const float e_min = group_e_min(W);
-            const float g_top = -logf(e_min);
-            const uint32_t p = W & 15u;
-            const uint32_t kpos0 = 4u * (lane & 3u);                    // this lane's first position in the group
-            if (pass && p - kpos0 < 4u) {
-                const int q = static_cast<int>(p - kpos0);
-                const float zq = q == 0 ? z[0] : q == 1 ? z[1] : q == 2 ? z[2] : z[3];
-                take(best, __fadd_rn(zq, g_top), e + q);
-            }
-            const unsigned long long top = warp_max_u64(best);
-            if (top != 0ull) lb = fmaxf(lb, float_from_order_bits(static_cast<uint32_t>(top >> 32)));
-            if (pass) {
-                const uint32_t G = static_cast<uint32_t>(e) >> 4;
-                uint4 ew = make_uint4(0, 0, 0, 0);
-                bool have = false;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (kpos0 + static_cast<uint32_t>(q) == p) continue;
-                    if (!(__fadd_rn(__fadd_rn(z[q], g_top), 1e-3f) >= lb)) continue;    // can not reach it (or NaN)
-                    if (!have) {
-                        ew = philox_at(a.seed, a.offset, (G << 2) | (lane & 3u), static_cast<uint32_t>(b),
-                                       kStreamGumbelLo, static_cast<uint32_t>(k));
-                        have = true;
-                    }
-                    take(best, __fadd_rn(z[q], draft_gumbel_of_entry(e_min, word_of(ew, static_cast<uint32_t>(q)))), e + q);
-                }
-            }
+            const int e = e0 + 128 * (8 * half + j);
+            argmax_take(f[j].x, e, bv, bi);
+            argmax_take(f[j].y, e + 1, bv, bi);
+            argmax_take(f[j].z, e + 2, bv, bi);
+            argmax_take(f[j].w, e + 3, bv, bi);
         }
     }
-    return warp_max_u64(best);
-}
-
-// Plain argmax of one chunk (a greedy request): lowest index on ties, NaN never wins.
-__device__ unsigned long long chunk_argmax(const GumbelArgs& a, const float* row, int c) {
-    const uint32_t lane = lane_id();
-    unsigned long long best = 0ull;
-    for (int jj = 0; jj < 16; ++jj) {
-        const int e = c * kChunk + 128 * jj + 4 * static_cast<int>(lane);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (e + q < a.V) take(best, __ldcs(row + e + q), e + q);
-    }
+    const unsigned long long best = bi >= 0 ? argmax_key(bv, static_cast<uint32_t>(bi)) : 0ull;
     return warp_max_u64(best);
 }
 
@@ -197,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_gumbel_kernel(GumbelArgs a
     // gtab[k]: bound on the largest variate -log(E_min) of a noise group whose group word has
     // top byte k (that of the largest such word, plus a margin for logf's rounding)
     __shared__ float gtab[256];
+    __shared__ uint4 s_words[kWarps][32];                // per-warp transpose of the chunk's group words
     for (int k = threadIdx.x; k < 256; k += kThreads)
         gtab[k] = k == 255 ? kDraftGumbelMax : -logf(group_e_min((static_cast<uint32_t>(k + 1) << 24) - 1u)) + 1e-3f;
     __syncthreads();
@@ -223,12 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_gumbel_kernel(GumbelArgs a
             if (!len_ok || k > Lb) continue;                      // rows past L_b are not needed
             const float* row = a.t + (static_cast<size_t>(b) * (a.gamma + 1) + k) * a.V;
             unsigned long long* slot = a.keys + static_cast<size_t>(b) * (a.gamma + 1) + k;
+            if (f + 1 < req_end) {
+                // bring the warp's next chunk of this request into L2 while this one is scored
+                const long long rn = rem + 1;
+                const int kn = static_cast<int>(rn / a.n_chunk), cn = static_cast<int>(rn % a.n_chunk);
+                if (kn <= Lb) {
+                    const float* nrow = a.t + (static_cast<size_t>(b) * (a.gamma + 1) + kn) * a.V;
+                    const int e = cn * kChunk + 64 * static_cast<int>(lane);
+                    if (e < a.V) prefetch_l2(nrow + e);
+                    if (e + 32 < a.V) prefetch_l2(nrow + e + 32);
+                }
+            }
             unsigned long long key;
             if (invT > 0.f) {
                 // the best exact value another chunk of the row has reached already
                 const unsigned long long seen = __ldcg(slot);
                 const float lb = seen != 0ull ? float_from_order_bits(static_cast<uint32_t>(seen >> 32)) : -INFINITY;
-                key = chunk_gumbel(a, row, b, k, c, invT, lb, gtab);
+                key = chunk_gumbel(a, row, b, k, c, invT, lb, gtab, s_words[warp_id()]);
             } else {
                 key = chunk_argmax(a, row, c);
             }
