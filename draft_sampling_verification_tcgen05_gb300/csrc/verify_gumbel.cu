@@ -10,8 +10,10 @@
 // target's own Gumbel-max sample sequence.
 //
 // One kernel, bound by reading the rows, with the item / count / decide
-// structure of the greedy verifier: every warp of a grid of one block per SM
-// takes an equal contiguous range of the B * (gamma+1) * n_chunk chunks of
+// structure of the greedy verifier: every warp of a grid of three 256-thread
+// blocks per SM (24 warps: more loads in flight than one 512-thread block at
+// the register count the noise test needs) takes an equal contiguous range of
+// the B * (gamma+1) * n_chunk chunks of
 // 2048 entries (rows k <= L_b only).  The draft noise comes in groups of 16
 // entries whose group word bounds the group's largest variate (see
 // draft_gumbel in device_common.cuh); per chunk one Philox round per lane
@@ -30,7 +32,8 @@
 namespace dspark {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
+constexpr int kBlocksPerSm = 3;                      // 24 warps per SM (registers capped at 80)
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 2048;                         // entries per warp item: 16 float4 per lane
 
@@ -249,7 +252,7 @@ __device__ void decide(const GumbelArgs& a, int b) {
     if (lane == 0) a.n_acc[b] = kstar;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) verify_gumbel_kernel(GumbelArgs a) {
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm) verify_gumbel_kernel(GumbelArgs a) {
     // gtab[k]: bound on the largest variate -log(E_min) of a noise group whose group word has
     // top byte k (that of the largest such word, plus a margin for logf's rounding)
     __shared__ float gtab[256];
@@ -348,7 +351,7 @@ dspark_status launch_verify_gumbel(const float* target_logits, const float* temp
     a.n_chunk = (V + kChunk - 1) / kChunk;
     a.total = static_cast<long long>(B) * (gamma + 1) * a.n_chunk;
     const long long want = (a.total + 3) / 4;                    // at least 4 chunks a warp
-    const int blocks = static_cast<int>(std::max(1LL, std::min(static_cast<long long>(dev.sm_count),
+    const int blocks = static_cast<int>(std::max(1LL, std::min(static_cast<long long>(dev.sm_count) * kBlocksPerSm,
                                                                 (want + kWarps - 1) / kWarps)));
     a.warps_total = blocks * kWarps;
     verify_gumbel_kernel<<<blocks, kThreads, 0, stream>>>(a);
