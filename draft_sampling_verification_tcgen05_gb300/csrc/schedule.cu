@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(32) schedule_warp_kernel(ScheduleArgs a) {
 // Pools of up to kSmemMaxCandidates: everything in shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kSmemMaxCandidates = 16384;
+constexpr int kBitonicMax = 2048;                                   // pools sorted by the bitonic network
 constexpr int kMaxRounds = kSmemMaxCandidates / (32 * 32);       // rounds of 32 keys per warp (1024 threads)
 
 // Dynamic shared memory: key[nn] u32 | idxA[nn] u16 | idxB[nn] u16 | cnt[kWarps][256] u16, nn = n
@@ -383,13 +384,44 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs
     __syncthreads();
     if (tid == 0 && s_bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
 
+    uint16_t* src = idxA;
+    if (kThreads == 1024 && n <= kBitonicMax) {
+        // ---- 2'. pools of up to 2048: bitonic sort of (key << 32 | index) in the counter area.
+        //      Equal keys fall to the lower index, as in the stable radix sort.  Pair i of a stage with
+        //      partner distance jj <= 32 lies in its warp's 64-entry window, so those stages
+        //      need only a warp barrier ----
+        unsigned long long* sk = reinterpret_cast<unsigned long long*>(cnt);
+        int P = 64;
+        while (P < n) P <<= 1;
+        for (int j = tid; j < P; j += kThreads)
+            sk[j] = j < n ? (static_cast<unsigned long long>(key[swz(j)]) << 32) | static_cast<unsigned long long>(j)
+                          : ~0ull;
+        __syncthreads();
+        for (int k = 2; k <= P; k <<= 1) {
+            for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                for (int i = tid; i < P / 2; i += kThreads) {
+                    const int pos = 2 * i - (i & (jj - 1));
+                    const unsigned long long x = sk[pos], y = sk[pos + jj];
+                    if ((x > y) == ((pos & k) == 0)) {
+                        sk[pos] = y;
+                        sk[pos + jj] = x;
+                    }
+                }
+                // the next stage crosses warps when its distance is 64 or more
+                const int next = jj > 1 ? jj >> 1 : k;
+                if (jj >= 64 || next >= 64) __syncthreads(); else __syncwarp();
+            }
+        }
+        __syncthreads();
+        for (int j = tid; j < n; j += kThreads) idxA[j] = static_cast<uint16_t>(sk[j] & 0xFFFFull);
+        __syncthreads();
+    } else {
     // ---- 2. stable LSD radix sort of the indices by key ----
     // warp w ranks the run [w0, w1) of the current order; chunk is a multiple of 32
     const int chunk = (((n + kWarps - 1) / kWarps) + 31) & ~31;
     const int w0 = static_cast<int>(warp) * chunk;
     const int w1 = min(n, w0 + chunk);
     const int rounds = w1 > w0 ? (w1 - w0 + 31) / 32 : 0;
-    uint16_t* src = idxA;
     uint16_t* dst = idxB;
     uint16_t* mycnt = cnt + warp * kRadix;
     for (int pass = 0; pass < 4; ++pass) {
@@ -483,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs
         uint16_t* t = src;
         src = dst;
         dst = t;
+    }
     }
     // sorted candidate indices are in src
 

@@ -63,10 +63,11 @@ def test_out_of_range_confidences_are_clamped_and_flagged(cuda_lib):
     assert ref["clamped"] and bits & cuda_lib.STATUS_INPUT_RANGE
 
 
-@pytest.mark.parametrize("B,N", [(16, 16), (257, 1), (32, 32), (41, 25), (1023, 16), (1, 16384)])
+@pytest.mark.parametrize("B,N", [(16, 16), (257, 1), (32, 32), (41, 25), (100, 20), (64, 32), (2049, 1),
+                                 (1023, 16), (1, 16384)])
 def test_pool_sizes_around_block_and_round_edges(cuda_lib, B, N):
-    """Pools at and just past 256 and 1024 candidates, ragged warp runs, the 16384 maximum
-    of the shared-memory sort with a single request."""
+    """Pools at and just past 256, 1024 and 2048 candidates (the bitonic and the radix sort),
+    ragged warp runs, the 16384 maximum of the shared-memory sort with a single request."""
     rng = np.random.default_rng(B * 1000 + N)
     c = rng.beta(4, 1.5, size=(B, N)).astype(np.float32)
     c[rng.random((B, N)) < 0.15] = 1.0
