@@ -27,6 +27,7 @@
 #include "markov_common.cuh"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace dspark {
 namespace {
@@ -39,6 +40,25 @@ constexpr size_t kW2CacheBytes = 144 * 1024;           // w2 slice kept in share
 constexpr size_t kZStoreBytes = 32 * 1024;             // z rows kept in shared memory when they fit
 constexpr int kMaxEFloats = 16384;                     // B * r limit of the shared E matrix
 
+// Decode tensor path (one request, bf16 head, r = 64): the block's w2 slice stays in tensor
+// memory for the whole call as the A operand of eight 128 x 16 x 64 tcgen05 MMAs per step,
+// E = w1[prev] is row 0 of the 16-row B operand in shared memory (128-byte swizzle), and the
+// bias of each entry is column 0 of its tile's accumulator.  Tensor memory: accumulators in
+// columns [0, 128) (16 per tile), the slice in [128, 384) (32 per tile: 64 bf16 per lane).
+constexpr int kTcRows = 2 * kThreads;                   // 1024 slice entries, 8 tiles of 128
+constexpr int kTcTiles = kTcRows / 128;
+constexpr int kTcR = 64;
+constexpr int kTcN = 16;
+constexpr uint32_t kTcCols = 512;
+constexpr uint32_t kTcACol = 128;
+constexpr size_t kTcBBytes = static_cast<size_t>(kTcN) * kTcR * 2;
+constexpr size_t kTcMinSmem = 120 * 1024;               // keeps one block per SM (it holds all of TMEM)
+constexpr uint32_t kWaitDecodeMma = 0x311;
+constexpr long long kPollHoldCycles = 800;              // about 0.4 us at 2 GHz
+
+// Entry 2 tid + h of the slice (thread tid, warp w) is row 32 (w mod 4) + lane of tile w / 4 + 4 h:
+// the two entries of a thread share a noise group word, and warp w reads exactly tensor-memory
+// lanes 32 (w mod 4) + lane.
 
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
@@ -198,7 +218,7 @@ __device__ __forceinline__ int w2_slot(const MarkovArgs& a, int t) {
     return a.w2_split ? ((t & 1) ? (a.slice >> 1) + (t >> 1) : (t >> 1)) : t;
 }
 
-template <typename WT>
+template <typename WT, bool kTC>
 __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sp = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
@@ -209,15 +229,24 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     __shared__ float s_inv[256];                      // their reciprocals (1 for greedy)
     __shared__ unsigned long long s_win[kExchangeMaxBN];  // exchange: the step's best key per request
     __shared__ int s_tok[kExchangeMaxBN];                  // exchange: winners [step][request]
+    __shared__ __align__(8) uint64_t s_mma_bar;            // tensor path: the step's MMAs completed
+    __shared__ uint32_t s_tmem;                            // tensor path: accumulator base
 
     const int v_lo = blockIdx.x * a.slice;
     const int v_hi = min(a.V, v_lo + a.slice);
     const int n_local = max(0, v_hi - v_lo);
     const int tid = threadIdx.x;
 
-    // shared-memory carve-up: [w2 cache][z store][E][prev]
+    // shared-memory carve-up: [w2 cache][z store][E][prev]; the tensor path keeps the slice in
+    // tensor memory and has the 1024-byte aligned B operand in place of the w2 cache
     uint8_t* w2s = sp;
-    sp += a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
+    uint8_t* bop = nullptr;
+    if constexpr (kTC) {
+        bop = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sp) + 1023) & ~static_cast<uintptr_t>(1023));
+        sp = bop + kTcBBytes;
+    } else {
+        sp += a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
+    }
     float* zs = reinterpret_cast<float*>(sp);
     sp += a.z_stored ? sizeof(float) * static_cast<size_t>(a.slice) * a.B : 0;
     float* E = reinterpret_cast<float*>(sp);
@@ -226,7 +255,42 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
 
     const size_t row_bytes = sizeof(WT) * static_cast<size_t>(a.r);
     const size_t row_bytes_w1 = row_bytes;
-    if (a.w2_cached) {
+    if constexpr (kTC) {
+        for (int idx = tid; idx < static_cast<int>(kTcBBytes / 16); idx += kThreads)
+            reinterpret_cast<uint4*>(bop)[idx] = make_uint4(0u, 0u, 0u, 0u);
+        if (tid == 0) {
+            mbar_init(&s_mma_bar, 1);
+            fence_mbarrier_init();
+        }
+        if (warp_id() == 0) {
+            tmem_alloc(&s_tmem, kTcCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        // the thread's entries 2 tid + h (zero rows past the slice) into lane 32 (w mod 4) + lane of
+        // tiles w / 4 + 4 h: 32 columns of bf16 pairs in K order
+        const uint32_t w = warp_id();
+        const uint32_t lanes = (32u * (w & 3u)) << 16;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.w2) +
+                                                          static_cast<size_t>(v_lo) * (2 * kTcR));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = 2 * tid + h;
+            uint32_t rw[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 q = t < n_local ? __ldcs(src + static_cast<size_t>(t) * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+                rw[4 * c] = q.x;
+                rw[4 * c + 1] = q.y;
+                rw[4 * c + 2] = q.z;
+                rw[4 * c + 3] = q.w;
+            }
+            tmem_st32(s_tmem + lanes + kTcACol + 32u * ((w >> 2) + 4u * h), rw);
+        }
+        tmem_wait_st();
+    } else if (a.w2_cached) {
         // load this block's w2 rows once; rows padded to w2_pitch bytes
         const uint8_t* src = static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v_lo) * row_bytes;
         const int chunks = static_cast<int>(row_bytes / 16);
@@ -269,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     };
     if (fast) prepare(0, pl0, pl1, pg0, pg1);
     bool alive = true;
+    int tc_fail = 0;                                  // tensor path: an MMA wait timed out
     for (int i = 0; i < a.N && alive; ++i) {
         // ---- 1. previous tokens and the Markov embedding E[b] = w1[prev_b] ----
         for (int b = tid; b < a.B; b += kThreads) {
@@ -286,12 +351,51 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         }
         if (i > 0) finish_lse(a, i - 1, tid, kThreads);
         __syncthreads();
-        for (int idx = tid; idx < a.B * a.r; idx += kThreads) {
-            const int b = idx / a.r, k = idx % a.r;
-            E[idx] = to_f<WT>(static_cast<const WT*>(a.w1)[static_cast<size_t>(prev[b]) * a.r + k]);
+        float tb0 = 0.f, tb1 = 0.f;                  // tensor path: this thread's two biases
+        if constexpr (kTC) {
+            // E = w1[prev] (bf16, unconverted) is row 0 of the B operand: the anchor's row here,
+            // later steps' rows were put there by the exchange
+            if (i == 0 && tid < 8) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(
+                    static_cast<const uint8_t*>(a.w1) + static_cast<size_t>(prev[0]) * (2 * kTcR)) + tid);
+                reinterpret_cast<uint4*>(bop)[tid] = q;
+            }
+            if (i > 0 && tid == 0) s_win[0] = 0ull;  // every thread read the last winner before the barrier above
+            fence_proxy_async_smem();                // operand writes -> the tensor core's view
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            const uint32_t tmem = s_tmem;
+            if (tid == 0) {
+                constexpr uint32_t idesc = mma_idesc(128, kTcN, false);
+                const uint32_t b0 = smem_u32(bop);
+#pragma unroll
+                for (int m = 0; m < kTcTiles; ++m)
+#pragma unroll
+                    for (int kk = 0; kk < kTcR / 16; ++kk)
+                        mma_issue_ta(tmem + static_cast<uint32_t>(kTcN * m),
+                                     tmem + kTcACol + static_cast<uint32_t>(32 * m + 8 * kk),
+                                     sw128_kmajor_desc(b0 + static_cast<uint32_t>(32 * kk)), idesc,
+                                     kk > 0 ? 1u : 0u);
+                mma_commit(&s_mma_bar);
+            }
+            if (!mbar_wait(&s_mma_bar, static_cast<uint32_t>(i & 1), a.ws, a.timeout_ns, kWaitDecodeMma))
+                tc_fail = 1;
+            tc_fence_after();
+            const uint32_t w = warp_id();
+            const uint32_t lanes = (32u * (w & 3u)) << 16;
+            tb0 = __uint_as_float(tmem_ld1(tmem + lanes + static_cast<uint32_t>(kTcN * (w >> 2))));
+            tb1 = __uint_as_float(tmem_ld1(tmem + lanes + static_cast<uint32_t>(kTcN * ((w >> 2) + 4))));
+            tmem_wait_ld();
+            tc_fence_before();                       // the next step's MMAs overwrite these columns
+        } else {
+            for (int idx = tid; idx < a.B * a.r; idx += kThreads) {
+                const int b = idx / a.r, k = idx % a.r;
+                E[idx] = to_f<WT>(static_cast<const WT*>(a.w1)[static_cast<size_t>(prev[b]) * a.r + k]);
+            }
+            if (i == 0 && a.w2_cached) asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncthreads();
         }
-        if (i == 0 && a.w2_cached) asm volatile("cp.async.wait_all;" ::: "memory");
-        __syncthreads();
 
         unsigned long long* slot = a.lay.slots + static_cast<size_t>(i) * a.B;
         uint32_t* lbs = a.lay.lb + static_cast<size_t>(i) * a.B;
@@ -318,9 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             unsigned long long best = 0ull;
             float2 ls = make_float2(0.f, 0.f);
             bool bad = false;
-            if (hot && a.single_pass && a.lse == nullptr) {
+            if ((hot || kTC) && a.single_pass && a.lse == nullptr) {
                 // one pass with noise on every entry; each thread takes two adjacent entries,
                 // which share their group word and element counter and interleave for ILP
+                // (the tensor path takes greedy requests here too, without the noise)
                 for (int t = 2 * tid; t < n_local; t += 2 * kThreads) {
                     const int v = v_lo + t;
                     const bool two = t + 1 < n_local;
@@ -329,7 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                     const uint8_t* wrow1 = a.w2_cached ? w2s + static_cast<size_t>(w2_slot(a, t + 1)) * a.w2_pitch
                                                        : wrow0 + row_bytes;
                     float b0, b1;
-                    bias_dot2<WT>(wrow0, two ? wrow1 : wrow0, e, a.r, b0, b1);
+                    if constexpr (kTC) {
+                        b0 = tb0;
+                        b1 = tb1;
+                    } else {
+                        bias_dot2<WT>(wrow0, two ? wrow1 : wrow0, e, a.r, b0, b1);
+                    }
                     float l0, l1, g0, g1;
                     if (fast) {
                         l0 = pl0; l1 = pl1; g0 = pg0; g1 = pg1;
@@ -346,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                         const uint32_t vv = static_cast<uint32_t>(v + h);
                         const float z = __fmul_rn(__fadd_rn(h ? l1 : l0, h ? b1 : b0), invT);
                         if (z != z) { bad = true; continue; }
-                        const float y = __fadd_rn(z, h ? g1 : g0);
+                        const float y = hot ? __fadd_rn(z, h ? g1 : g0) : z;
                         if (y != y) continue;
                         const unsigned long long k = argmax_key(y, vv);
                         best = k > best ? k : best;
@@ -425,10 +535,24 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             // every block's candidates for this step, polled (bounded) and reduced here
             // the next step's logits and noise do not depend on this step's token: drawn
             // while the other blocks finish
-            if (fast && i + 1 < a.N) prepare(i + 1, pl0, pl1, pg0, pg1);
+            if (fast && i + 1 < a.N) {
+                prepare(i + 1, pl0, pl1, pg0, pg1);
+            } else {
+                // nothing to prefetch: polling the moment this block has published delays the
+                // publications of the others (measured: about 3 us instead of 1.5 us at 149
+                // blocks); the first poll waits as long as the prefetch would have taken
+                const long long c0 = clock64();
+                while (clock64() - c0 < kPollHoldCycles) {
+                }
+            }
             const int n_ent = static_cast<int>(gridDim.x) * a.B;
             const unsigned long long* cs = a.lay.cand + static_cast<size_t>(i) * n_ent;
             int fail = 0;
+            // tensor path: a candidate that beats every one this block has seen so far has its w1
+            // row fetched at once, so the winner's row (the next B operand) is in flight while the
+            // last candidates arrive
+            unsigned long long row_key = 0ull;
+            uint4 row[8];
             for (int e = tid; e < n_ent; e += kThreads) {
                 unsigned long long k = ld_relaxed_u64(cs + e);
                 const long long t0 = global_ns();
@@ -445,21 +569,50 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                     }
                     k = ld_relaxed_u64(cs + e);
                 }
-                if (k > 1ull) atomicMax(&s_win[e % a.B], k);
+                if (k > 1ull) {
+                    const unsigned long long old = atomicMax(&s_win[e % a.B], k);
+                    if constexpr (kTC) {
+                        if (k > old) {
+                            const uint4* src = reinterpret_cast<const uint4*>(
+                                static_cast<const uint8_t*>(a.w1) + static_cast<size_t>(key_index(k)) * (2 * kTcR));
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) row[c] = __ldg(src + c);
+                            row_key = k;
+                        }
+                    }
+                }
             }
-            alive = __syncthreads_or(fail) == 0;
+            alive = __syncthreads_or(fail | tc_fail) == 0;
+            if constexpr (kTC) {
+                const unsigned long long kw = s_win[0];
+                if (kw == 0ull) {                     // no finite candidate: token 0's row
+                    if (tid < 8)
+                        reinterpret_cast<uint4*>(bop)[tid] = __ldg(reinterpret_cast<const uint4*>(a.w1) + tid);
+                } else if (row_key == kw) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(bop)[c] = row[c];
+                }
+            }
             for (int b = tid; b < a.B; b += kThreads) {
                 const unsigned long long k = s_win[b];
                 int x = 0;
                 if (k == 0ull) set_status(a.ws, DSPARK_STATUS_NUMERIC);    // no finite candidate at all
                 else x = static_cast<int>(key_index(k));
                 s_tok[i * a.B + b] = x;
-                s_win[b] = 0ull;
+                if constexpr (!kTC) s_win[b] = 0ull;
             }
         } else {
             grid_arrive(a.ws);
             if (fast && i + 1 < a.N) prepare(i + 1, pl0, pl1, pg0, pg1);
             alive = grid_wait(a.ws, static_cast<uint32_t>(i), a.timeout_ns, kWaitStep + i);
+        }
+    }
+    if constexpr (kTC) {
+        tc_fence_before();
+        __syncthreads();
+        if (warp_id() == 0) {
+            tc_fence_after();
+            tmem_dealloc(s_tmem, kTcCols);
         }
     }
     if (!alive) return;
@@ -497,15 +650,23 @@ dspark_status run_generic(MarkovArgs& a, cudaStream_t stream, const DeviceInfo& 
         set_error("markov_sample: B*r = %d exceeds the %d the sampler holds on chip", a.B * a.r, kMaxEFloats);
         return DSPARK_ERR_UNSUPPORTED;
     }
+    // one request with a bf16 head of rank 64 whose slice fits eight 128-row tiles: the bias on
+    // the tensor cores
+    bool tc = false;
+    if constexpr (std::is_same<WT, __nv_bfloat16>::value)
+        tc = a.B == 1 && a.r == kTcR && a.single_pass && a.lse == nullptr && a.exchange && a.slice <= kTcRows;
     size_t smem = 16;
-    smem += a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
+    smem += tc ? 1023 + kTcBBytes : a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
     smem += a.z_stored ? sizeof(float) * static_cast<size_t>(a.slice) * a.B : 0;
     smem += sizeof(float) * static_cast<size_t>(a.B) * a.r + sizeof(int) * static_cast<size_t>(a.B);
+    if (tc) smem = std::max(smem, kTcMinSmem);
     if (smem > dev.smem_optin) {
         set_error("markov_sample: needs %zu bytes of shared memory", smem);
         return DSPARK_ERR_UNSUPPORTED;
     }
-    auto kernel = markov_generic_kernel<WT>;
+    auto kernel = markov_generic_kernel<WT, false>;
+    if constexpr (std::is_same<WT, __nv_bfloat16>::value)
+        if (tc) kernel = markov_generic_kernel<WT, true>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(markov_sample)");

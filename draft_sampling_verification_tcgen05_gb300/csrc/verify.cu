@@ -266,13 +266,19 @@ __device__ void finish_request(const VerifyArgs& a, int b, int dec, unsigned lon
         __syncthreads();
         const int s = *s_pick;
         if (warp_id() == 0) {
-            // walk the segment's four 128-entry slices to the one holding tl, then pick inside it
+            // the segment's four 128-entry slices are loaded at once (one memory round trip),
+            // then walked to the one holding tl, and tl is picked inside it
             unsigned long long tl = *s_tloc;
             int pick_v = -1;
-            for (int i = 0; i < 4 && pick_v < 0; ++i) {
-                unsigned long long q[4];
+            unsigned long long qs[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                masses4(rt, rd, s * kSeg + i * kSlice + 4 * static_cast<int>(lane_id()), V, vec, qs[i]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (pick_v >= 0) break;
+                const unsigned long long (&q)[4] = qs[i];
                 const int e = s * kSeg + i * kSlice;
-                masses4(rt, rd, e + 4 * static_cast<int>(lane_id()), V, vec, q);
                 const unsigned long long lane_sum = q[0] + q[1] + q[2] + q[3];
                 const unsigned long long incl_l = warp_incl_scan_u64(lane_sum);
                 const unsigned long long slice = __shfl_sync(0xFFFFFFFFu, incl_l, 31);

@@ -74,8 +74,11 @@ def test_batched_draft_sampled_requests(cuda_lib):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("B,N,V,r,T", [(1, 1, 2, 1, 1.0), (3, 5, 1001, 5, 0.7), (2, 4, 4097, 16, 0.0),
-                                       (5, 3, 40000, 64, 1.3), (16, 2, 3000, 256, 0.9)])
+                                       (5, 3, 40000, 64, 1.3), (16, 2, 3000, 256, 0.9),
+                                       (1, 6, 2000, 64, 1.0), (1, 5, 70001, 64, 0.8), (1, 3, 9000, 64, 0.0)])
 def test_ragged_and_edge_shapes(cuda_lib, dtype, B, N, V, r, T):
+    """Includes single requests at r = 64 (bf16: the bias on the tensor cores) with slices of
+    a few hundred entries and a ragged last slice."""
     cfg = DraftConfig("edge", B=B, N=N, H=8, V=V, r=r, dtype=dtype, temperatures=(T,), data_seed=91)
     L = markov_logits(cfg, scale=2.0)
     w1 = normal_rows(V, r, 1.0, 91, "w1")
@@ -154,3 +157,22 @@ def test_step_without_finite_logits_sets_numeric_and_spares_other_requests(cuda_
     assert tok[1, 1] == 0
     ref, gap, _ = oracle.markov_sample(L[:1], anchor[:1], w1, w2, T[:1], 4, 0)
     compare_markov_tokens(tok[:1], ref, gap)
+
+
+def test_single_request_bf16_step_without_finite_logits(cuda_lib):
+    """One request, bf16 head at r = 64 (the tensor-core bias): a step whose base logits are all
+    NaN has no candidate (token 0, NUMERIC bit); the step before it matches the oracle and the
+    call completes."""
+    B, N, V, r = 1, 4, 20000, 64
+    cfg = DraftConfig("nan1", B=B, N=N, H=8, V=V, r=r, dtype="bf16", temperatures=(1.0,), data_seed=8)
+    L = markov_logits(cfg)
+    L[0, 2, :] = np.nan
+    tw1, w1 = to_bf16_values(normal_rows(V, r, 1.0, 8, "w1"))
+    tw2, w2 = to_bf16_values(normal_rows(V, r, 1.0 / np.sqrt(r), 8, "w2"))
+    anchor = np.array([17], np.int32)
+    T = np.ones(B, np.float32)
+    tok, _, st, bits = _gpu(cuda_lib, L, anchor, tw1, tw2, T, 6, 0)
+    assert bits & cuda_lib.STATUS_NUMERIC and not bits & cuda_lib.STATUS_TIMEOUT
+    assert tok[0, 2] == 0
+    ref, gap, _ = oracle.markov_sample(L[:, :2], anchor, w1, w2, T, 6, 0)
+    compare_markov_tokens(tok[:, :2], ref, gap)
