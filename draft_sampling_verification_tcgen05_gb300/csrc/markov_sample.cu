@@ -52,7 +52,8 @@ constexpr int kTcN = 16;
 constexpr uint32_t kTcCols = 512;
 constexpr uint32_t kTcACol = 128;
 constexpr size_t kTcBBytes = static_cast<size_t>(kTcN) * kTcR * 2;
-constexpr size_t kTcMinSmem = 120 * 1024;               // keeps one block per SM (it holds all of TMEM)
+constexpr size_t kTcStageBytes = static_cast<size_t>(kTcRows) * kTcR * 2;   // slice staging (also
+                                                        // keeps one block per SM, which holds all of TMEM)
 constexpr uint32_t kWaitDecodeMma = 0x311;
 constexpr long long kPollHoldCycles = 800;              // about 0.4 us at 2 GHz
 
@@ -241,9 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     // tensor memory and has the 1024-byte aligned B operand in place of the w2 cache
     uint8_t* w2s = sp;
     uint8_t* bop = nullptr;
+    uint8_t* stage = nullptr;
     if constexpr (kTC) {
         bop = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sp) + 1023) & ~static_cast<uintptr_t>(1023));
-        sp = bop + kTcBBytes;
+        stage = bop + kTcBBytes;
+        sp = stage + kTcStageBytes;
     } else {
         sp += a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
     }
@@ -255,6 +258,56 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
 
     const size_t row_bytes = sizeof(WT) * static_cast<size_t>(a.r);
     const size_t row_bytes_w1 = row_bytes;
+    // Decode fast path (one request, one pair of entries per thread): the base logits and
+    // the noise of step i+1 do not depend on the token of step i, so they are fetched and
+    // drawn while the block waits at step i's grid barrier.
+    const bool fast = a.B == 1 && a.single_pass && a.lse == nullptr && 2 * kThreads >= n_local;
+    float pl0 = 0.f, pl1 = 0.f, pg0 = 0.f, pg1 = 0.f;       // this step's logits and noise
+    auto prepare = [&](int j, float& l0, float& l1, float& g0, float& g1) {
+        const int t = 2 * tid;
+        if (t >= n_local) return;
+        const int v = v_lo + t;
+        const bool two = t + 1 < n_local;
+        const float* lr = a.base + static_cast<size_t>(j) * a.V;
+        l0 = __ldcs(lr + v);
+        l1 = two ? __ldcs(lr + v + 1) : 0.f;
+        draft_gumbel_pair(a.seed, a.offset, 0u, static_cast<uint32_t>(j), static_cast<uint32_t>(v), g0, g1);
+        if (!two) g1 = 0.f;
+    };
+    // step 0's inputs are fetched before anything waits on memory: the first request's
+    // temperature and anchor per thread, and (tensor path) the anchor's w1 row
+    const float T_first = tid < a.B ? __ldg(a.temperature + tid) : 0.f;
+    const int anchor_first = tid < a.B ? __ldg(a.anchor + tid) : 0;
+    uint4 e_first = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (kTC) {
+        if (tid < 8) {
+            const int p = __ldg(a.anchor);
+            e_first = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.w1) +
+                                                           static_cast<size_t>(p >= 0 && p < a.V ? p : 0) * (2 * kTcR)) + tid);
+        }
+    }
+    if constexpr (kTC) {
+        // warp w's entries [64 w, 64 w + 64) (its threads' pairs) are 8 KB of contiguous rows: copied
+        // in 512-byte warp-wide pieces into the staging area, chunk c of entry e at chunk
+        // c ^ ((e / 2) mod 8) of its 128-byte row, so that the row-per-thread reads below are free of
+        // bank conflicts; rows past the slice are zero.  The copies land while step 0's noise is
+        // drawn and tensor memory is allocated.
+        const uint8_t* src = static_cast<const uint8_t*>(a.w2) + static_cast<size_t>(v_lo) * (2 * kTcR);
+        const int e_base = 64 * static_cast<int>(warp_id());
+        const int lane = static_cast<int>(lane_id());
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) {
+            const int e = e_base + 4 * j + (lane >> 3), c = lane & 7;
+            uint8_t* dst = stage + static_cast<size_t>(e) * 128 + 16 * (c ^ ((e >> 1) & 7));
+            if (e < n_local)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             :: "r"(smem_u32(dst)), "l"(src + static_cast<size_t>(e) * 128 + 16 * c) : "memory");
+            else
+                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    if (fast) prepare(0, pl0, pl1, pg0, pg1);
     if constexpr (kTC) {
         for (int idx = tid; idx < static_cast<int>(kTcBBytes / 16); idx += kThreads)
             reinterpret_cast<uint4*>(bop)[idx] = make_uint4(0u, 0u, 0u, 0u);
@@ -269,19 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        // the thread's entries 2 tid + h (zero rows past the slice) into lane 32 (w mod 4) + lane of
-        // tiles w / 4 + 4 h: 32 columns of bf16 pairs in K order
+        // entry 2 tid + h into lane 32 (w mod 4) + lane of tile w / 4 + 4 h: 32 columns of bf16
+        // pairs in K order
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncwarp();
         const uint32_t w = warp_id();
         const uint32_t lanes = (32u * (w & 3u)) << 16;
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.w2) +
-                                                          static_cast<size_t>(v_lo) * (2 * kTcR));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int t = 2 * tid + h;
+            const int e = 2 * tid + h;
+            const uint8_t* row = stage + static_cast<size_t>(e) * 128;
             uint32_t rw[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const uint4 q = t < n_local ? __ldcs(src + static_cast<size_t>(t) * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 q = *reinterpret_cast<const uint4*>(row + 16 * (c ^ ((e >> 1) & 7)));
                 rw[4 * c] = q.x;
                 rw[4 * c + 1] = q.y;
                 rw[4 * c + 2] = q.z;
@@ -305,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     }
 
     for (int b = tid; b < 256 && b < a.B; b += kThreads) {
-        float T = __ldg(a.temperature + b);
+        float T = b == tid ? T_first : __ldg(a.temperature + b);
         if (!(T >= 0.f) || isinf(T)) {
             set_status(a.ws, DSPARK_STATUS_NUMERIC);
             T = 0.f;
@@ -315,23 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     }
     if (a.exchange)
         for (int b = tid; b < a.B; b += kThreads) s_win[b] = 0ull;
-    // Decode fast path (one request, one pair of entries per thread): the base logits and
-    // the noise of step i+1 do not depend on the token of step i, so they are fetched and
-    // drawn while the block waits at step i's grid barrier.
-    const bool fast = a.B == 1 && a.single_pass && a.lse == nullptr && 2 * kThreads >= n_local;
-    float pl0 = 0.f, pl1 = 0.f, pg0 = 0.f, pg1 = 0.f;       // this step's logits and noise
-    auto prepare = [&](int j, float& l0, float& l1, float& g0, float& g1) {
-        const int t = 2 * tid;
-        if (t >= n_local) return;
-        const int v = v_lo + t;
-        const bool two = t + 1 < n_local;
-        const float* lr = a.base + static_cast<size_t>(j) * a.V;
-        l0 = __ldcs(lr + v);
-        l1 = two ? __ldcs(lr + v + 1) : 0.f;
-        draft_gumbel_pair(a.seed, a.offset, 0u, static_cast<uint32_t>(j), static_cast<uint32_t>(v), g0, g1);
-        if (!two) g1 = 0.f;
-    };
-    if (fast) prepare(0, pl0, pl1, pg0, pg1);
     bool alive = true;
     int tc_fail = 0;                                  // tensor path: an MMA wait timed out
     for (int i = 0; i < a.N && alive; ++i) {
@@ -339,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         for (int b = tid; b < a.B; b += kThreads) {
             int p;
             if (i == 0) {
-                p = a.anchor[b];
+                p = b == tid ? anchor_first : a.anchor[b];
                 if (p < 0 || p >= a.V) {
                     set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
                     p = 0;
@@ -355,11 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
         if constexpr (kTC) {
             // E = w1[prev] (bf16, unconverted) is row 0 of the B operand: the anchor's row here,
             // later steps' rows were put there by the exchange
-            if (i == 0 && tid < 8) {
-                const uint4 q = __ldg(reinterpret_cast<const uint4*>(
-                    static_cast<const uint8_t*>(a.w1) + static_cast<size_t>(prev[0]) * (2 * kTcR)) + tid);
-                reinterpret_cast<uint4*>(bop)[tid] = q;
-            }
+            if (i == 0 && tid < 8) reinterpret_cast<uint4*>(bop)[tid] = e_first;
             if (i > 0 && tid == 0) s_win[0] = 0ull;  // every thread read the last winner before the barrier above
             fence_proxy_async_smem();                // operand writes -> the tensor core's view
             tc_fence_before();
@@ -656,10 +689,9 @@ dspark_status run_generic(MarkovArgs& a, cudaStream_t stream, const DeviceInfo& 
     if constexpr (std::is_same<WT, __nv_bfloat16>::value)
         tc = a.B == 1 && a.r == kTcR && a.single_pass && a.lse == nullptr && a.exchange && a.slice <= kTcRows;
     size_t smem = 16;
-    smem += tc ? 1023 + kTcBBytes : a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
+    smem += tc ? 1023 + kTcBBytes + kTcStageBytes : a.w2_cached ? static_cast<size_t>(a.slice) * a.w2_pitch : 0;
     smem += a.z_stored ? sizeof(float) * static_cast<size_t>(a.slice) * a.B : 0;
     smem += sizeof(float) * static_cast<size_t>(a.B) * a.r + sizeof(int) * static_cast<size_t>(a.B);
-    if (tc) smem = std::max(smem, kTcMinSmem);
     if (smem > dev.smem_optin) {
         set_error("markov_sample: needs %zu bytes of shared memory", smem);
         return DSPARK_ERR_UNSUPPORTED;
