@@ -162,6 +162,25 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+class Arena:
+    """One allocation holding several tensors at 256-byte aligned offsets (device, or pinned host
+    memory): a step's inputs (or outputs) then cross between host and device in one copy."""
+
+    def __init__(self, specs, device=None, pin=False):
+        import torch
+        self.offsets, off = {}, 0
+        for name, shape, dtype in specs:
+            nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            self.offsets[name] = (off, shape, dtype, nbytes)
+            off = (off + nbytes + 255) & ~255
+        self.nbytes = off
+        self.buf = torch.empty(off, dtype=torch.uint8, device=device, pin_memory=pin)
+
+    def view(self, name):
+        off, shape, dtype, nbytes = self.offsets[name]
+        return self.buf[off: off + nbytes].view(dtype).view(shape)
+
+
 def run_gpu(args):
     import torch
     import draft_sampling_verification_tcgen05_gb300 as ds
@@ -186,24 +205,24 @@ def run_gpu(args):
     d, v, s, di, vi, si, T = host_inputs(args.workload)
     B, N, V, H, r = d.B, d.N, d.V, d.H, d.r
     M = B * N
-    # device-resident inputs and fixed output buffers
-    X = di["hidden"].to(dev)
+    # device-resident weights; the per-step inputs and the results the host reads back live in
+    # one input and one output arena (one host<->device copy each way in the end-to-end leg)
     W = di["lm_head"].to(dev)
     w1 = di["w1"].to(dev)
     w2 = di["w2"].to(dev)
-    anchor = torch.from_numpy(di["anchor"]).to(dev)
-    temp = torch.from_numpy(T).to(dev)
-    p_t = torch.from_numpy(vi["p_t"]).to(dev)
-    p_d = torch.from_numpy(vi["p_d"]).to(dev)
-    conf = torch.from_numpy(si["cond_accept"]).to(dev)
-    sps = torch.from_numpy(si["sps"]).to(dev)
+    h_in = {"X": di["hidden"], "anchor": torch.from_numpy(di["anchor"]), "temp": torch.from_numpy(T),
+            "p_t": torch.from_numpy(vi["p_t"]), "p_d": torch.from_numpy(vi["p_d"]),
+            "conf": torch.from_numpy(si["cond_accept"]), "sps": torch.from_numpy(si["sps"])}
+    in_specs = [(k, tuple(t.shape), t.dtype) for k, t in h_in.items()]
+    out_specs = [("tok", (B, N), torch.int32), ("out", (B, N + 1), torch.int32), ("nacc", (B,), torch.int32),
+                 ("K_out", (1,), torch.int32), ("lens", (B,), torch.int32)]
+    d_in, d_out = Arena(in_specs, device=dev), Arena(out_specs, device=dev)
+    for k, t in h_in.items():
+        d_in.view(k).copy_(t)
+    X, anchor, temp, p_t, p_d, conf, sps = (d_in.view(k) for k in ("X", "anchor", "temp", "p_t", "p_d", "conf", "sps"))
+    tok, out, nacc, K_out, lens = (d_out.view(k) for k in ("tok", "out", "nacc", "K_out", "lens"))
     L = torch.empty(M, V, dtype=torch.float32, device=dev)
-    tok = torch.empty(B, N, dtype=torch.int32, device=dev)
-    out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
-    nacc = torch.empty(B, dtype=torch.int32, device=dev)
     surv = torch.empty(B, N, dtype=torch.float32, device=dev)
-    K_out = torch.empty(1, dtype=torch.int32, device=dev)
-    lens = torch.empty(B, dtype=torch.int32, device=dev)
     sel = torch.empty(B * N, dtype=torch.int32, device=dev)
     ws_g = ds.Workspace(ds.OP_DRAFT_LOGITS, device=dev)
     ws_m = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
@@ -324,22 +343,14 @@ def run_gpu(args):
     # ---------------- end to end through host buffers ----------------
     e2e = None
     if not args.skip_e2e:
-        h_X = di["hidden"].pin_memory()
-        h_anchor = torch.from_numpy(di["anchor"]).pin_memory()
-        h_T = torch.from_numpy(T).pin_memory()
-        h_pt = torch.from_numpy(vi["p_t"]).pin_memory()
-        h_pd = torch.from_numpy(vi["p_d"]).pin_memory()
-        h_c = torch.from_numpy(si["cond_accept"]).pin_memory()
-        h_sps = torch.from_numpy(si["sps"]).pin_memory()
-        h_out = torch.empty_like(out, device="cpu").pin_memory()
-        h_nacc = torch.empty_like(nacc, device="cpu").pin_memory()
-        h_tok = torch.empty_like(tok, device="cpu").pin_memory()
-        h_K = torch.empty_like(K_out, device="cpu").pin_memory()
-        h_lens = torch.empty_like(lens, device="cpu").pin_memory()
-        ins = [(X, h_X), (anchor, h_anchor), (temp, h_T), (p_t, h_pt), (p_d, h_pd), (conf, h_c), (sps, h_sps)]
-        outs = [(h_tok, tok), (h_out, out), (h_nacc, nacc), (h_K, K_out), (h_lens, lens)]
-        h2d = sum(h.numel() * h.element_size() for _, h in ins)
-        d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+        # the step's inputs in one pinned host arena laid out like the device one (copied whole),
+        # and the results read back whole from the device output arena
+        hin, hout = Arena(in_specs, pin=True), Arena(out_specs, pin=True)
+        for k, t in h_in.items():
+            hin.view(k).copy_(t)
+        ins = [(d_in.buf, hin.buf)]
+        outs = [(hout.buf, d_out.buf)]
+        h2d, d2h = hin.nbytes, hout.nbytes
         e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for k in range(args.warmup + args.steps):
