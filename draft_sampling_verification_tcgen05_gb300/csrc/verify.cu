@@ -5,15 +5,14 @@
 // correction from norm(max(0, p_t - p_d)); if all tested tokens pass, a bonus
 // token is drawn from p_t at the position after the block.
 //
-// Two launches.  The decide kernel (one warp per request) checks all tested
-// positions k < L_b at once, one lane each: fl32(u_k * p_d[x_k]) < p_t[x_k];
-// k* = the smallest failing k.  The stream kernel (two blocks per SM, launched
-// as a programmatic dependent of the decide kernel so that its blocks are
-// resident before k* is known) cuts the B * ceil(V / 512) segments of the
-// rows to stream -- residual rows p_t[k*], p_d[k*] for a rejection, the bonus
-// row p_t[L_b] otherwise -- into equal contiguous ranges, one per block; each
-// warp turns 512 consecutive entries into integer masses q_v = floor(w_v * 2^40)
-// and writes their sum to the workspace.  The block that completes a request's
+// One launch (two blocks per SM).  The B * ceil(V / 512) segments of the rows to
+// stream -- residual rows p_t[k*], p_d[k*] for a rejection, the bonus row p_t[L_b]
+// otherwise -- are cut into equal contiguous ranges, one per block.  A block first
+// decides the requests its range touches, one warp per request checking all tested
+// positions k < L_b at once, one lane each: fl32(u_k * p_d[x_k]) < p_t[x_k]; k* = the
+// smallest failing k (every block touching a request reaches the same k*, so no
+// decision crosses blocks).  Each warp then turns 512 consecutive entries into
+// integer masses q_v = floor(w_v * 2^40) and writes their sum to the workspace.  The block that completes a request's
 // segment count (an atomic counter) then sums the segment masses,
 // t = floor(R * Q / 2^64), finds the segment holding t with a block-wide
 // exclusive scan, re-reads that segment with one warp (128 entries at a time)
@@ -42,7 +41,6 @@ struct VerifyArgs {
     int32_t* n_acc;
     WsHeader* ws;
     uint32_t* done;              // [B] segments finished per request
-    int32_t* decision;           // [B] (k* << 1) | rejected, or -1 for a request with bad input
     unsigned long long* seg;     // [B][n_seg] segment masses
     uint64_t seed;
     uint32_t offset;
@@ -148,18 +146,9 @@ __device__ unsigned long long block_sum_u64(unsigned long long x, unsigned long 
     return s;
 }
 
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-constexpr int kDecideWarps = 8;                  // requests per decide block
-
-// k* of every request: one warp per request, one lane per tested position.
-__global__ void __launch_bounds__(kDecideWarps * 32) verify_decide_kernel(VerifyArgs a) {
-    griddep_launch_dependents();                 // the stream kernel may start launching now
-    const int b = static_cast<int>(blockIdx.x) * kDecideWarps + static_cast<int>(warp_id());
-    if (b >= a.B) return;
+// Decision of request b, (k* << 1) | rejected, or -1 for bad input (then INPUT_RANGE is set);
+// warp-collective, one lane per tested position, the result in every lane.
+__device__ int decide_request(const VerifyArgs& a, int b) {
     const uint32_t lane = lane_id();
     const int V = a.V, g = a.gamma;
     const int Lb = a.lengths != nullptr ? a.lengths[b] : g;
@@ -182,10 +171,8 @@ __global__ void __launch_bounds__(kDecideWarps * 32) verify_decide_kernel(Verify
     }
     bad = __any_sync(0xFFFFFFFFu, bad);
     kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-    if (lane == 0) {
-        a.decision[b] = bad ? -1 : ((kmin << 1) | (kmin < Lb ? 1 : 0));
-        if (bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
-    }
+    if (bad && lane == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+    return bad ? -1 : ((kmin << 1) | (kmin < Lb ? 1 : 0));
 }
 
 // The last block to stream a request draws its token and writes its outputs.
@@ -320,7 +307,8 @@ __device__ void finish_request(const VerifyArgs& a, int b, int dec, unsigned lon
 
 // Streams block blockIdx.x's contiguous range of the B * n_seg row segments.
 __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(VerifyArgs a) {
-    extern __shared__ unsigned long long s_seg[];         // [n_seg] (finishing blocks only)
+    extern __shared__ unsigned long long s_seg[];         // [n_seg] (finishing blocks only), then the
+                                                          // decisions of the block's requests
     __shared__ unsigned long long s_red[kWarps];
     __shared__ unsigned long long s_scan[kWarps];
     __shared__ int s_pick, s_last;
@@ -332,13 +320,21 @@ __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(VerifyArgs a
     const long long T = a.total_seg;
     long long f = T * blockIdx.x / a.grid;
     const long long f1 = T * (blockIdx.x + 1) / a.grid;
+    int* s_dec = reinterpret_cast<int*>(s_seg + n_seg);
 
-    griddep_wait();                                       // every k* is written and visible
+    // the decisions of the requests [b_first, b_last] this block streams, one warp each
+    const int b_first = static_cast<int>(f / n_seg);
+    const int n_req = f < f1 ? static_cast<int>((f1 - 1) / n_seg) - b_first + 1 : 0;
+    for (int j = static_cast<int>(warp_id()); j < n_req; j += kWarps) {
+        const int dec = decide_request(a, b_first + j);
+        if (lane_id() == 0) s_dec[j] = dec;
+    }
+    __syncthreads();
     while (f < f1) {
         const int b = static_cast<int>(f / n_seg);
         const int s0 = static_cast<int>(f - static_cast<long long>(b) * n_seg);
         const int s1 = static_cast<int>(min(static_cast<long long>(n_seg), s0 + (f1 - f)));
-        const int dec = a.decision[b];
+        const int dec = s_dec[b - b_first];
         if (dec >= 0) {
             const int kstar = dec >> 1;
             const float* rt = a.p_t + (static_cast<size_t>(b) * (g + 1) + kstar) * V;
@@ -368,7 +364,7 @@ size_t done_bytes(int B) { return (sizeof(uint32_t) * static_cast<size_t>(B) + 1
 }  // namespace
 
 size_t verify_workspace_bytes(int B, int V) {
-    return sizeof(WsHeader) + 2 * done_bytes(B) + sizeof(unsigned long long) * static_cast<size_t>(B) * n_segments(V);
+    return sizeof(WsHeader) + done_bytes(B) + sizeof(unsigned long long) * static_cast<size_t>(B) * n_segments(V);
 }
 
 dspark_status launch_verify(const float* p_target, const float* p_draft, const int32_t* draft_tokens,
@@ -376,7 +372,13 @@ dspark_status launch_verify(const float* p_target, const float* p_draft, const i
                             int V, int32_t* out_tokens, int32_t* num_accepted, void* ws,
                             cudaStream_t stream, const DeviceInfo& dev) {
     const int n_seg = n_segments(V);
-    const size_t smem = sizeof(unsigned long long) * static_cast<size_t>(n_seg);
+    const long long total_seg = static_cast<long long>(B) * n_seg;
+    // two resident blocks per SM, each streaming at least 2 segments (1024 row entries)
+    const int grid = static_cast<int>(std::max(1LL, std::min(2LL * dev.sm_count, (total_seg + 1) / 2)));
+    // a block's range of at most ceil(total / grid) segments touches at most this many requests
+    const long long per_block = (total_seg + grid - 1) / grid;
+    const long long max_req = (per_block + n_seg - 1) / n_seg + 1;
+    const size_t smem = sizeof(unsigned long long) * static_cast<size_t>(n_seg) + sizeof(int) * static_cast<size_t>(max_req);
     if (smem > dev.smem_optin) {
         set_error("verify: V=%d needs %zu bytes of shared memory", V, smem);
         return DSPARK_ERR_UNSUPPORTED;
@@ -396,37 +398,18 @@ dspark_status launch_verify(const float* p_target, const float* p_draft, const i
     a.ws = static_cast<WsHeader*>(ws);
     uint8_t* p = static_cast<uint8_t*>(ws) + sizeof(WsHeader);
     a.done = reinterpret_cast<uint32_t*>(p);
-    a.decision = reinterpret_cast<int32_t*>(p + done_bytes(B));
-    a.seg = reinterpret_cast<unsigned long long*>(p + 2 * done_bytes(B));
+    a.seg = reinterpret_cast<unsigned long long*>(p + done_bytes(B));
     a.seed = seed;
     a.offset = offset;
     a.B = B;
     a.gamma = gamma;
     a.V = V;
     a.n_seg = n_seg;
-    a.total_seg = static_cast<long long>(B) * n_seg;
-    // two resident blocks per SM, each streaming at least 2 segments (1024 row entries)
-    a.grid = static_cast<int>(std::max(1LL, std::min(2LL * dev.sm_count, (a.total_seg + 1) / 2)));
-
-    const unsigned decide_grid = static_cast<unsigned>((B + kDecideWarps - 1) / kDecideWarps);
-    verify_decide_kernel<<<decide_grid, kDecideWarps * 32, 0, stream>>>(a);
+    a.total_seg = total_seg;
+    a.grid = grid;
+    verify_stream_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "launch(verify decide)");
-
-    // programmatic dependent launch: the stream kernel's blocks become resident while the
-    // decide kernel runs and wait (griddepcontrol.wait) for its results
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, verify_stream_kernel, a);
-    if (e != cudaSuccess) return cuda_error(e, "launch(verify stream)");
+    if (e != cudaSuccess) return cuda_error(e, "launch(verify)");
     return DSPARK_OK;
 }
 
