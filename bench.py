@@ -565,7 +565,7 @@ def run_gpu(args):
                             "achieved": markov_bytes / (kernel_ms[1] / 1e3) / 1e9, "peak": hbm_peak,
                             "unit": "GB/s", "frac": markov_bytes / (kernel_ms[1] / 1e3) / 1e9 / hbm_peak},
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,           # GEMM, Markov sampler, verify decide + stream, schedule
+        "gpu_launches": 4 * args.steps,           # GEMM, Markov sampler, verify, schedule
         "step_launch": "one CUDA graph replay per step" if graph is not None else "four eager calls per step",
         "kernel_ms_note": "per-kernel CUDA-event times from an eager pass over the same K steps",
         "clocks": clk.summary(),
