@@ -2,14 +2,15 @@
  * dspark.h -- C ABI of the DSpark draft-sampling / verification hot path on one
  * GB300 (sm_103a).
  *
- * Four operations, each one or two kernel launches on the caller's stream:
+ * Four operations, each one kernel launch on the caller's stream (after a
+ * memset of the workspace header):
  *
  *   dspark_draft_logits   base logits of the draft LM head (tcgen05 GEMM)
  *   dspark_markov_sample  N-step Markov-biased Gumbel-max sampling (one
  *                         persistent kernel)
  *   dspark_verify         lossless speculative rejection sampling
  *   dspark_schedule       confidence-scheduled admission (survival chain,
- *                         global radix sort, throughput-optimal K, fill)
+ *                         global sort, throughput-optimal K, fill)
  *
  * Conventions shared by every call
  *   - All array arguments are DEVICE pointers on the current CUDA device,
@@ -211,8 +212,7 @@ DSPARK_API dspark_status dspark_markov_sample_reduced(const float* base_logits, 
  * offset < 2^32; p_target/p_draft 16-byte aligned.
  * Device-side: a token or length out of range sets INPUT_RANGE (the request
  * outputs num_accepted 0 and -1 tokens).
- * Launches two kernels on `stream`, the second as a programmatic dependent
- * launch of the first (both are captured by CUDA stream capture).
+ * Launches one kernel on `stream` (captured by CUDA stream capture).
  * workspace: >= dspark_workspace_size(DSPARK_OP_VERIFY, ...) bytes.
  */
 DSPARK_API dspark_status dspark_verify(const float* p_target, const float* p_draft,

@@ -36,7 +36,8 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_workspace_sizes(L):
     assert L.dspark_workspace_size(0, 0, 0, 0, 0) == 256
-    assert L.dspark_workspace_size(2, 256, 8, 151936, 0) == 256 + 2 * 1024 + 8 * 256 * 297
+    # header, per-request segment counters, per-segment masses
+    assert L.dspark_workspace_size(2, 256, 8, 151936, 0) == 256 + 1024 + 8 * 256 * 297
     m = L.dspark_workspace_size(1, 64, 16, 151936, 256)
     assert m >= 256 + 64 * 16 * 12
     assert L.dspark_workspace_size(3, 1024, 16, 0, 0) == 256 + 2 * 8 * 1024 * 16
