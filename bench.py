@@ -3,9 +3,14 @@
 One step = one pass of the whole hot path over one synthetic batch:
     dspark_draft_logits -> dspark_markov_sample -> dspark_verify -> dspark_schedule
 Metric: draft tokens per second (B*N drafted tokens per step), plus the roofline
-fraction of the dominant kernel.
+fraction of the dominant kernel and of the Markov sampler.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gpu|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--secondary NAME|none]
+                  [--impl gpu|reference]
+
+The default workload is the batched serving draft (B=64, N=16, r=256); the
+single-request Qwen3-8B-shaped decode (B=1, N=8) is measured after it in the
+same run and reported in the same JSON line under "secondary".
 
 Under torchrun (N > 1) every rank runs its own replica of the workload on its own
 GPU (requests shard across GPUs with no data exchange: weak scaling); ranks meet
@@ -28,22 +33,20 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import (DRAFT_CONFIGS, VERIFY_CONFIGS, SCHEDULE_CONFIGS, VerifyConfig,  # noqa: E402
-                       ScheduleConfig, draft_inputs, verify_inputs, schedule_inputs, markov_logits)
+from workloads import (DRAFT_CONFIGS, VerifyConfig, ScheduleConfig, draft_inputs,  # noqa: E402
+                       verify_inputs, schedule_inputs)
 
 METRIC = "draft tokens/sec (B·N per draft step) and % of roofline for logits+Markov sampling"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 * 1024 * 1024      # > 4x the 129 MB L2
 WORKLOAD_TEMPERATURE = {"qwen3_8b_single": 1.0, "batched_draft": 0.8, "tiny": 1.0}
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one dspark_draft_logits launch,
-# from one ncu capture per workload (summarised under profiles/), with a digest of the kernel's
-# sources at capture time: once the sources change the figure is reported as null.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one dspark_draft_logits launch on
+# each workload, from one ncu capture of that kernel on that workload, with a digest of the
+# kernel's sources at capture time: once the sources change the figure is reported as null.
 GEMM_TRAFFIC = {
-    "qwen3_8b_single": {"bytes": 1244763648 + 5437696, "src_digest": "c2b6df7bfbe9",
-                        "profile": "profiles/draft_logits_qwen3_8b_single.md"},
-    "batched_draft": {"bytes": 1264973056 + 591100416, "src_digest": "c2b6df7bfbe9",
-                      "profile": "profiles/draft_logits_batched_draft.md"},
+    "qwen3_8b_single": {"bytes": 1244763648 + 5437696, "src_digest": "c2b6df7bfbe9"},
+    "batched_draft": {"bytes": 1264973056 + 591100416, "src_digest": "c2b6df7bfbe9"},
 }
 GEMM_SOURCES = ("draft_sampling_verification_tcgen05_gb300/csrc/draft_logits.cu",
                 "draft_sampling_verification_tcgen05_gb300/csrc/device_common.cuh")
@@ -64,12 +67,15 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="qwen3_8b_single", choices=sorted(DRAFT_CONFIGS))
+    ap.add_argument("--workload", default="batched_draft", choices=sorted(DRAFT_CONFIGS))
+    ap.add_argument("--secondary", default="qwen3_8b_single", choices=sorted(DRAFT_CONFIGS) + ["none"],
+                    help="a second workload measured after the first (GPU figures only)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the four calls eagerly each step")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle sample")
+    ap.add_argument("--oracle-one-request", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -181,28 +187,42 @@ class Arena:
         return self.buf[off: off + nbytes].view(dtype).view(shape)
 
 
-def run_gpu(args):
+def _nvtx(name):
+    """An NVTX range around one C-ABI call (host side; visible in a profiler's timeline)."""
+    import contextlib
+    import torch
+    try:
+        return torch.cuda.nvtx.range(name)
+    except Exception:                             # a build without NVTX: no range
+        return contextlib.nullcontext()
+
+
+def _timed_calls(fn, flush_l2, stream, n=20):
+    """Median CUDA-event time (ms) of `fn` over n launches, L2 flushed before each."""
+    import torch
+    for _ in range(3):
+        fn()
+    ms = []
+    for k in range(n):
+        flush_l2(k)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return float(np.median(ms))
+
+
+def measure(name, args, dev, dist, world, rank, full):
+    """Time the step on workload `name`; with `full`, also the end-to-end leg, the library's
+    other entry points and the oracle leg.  Returns the JSON fields of the line."""
     import torch
     import draft_sampling_verification_tcgen05_gb300 as ds
-    from draft_sampling_verification_tcgen05_gb300 import _build
-    from draft_sampling_verification_tcgen05_gb300.replicas import (job_throughput, max_over_ranks, rank_info,
-                                                                    replica_seed)
+    from draft_sampling_verification_tcgen05_gb300.replicas import job_throughput, max_over_ranks, replica_seed
+    from workloads import zipf_offsets
 
-    ri = rank_info()
-    rank, world, local = ri.rank, ri.world, ri.local_rank
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if rank == 0 or world == 1:
-        _build.build()
-    if dist is not None:
-        dist.barrier()
-    ds.lib()
-
-    d, v, s, di, vi, si, T = host_inputs(args.workload)
+    d, v, s, di, vi, si, T = host_inputs(name)
     B, N, V, H, r = d.B, d.N, d.V, d.H, d.r
     M = B * N
     # device-resident weights; the per-step inputs and the results the host reads back live in
@@ -215,15 +235,14 @@ def run_gpu(args):
             "conf": torch.from_numpy(si["cond_accept"]), "sps": torch.from_numpy(si["sps"])}
     in_specs = [(k, tuple(t.shape), t.dtype) for k, t in h_in.items()]
     out_specs = [("tok", (B, N), torch.int32), ("out", (B, N + 1), torch.int32), ("nacc", (B,), torch.int32),
-                 ("K_out", (1,), torch.int32), ("lens", (B,), torch.int32)]
+                 ("K_out", (1,), torch.int32), ("lens", (B,), torch.int32), ("sel", (B * N,), torch.int32),
+                 ("surv", (B, N), torch.float32)]
     d_in, d_out = Arena(in_specs, device=dev), Arena(out_specs, device=dev)
     for k, t in h_in.items():
         d_in.view(k).copy_(t)
     X, anchor, temp, p_t, p_d, conf, sps = (d_in.view(k) for k in ("X", "anchor", "temp", "p_t", "p_d", "conf", "sps"))
-    tok, out, nacc, K_out, lens = (d_out.view(k) for k in ("tok", "out", "nacc", "K_out", "lens"))
+    tok, out, nacc, K_out, lens, sel, surv = (d_out.view(k) for k in ("tok", "out", "nacc", "K_out", "lens", "sel", "surv"))
     L = torch.empty(M, V, dtype=torch.float32, device=dev)
-    surv = torch.empty(B, N, dtype=torch.float32, device=dev)
-    sel = torch.empty(B * N, dtype=torch.int32, device=dev)
     ws_g = ds.Workspace(ds.OP_DRAFT_LOGITS, device=dev)
     ws_m = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
     ws_v = ds.Workspace(ds.OP_VERIFY, B, N, V, device=dev)
@@ -243,17 +262,15 @@ def run_gpu(args):
 
     # The batched-draft workload defines its Markov-step logits as the base logits plus a
     # per-row Zipf(1.1) rank offset (peaked rows, as real LM logits are).  The offset is not
-    # part of the method, so the GEMM output is offset once before timing and the sampler
-    # reads that buffer; both kernels still do their full work every step.
+    # part of the method: it is drawn on the host (the same rows the oracle leg uses), added to
+    # the GEMM output once before timing, and the sampler reads that buffer; both kernels still
+    # do their full work every step.
     L_markov = L
+    zipf_host = None
     if d.zipf > 0:
+        zipf_host = zipf_offsets(d)
         ds.dspark_draft_logits(X, W, logits=L, workspace=ws_g)
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(d.data_seed)
-        base_off = -d.zipf * torch.log(torch.arange(1, V + 1, device=dev, dtype=torch.float64)).float()
-        L_markov = torch.empty_like(L)
-        for row in range(M):
-            L_markov[row].index_copy_(0, torch.randperm(V, device=dev, generator=gen), base_off)
+        L_markov = torch.from_numpy(zipf_host).to(dev)
         L_markov += L
         torch.cuda.synchronize()
 
@@ -263,15 +280,19 @@ def run_gpu(args):
     def step(k=None):
         e = ev[k] if k is not None else None
         if e: e[0].record(stream)
-        ds.dspark_draft_logits(X, W, logits=L, workspace=ws_g)
+        with _nvtx("dspark_draft_logits"):
+            ds.dspark_draft_logits(X, W, logits=L, workspace=ws_g)
         if e: e[1].record(stream)
-        ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, draft_tokens=tok,
-                                workspace=ws_m)
+        with _nvtx("dspark_markov_sample"):
+            ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, draft_tokens=tok,
+                                    workspace=ws_m)
         if e: e[2].record(stream)
-        ds.dspark_verify(p_t, p_d, tok, None, seed_verify, 0, out_tokens=out, num_accepted=nacc, workspace=ws_v)
+        with _nvtx("dspark_verify"):
+            ds.dspark_verify(p_t, p_d, tok, None, seed_verify, 0, out_tokens=out, num_accepted=nacc, workspace=ws_v)
         if e: e[3].record(stream)
-        ds.dspark_schedule(conf, sps, -1, survival=surv, K_out=K_out, lengths=lens, selected=sel,
-                           workspace=ws_s)
+        with _nvtx("dspark_schedule"):
+            ds.dspark_schedule(conf, sps, -1, survival=surv, K_out=K_out, lengths=lens, selected=sel,
+                               workspace=ws_s)
         if e: e[4].record(stream)
 
     for _ in range(args.warmup):
@@ -340,156 +361,7 @@ def run_gpu(args):
     step_ms = max_over_ranks(step_ms, dist, dev)
     value = job_throughput(M, world, step_ms)
 
-    # ---------------- end to end through host buffers ----------------
-    e2e = None
-    if not args.skip_e2e:
-        # the step's inputs in one pinned host arena laid out like the device one (copied whole),
-        # and the results read back whole from the device output arena
-        hin, hout = Arena(in_specs, pin=True), Arena(out_specs, pin=True)
-        for k, t in h_in.items():
-            hin.view(k).copy_(t)
-        ins = [(d_in.buf, hin.buf)]
-        outs = [(hout.buf, d_out.buf)]
-        h2d, d2h = hin.nbytes, hout.nbytes
-        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        for k in range(args.warmup + args.steps):
-            timed = k >= args.warmup
-            flush_l2(k)
-            if timed:
-                e0[k - args.warmup].record(stream)
-            for dst, src in ins:
-                dst.copy_(src, non_blocking=True)
-            step()
-            for dst, src in outs:
-                dst.copy_(src, non_blocking=True)
-            if timed:
-                e1[k - args.warmup].record(stream)
-            stream.synchronize()
-        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(e0, e1)]))
-        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
-        e2e = {"value": job_throughput(M, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
-
-    # ---------------- the library's other entry points, timed on their own ----------------
-    # greedy verification of the step's draft tokens against the same target rows (all rows
-    # k <= gamma are read)
-    ws_g2 = ds.Workspace(ds.OP_VERIFY_GREEDY, B, N, device=dev)
-    g_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
-    g_nacc = torch.empty(B, dtype=torch.int32, device=dev)
-    for _ in range(3):
-        ds.dspark_verify_greedy(p_t, tok, None, out_tokens=g_out, num_accepted=g_nacc, workspace=ws_g2)
-    g_ms = []
-    for k in range(20):
-        flush_l2(k)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ds.dspark_verify_greedy(p_t, tok, None, out_tokens=g_out, num_accepted=g_nacc, workspace=ws_g2)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        g_ms.append(e0.elapsed_time(e1))
-    greedy_ms = float(np.median(g_ms))
-    # calibrated confidence head on the step's hidden rows and draft tokens (synthetic head weights)
-    hrng = np.random.default_rng(d.data_seed + 7)
-    w_h = torch.from_numpy((hrng.standard_normal(H) / np.sqrt(H)).astype(np.float32)).to(dev)
-    w_e = torch.from_numpy((hrng.standard_normal(r) / np.sqrt(r)).astype(np.float32)).to(dev)
-    tau = torch.from_numpy(hrng.uniform(0.7, 1.6, N).astype(np.float32)).to(dev)
-    ws_c = ds.Workspace(ds.OP_CONFIDENCE, B, N, V, r, device=dev)
-    conf_out = torch.empty(B, N, dtype=torch.float32, device=dev)
-    for _ in range(3):
-        ds.dspark_confidence(X, w1, anchor, tok, w_h, w_e, 0.5, tau, conf=conf_out, workspace=ws_c)
-    c_ms = []
-    for k in range(20):
-        flush_l2(k)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ds.dspark_confidence(X, w1, anchor, tok, w_h, w_e, 0.5, tau, conf=conf_out, workspace=ws_c)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        c_ms.append(e0.elapsed_time(e1))
-    conf_ms = float(np.median(c_ms))
-    conf_bytes = M * H * X.element_size() + M * r * w1.element_size() + (H + r + N) * 4 + M * 4
-    # the sampler on an EAGLE-3-sized reduced draft vocabulary (first 32000 entries of the step's
-    # logits and Markov head, ids mapped into the target vocabulary through an index table)
-    Vd = min(32000, V)
-    L_red = L_markov.view(B, N, V)[:, :, :Vd].contiguous()
-    w1_red, w2_red = w1[:Vd].contiguous(), w2[:Vd].contiguous()
-    d2t = torch.from_numpy(np.sort(np.random.default_rng(d.data_seed + 8).choice(V, Vd, replace=False))
-                           .astype(np.int32)).to(dev)
-    ws_r = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, Vd, r, device=dev)
-    tok_red = torch.empty(B, N, dtype=torch.int32, device=dev)
-    red_args = (L_red, anchor % Vd, w1_red, w2_red, temp, seed_draft, 0, d2t, ds.D2T_INDEX, V)
-    for _ in range(3):
-        ds.dspark_markov_sample_reduced(*red_args, draft_tokens=tok_red, workspace=ws_r)
-    r_ms = []
-    for k in range(20):
-        flush_l2(k)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ds.dspark_markov_sample_reduced(*red_args, draft_tokens=tok_red, workspace=ws_r)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        r_ms.append(e0.elapsed_time(e1))
-    red_ms = float(np.median(r_ms))
-    # verification straight from logits (the draft distribution never written): target logits
-    # log p_t of the step's target rows, the step's draft base logits, tokens and sampler lse
-    lse_d = torch.empty(B, N, dtype=torch.float32, device=dev)
-    ws_m2 = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
-    ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, draft_tokens=tok,
-                            lse=lse_d, workspace=ws_m2)
-    # target logits that follow the draft: the draft's base logit rows (the last one again for the
-    # bonus position) plus N(0, sigma_b^2) noise, sigma_b in {0.3, 1, 3} per request
-    gen_t = torch.Generator(device=dev)
-    gen_t.manual_seed(d.data_seed + 9)
-    sig = torch.tensor([0.3, 1.0, 3.0], device=dev)[torch.randint(0, 3, (B,), generator=gen_t, device=dev)]
-    Lm = L_markov.view(B, N, V)
-    t_logits = torch.cat([Lm, Lm[:, -1:]], dim=1) + sig[:, None, None] * torch.randn(
-        B, N + 1, V, generator=gen_t, device=dev)
-    del Lm
-    T_t = torch.ones(B, dtype=torch.float32, device=dev)
-    ws_l = ds.Workspace(ds.OP_VERIFY_LOGITS, B, N, V, r, device=dev)
-    l_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
-    l_nacc = torch.empty(B, dtype=torch.int32, device=dev)
-    vl_args = (t_logits, T_t, L_markov.view(B, N, V), anchor, w1, w2, temp, lse_d, tok, None, seed_verify, 0)
-    for _ in range(3):
-        ds.dspark_verify_logits(*vl_args, out_tokens=l_out, num_accepted=l_nacc, workspace=ws_l)
-    l_ms = []
-    for k in range(20):
-        flush_l2(k)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ds.dspark_verify_logits(*vl_args, out_tokens=l_out, num_accepted=l_nacc, workspace=ws_l)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        l_ms.append(e0.elapsed_time(e1))
-    vlog_ms = float(np.median(l_ms))
-    # bytes a request needs: its target rows k <= k* once for the normalisers (k* = the number
-    # accepted, N if none was rejected) and row k* once more for the draw; the draft's base logits
-    # and Markov rows are read only at the few candidate entries
-    vlog_rows = int((l_nacc.long() + 2).sum().item())
-    vlog_bytes = vlog_rows * V * 4
-    # verification with the draft's own Gumbel noise on the same target logits (the draft's
-    # temperature for the target, the sampler's seed and offset); all rows k <= gamma are read
-    ws_gu = ds.Workspace(ds.OP_VERIFY_GUMBEL, B, N, device=dev)
-    gu_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
-    gu_nacc = torch.empty(B, dtype=torch.int32, device=dev)
-    gu_args = (t_logits, temp, tok, None, seed_draft, 0)
-    for _ in range(3):
-        ds.dspark_verify_gumbel(*gu_args, out_tokens=gu_out, num_accepted=gu_nacc, workspace=ws_gu)
-    gu_ms = []
-    for k in range(20):
-        flush_l2(k)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ds.dspark_verify_gumbel(*gu_args, out_tokens=gu_out, num_accepted=gu_nacc, workspace=ws_gu)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        gu_ms.append(e0.elapsed_time(e1))
-    gumbel_ms = float(np.median(gu_ms))
-    gumbel_bytes = B * (N + 1) * V * 4
-    del ws_l, ws_m2, t_logits
-
-    # ---------------- roofline of the dominant kernel ----------------
+    # ---------------- roofline of the dominant kernel and of the sampler ----------------
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -507,72 +379,227 @@ def run_gpu(args):
     gemm_bound = "hbm" if gemm_bytes / (hbm_peak * 1e9) >= gemm_flops / (bf16_peak * 1e12) else "tensor"
     if gemm_bound == "hbm":
         ach = gemm_bytes / t_gemm / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak}
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                "algorithmic_bytes_per_launch": gemm_bytes}
     else:
         ach = gemm_flops / t_gemm / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s", "frac": ach / bf16_peak}
+        roof = {"bound": "tensor", "achieved": ach, "peak": bf16_peak, "unit": "TFLOP/s", "frac": ach / bf16_peak,
+                "algorithmic_flops_per_launch": gemm_flops}
     roof["kernel"] = "dspark_draft_logits"
     roof["peak_source"] = peak_src
-    tr = GEMM_TRAFFIC.get(args.workload)
+    tr = GEMM_TRAFFIC.get(name)
     roof["traffic"] = tr["bytes"] if tr is not None and tr["src_digest"] == gemm_source_digest() else None
     if roof["traffic"] is not None:
-        roof["traffic_source"] = tr["profile"]
-
-    if dist is not None and rank != 0:
-        dist.barrier()
-        dist.destroy_process_group()
-        return
+        roof["traffic_source"] = ("dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture of "
+                                  f"dspark_draft_logits on {name}")
+    markov_roof = {"bound": "hbm", "algorithmic_bytes": markov_bytes,
+                   "achieved": markov_bytes / (kernel_ms[1] / 1e3) / 1e9, "peak": hbm_peak,
+                   "unit": "GB/s", "frac": markov_bytes / (kernel_ms[1] / 1e3) / 1e9 / hbm_peak,
+                   "peak_source": peak_src}
 
     res = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": d.dtype, "data": "synthetic",
+        "value": value, "ms_per_step": step_ms, "dtype": d.dtype,
         "config": {"workload": f"{d.name}: B={B} N={N} H={H} V={V} r={r} {d.dtype} "
-                               f"T={WORKLOAD_TEMPERATURE[args.workload]}, verify gamma={N}, "
+                               f"T={WORKLOAD_TEMPERATURE[name]}, verify gamma={N}, "
                                f"schedule over B*N={M} candidates",
                    "global_batch_requests": B * world, "draft_tokens_per_step": M * world,
                    "parallelism": f"replicas x{world} (requests sharded, no collective)",
                    "l2": "flushed between timed steps: 512 MB write, then a 256 MB read-back that evicts the dirty lines",
-                   "markov_input": ("base logits + per-row Zipf(1.1) rank offset, offset applied once "
-                                    "before timing" if d.zipf > 0 else "this step's base logits")},
+                   "markov_input": ("base logits + per-row Zipf(1.1) rank offset (seeded host draw), offset "
+                                    "applied once before timing" if d.zipf > 0 else "this step's base logits")},
         "kernel_ms": {"draft_logits": kernel_ms[0], "markov_sample": kernel_ms[1],
                       "verify": kernel_ms[2], "schedule": kernel_ms[3]},
         "roofline": roof,
-        "markov_sample_reduced_vocab": {"ms": red_ms, "draft_vocab": Vd, "target_vocab": V,
-                                        "note": "median of 20 launches, L2 flushed, outside the step"},
-        "confidence": {"ms": conf_ms, "bound": "hbm", "algorithmic_bytes": conf_bytes,
-                       "achieved": conf_bytes / (conf_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                       "frac": conf_bytes / (conf_ms / 1e3) / 1e9 / hbm_peak,
-                       "note": "median of 20 launches, L2 flushed, outside the step (latency-bound at these sizes)"},
-        "verify_logits": {"ms": vlog_ms, "bound": "hbm", "algorithmic_bytes": vlog_bytes,
-                          "achieved": vlog_bytes / (vlog_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                          "frac": vlog_bytes / (vlog_ms / 1e3) / 1e9 / hbm_peak,
-                          "accepted_mean": float(l_nacc.float().mean().item()),
-                          "target": "the draft's base-logit rows + N(0, s^2), s in {0.3, 1, 3} per request",
-                          "note": "median of 20 calls (2 kernels), L2 flushed, outside the step; bytes = "
-                                  "target rows k <= k* plus row k* again, from the measured k*"},
-        "verify_gumbel": {"ms": gumbel_ms, "bound": "hbm", "algorithmic_bytes": gumbel_bytes,
-                          "achieved": gumbel_bytes / (gumbel_ms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                          "frac": gumbel_bytes / (gumbel_ms / 1e3) / 1e9 / hbm_peak,
-                          "accepted_mean": float(gu_nacc.float().mean().item()),
-                          "note": "median of 20 launches, L2 flushed, outside the step; target logits as for "
-                                  "verify_logits, the draft's temperature and noise"},
-        "verify_greedy": {"ms": greedy_ms, "bound": "hbm", "algorithmic_bytes": B * (N + 1) * V * 4,
-                          "achieved": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9, "peak": hbm_peak,
-                          "unit": "GB/s", "frac": B * (N + 1) * V * 4 / (greedy_ms / 1e3) / 1e9 / hbm_peak,
-                          "note": "median of 20 launches, L2 flushed, outside the step"},
-        "markov_roofline": {"bound": "hbm", "algorithmic_bytes": markov_bytes,
-                            "achieved": markov_bytes / (kernel_ms[1] / 1e3) / 1e9, "peak": hbm_peak,
-                            "unit": "GB/s", "frac": markov_bytes / (kernel_ms[1] / 1e3) / 1e9 / hbm_peak},
-        "e2e": e2e,
+        "markov_roofline": markov_roof,
         "gpu_launches": 4 * args.steps,           # GEMM, Markov sampler, verify, schedule
         "step_launch": "one CUDA graph replay per step" if graph is not None else "four eager calls per step",
         "kernel_ms_note": "per-kernel CUDA-event times from an eager pass over the same K steps",
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
+    if not full:
+        return res
+
+    # the step's outputs, read once for the oracle leg and the acceptance figures
+    gpu_step = {"tok": tok.cpu().numpy(), "out": out.cpu().numpy(), "nacc": nacc.cpu().numpy(),
+                "K": int(K_out.item()), "lens": lens.cpu().numpy(), "sel": sel.cpu().numpy(),
+                "surv": surv.cpu().numpy()}
+    tested = gpu_step["nacc"] + (gpu_step["nacc"] < N)
+    res["step_verify"] = {"accepted_mean": float(gpu_step["nacc"].mean()),
+                          "acceptance_rate": float(gpu_step["nacc"].sum() / max(1, tested.sum())),
+                          "note": "empirical, over the step's requests: accepted tokens / tested positions "
+                                  "(Markov draft tokens against the verify workload's p_t, p_d)"}
+
+    # ---------------- end to end through host buffers ----------------
+    e2e = None
+    if not args.skip_e2e:
+        # the step's inputs in one pinned host arena laid out like the device one (copied whole),
+        # and the results read back whole from the device output arena
+        hin, hout = Arena(in_specs, pin=True), Arena(out_specs, pin=True)
+        for k, t in h_in.items():
+            hin.view(k).copy_(t)
+        h2d, d2h = hin.nbytes, hout.nbytes
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for k in range(args.warmup + args.steps):
+            timed = k >= args.warmup
+            flush_l2(k)
+            if timed:
+                e0[k - args.warmup].record(stream)
+            d_in.buf.copy_(hin.buf, non_blocking=True)
+            step()
+            hout.buf.copy_(d_out.buf, non_blocking=True)
+            if timed:
+                e1[k - args.warmup].record(stream)
+            stream.synchronize()
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(e0, e1)]))
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+        e2e = {"value": job_throughput(M, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+    res["e2e"] = e2e
+
+    # ---------------- the library's other entry points, timed on their own ----------------
+    # greedy verification of the step's draft tokens against the same target rows (all rows
+    # k <= gamma are read)
+    ws_g2 = ds.Workspace(ds.OP_VERIFY_GREEDY, B, N, device=dev)
+    g_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    g_nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    greedy_ms = _timed_calls(lambda: ds.dspark_verify_greedy(p_t, tok, None, out_tokens=g_out, num_accepted=g_nacc,
+                                                             workspace=ws_g2), flush_l2, stream)
+    # calibrated confidence head on the step's hidden rows and draft tokens (synthetic head weights)
+    hrng = np.random.default_rng(d.data_seed + 7)
+    w_h = torch.from_numpy((hrng.standard_normal(H) / np.sqrt(H)).astype(np.float32)).to(dev)
+    w_e = torch.from_numpy((hrng.standard_normal(r) / np.sqrt(r)).astype(np.float32)).to(dev)
+    tau = torch.from_numpy(hrng.uniform(0.7, 1.6, N).astype(np.float32)).to(dev)
+    ws_c = ds.Workspace(ds.OP_CONFIDENCE, B, N, V, r, device=dev)
+    conf_out = torch.empty(B, N, dtype=torch.float32, device=dev)
+    conf_ms = _timed_calls(lambda: ds.dspark_confidence(X, w1, anchor, tok, w_h, w_e, 0.5, tau, conf=conf_out,
+                                                        workspace=ws_c), flush_l2, stream)
+    conf_bytes = M * H * X.element_size() + M * r * w1.element_size() + (H + r + N) * 4 + M * 4
+    # the sampler on an EAGLE-3-sized reduced draft vocabulary (first 32000 entries of the step's
+    # logits and Markov head, ids mapped into the target vocabulary through an index table)
+    Vd = min(32000, V)
+    L_red = L_markov.view(B, N, V)[:, :, :Vd].contiguous()
+    w1_red, w2_red = w1[:Vd].contiguous(), w2[:Vd].contiguous()
+    d2t = torch.from_numpy(np.sort(np.random.default_rng(d.data_seed + 8).choice(V, Vd, replace=False))
+                           .astype(np.int32)).to(dev)
+    ws_r = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, Vd, r, device=dev)
+    tok_red = torch.empty(B, N, dtype=torch.int32, device=dev)
+    red_args = (L_red, anchor % Vd, w1_red, w2_red, temp, seed_draft, 0, d2t, ds.D2T_INDEX, V)
+    red_ms = _timed_calls(lambda: ds.dspark_markov_sample_reduced(*red_args, draft_tokens=tok_red, workspace=ws_r),
+                          flush_l2, stream)
+    del L_red
+    # verification straight from logits (the draft distribution never written): target logits
+    # log p_t of the step's target rows, the step's draft base logits, tokens and sampler lse
+    lse_d = torch.empty(B, N, dtype=torch.float32, device=dev)
+    ws_m2 = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
+    tok_l = torch.empty(B, N, dtype=torch.int32, device=dev)
+    ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, draft_tokens=tok_l,
+                            lse=lse_d, workspace=ws_m2)
+    # target logits that follow the draft: the draft's base logit rows (the last one again for the
+    # bonus position) plus N(0, sigma_b^2) noise, sigma_b in {0.3, 1, 3} per request
+    gen_t = torch.Generator(device=dev)
+    gen_t.manual_seed(d.data_seed + 9)
+    sig = torch.tensor([0.3, 1.0, 3.0], device=dev)[torch.randint(0, 3, (B,), generator=gen_t, device=dev)]
+    Lm = L_markov.view(B, N, V)
+    t_logits = torch.cat([Lm, Lm[:, -1:]], dim=1) + sig[:, None, None] * torch.randn(
+        B, N + 1, V, generator=gen_t, device=dev)
+    del Lm
+    T_t = torch.ones(B, dtype=torch.float32, device=dev)
+    ws_l = ds.Workspace(ds.OP_VERIFY_LOGITS, B, N, V, r, device=dev)
+    l_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    l_nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    vl_args = (t_logits, T_t, L_markov.view(B, N, V), anchor, w1, w2, temp, lse_d, tok_l, None, seed_verify, 0)
+    vlog_ms = _timed_calls(lambda: ds.dspark_verify_logits(*vl_args, out_tokens=l_out, num_accepted=l_nacc,
+                                                           workspace=ws_l), flush_l2, stream)
+    # bytes a request needs: its target rows k <= k* once for the normalisers (k* = the number
+    # accepted, N if none was rejected) and row k* once more for the draw; the draft's base logits
+    # and Markov rows are read only at the few candidate entries
+    vlog_rows = int((l_nacc.long() + 2).sum().item())
+    vlog_bytes = vlog_rows * V * 4
+    # verification with the draft's own Gumbel noise on the same target logits (the draft's
+    # temperature for the target, the sampler's seed and offset); all rows k <= gamma are read
+    ws_gu = ds.Workspace(ds.OP_VERIFY_GUMBEL, B, N, device=dev)
+    gu_out = torch.empty(B, N + 1, dtype=torch.int32, device=dev)
+    gu_nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    gu_args = (t_logits, temp, tok_l, None, seed_draft, 0)
+    gumbel_ms = _timed_calls(lambda: ds.dspark_verify_gumbel(*gu_args, out_tokens=gu_out, num_accepted=gu_nacc,
+                                                             workspace=ws_gu), flush_l2, stream)
+    gumbel_bytes = B * (N + 1) * V * 4
+    del ws_l, ws_m2, t_logits
+
+    def hbm_entry(ms, nbytes, note, **extra):
+        e = {"ms": ms, "bound": "hbm", "algorithmic_bytes": nbytes, "achieved": nbytes / (ms / 1e3) / 1e9,
+             "peak": hbm_peak, "unit": "GB/s", "frac": nbytes / (ms / 1e3) / 1e9 / hbm_peak, "note": note}
+        e.update(extra)
+        return e
+
+    res["markov_sample_reduced_vocab"] = {"ms": red_ms, "draft_vocab": Vd, "target_vocab": V,
+                                          "note": "median of 20 launches, L2 flushed, outside the step"}
+    res["confidence"] = hbm_entry(conf_ms, conf_bytes, "median of 20 launches, L2 flushed, outside the step "
+                                                       "(latency-bound at these sizes)")
+    res["verify_logits"] = hbm_entry(vlog_ms, vlog_bytes,
+                                     "median of 20 calls (2 kernels), L2 flushed, outside the step; bytes = "
+                                     "target rows k <= k* plus row k* again, from the measured k*",
+                                     accepted_mean=float(l_nacc.float().mean().item()),
+                                     target="the draft's base-logit rows + N(0, s^2), s in {0.3, 1, 3} per request")
+    res["verify_gumbel"] = hbm_entry(gumbel_ms, gumbel_bytes,
+                                     "median of 20 launches, L2 flushed, outside the step; target logits as for "
+                                     "verify_logits, the draft's temperature and noise",
+                                     accepted_mean=float(gu_nacc.float().mean().item()))
+    res["verify_greedy"] = hbm_entry(greedy_ms, B * (N + 1) * V * 4,
+                                     "median of 20 launches, L2 flushed, outside the step")
+    res["_oracle_inputs"] = (d, v, s, di, vi, si, T, None if zipf_host is None else zipf_host.__getitem__,
+                             gpu_step)
+    return res
+
+
+def run_gpu(args):
+    import torch
+    import draft_sampling_verification_tcgen05_gb300 as ds
+    from draft_sampling_verification_tcgen05_gb300 import _build
+    from draft_sampling_verification_tcgen05_gb300.replicas import rank_info
+
+    ri = rank_info()
+    rank, world, local = ri.rank, ri.world, ri.local_rank
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    ds.lib()
+
+    main_res = measure(args.workload, args, dev, dist, world, rank, full=True)
+    oracle_inputs = main_res.pop("_oracle_inputs")
+    secondary = None
+    if args.secondary != "none" and args.secondary != args.workload:
+        torch.cuda.empty_cache()
+        sec = measure(args.secondary, args, dev, dist, world, rank, full=False)
+        secondary = {"workload": sec["config"]["workload"], "value": sec["value"], "unit": UNIT,
+                     "ms_per_step": sec["ms_per_step"], "kernel_ms": sec["kernel_ms"],
+                     "roofline": sec["roofline"], "markov_roofline": sec["markov_roofline"],
+                     "clocks": sec["clocks"], "gpu_launches": sec["gpu_launches"],
+                     "note": "same step, timing and L2 flush as the headline workload"}
+
+    if dist is not None and rank != 0:
+        dist.barrier()
+        dist.destroy_process_group()
+        return
+
+    res = {"metric": METRIC, "value": main_res.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": main_res.pop("ms_per_step"), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": main_res.pop("dtype"), "data": "synthetic"}
+    res.update(main_res)
+    if secondary is not None:
+        res["gpu_launches"] += secondary["gpu_launches"]
+        res["secondary"] = secondary
     if not args.skip_cpu_baseline and rank == 0:
-        res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, (d, v, s, di, vi, si, T))
+        res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, oracle_inputs)
     print(json.dumps(res))
     if dist is not None:
         dist.barrier()
@@ -593,33 +620,101 @@ def _blas_threads():
     return os.cpu_count() or 1
 
 
-def oracle_step(name, inputs, req):
-    """The whole hot path on the CPU oracle for the requests `req` of one batch."""
+def oracle_step(inputs, req, gpu=None, parity=None):
+    """The whole hot path on the CPU oracle for the requests `req` of one batch.
+
+    With `gpu` (the GPU step's outputs), the sampler runs teacher-forced on the GPU's draft
+    tokens and verification takes the GPU's tokens, so that `parity` can count how the two
+    agree (the oracle's work per step is the same either way)."""
     import oracle
-    d, v, s, di, vi, si, T = inputs
+    d, v, s, di, vi, si, T, zipf_of = inputs[:8]
     rows = (req[:, None] * d.N + np.arange(d.N)[None, :]).reshape(-1)
-    Lr = oracle.draft_logits(di["hidden_f32"][rows], di["lm_head_f32"]).reshape(len(req), d.N, d.V)
-    tok, _, _ = oracle.markov_sample(Lr, di["anchor"][req], di["w1_f32"], di["w2_f32"], T[req], 0, 0,
-                                     req_ids=req)
-    oracle.verify(vi["p_t"][req], vi["p_d"][req], tok, None, 2, 0, req_ids=req)
+    Lr = oracle.draft_logits(di["hidden_f32"][rows], di["lm_head_f32"])
+    if zipf_of is not None:
+        Lr = Lr + zipf_of(rows)
+    Lr = Lr.reshape(len(req), d.N, d.V)
+    forced = None if gpu is None else gpu["tok"][req].astype(np.int64)
+    tok, gap, _ = oracle.markov_sample(Lr, di["anchor"][req], di["w1_f32"], di["w2_f32"], T[req], 0, 0,
+                                       req_ids=req, forced_tokens=forced)
+    x = tok if gpu is None else forced
+    out, nacc, _, _ = oracle.verify(vi["p_t"][req], vi["p_d"][req], x, None, 2, 0, req_ids=req)
     oracle.schedule(si["cond_accept"][req], si["sps"][: len(req) * d.N], -1)
+    if parity is not None and gpu is not None:
+        diff = tok != forced
+        parity["markov_compared"] += int(tok.size)
+        parity["markov_near_tie"] += int((diff & (gap < 5e-2)).sum())
+        parity["markov_mismatch"] += int((diff & (gap >= 5e-2)).sum())
+        parity["verify_compared"] += len(req)
+        parity["verify_mismatch"] += int(np.sum(np.any(out != gpu["out"][req], axis=1) | (nacc != gpu["nacc"][req])))
     return len(req) * d.N
 
 
+ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def oracle_single_thread(name):
+    """One request of the workload through the oracle in a child process whose BLAS runs on one
+    thread (numpy's own array work is single-threaded already)."""
+    env = dict(os.environ, **{k: "1" for k in ONE_THREAD_ENV})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-request", "--workload", name],
+                       env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"unavailable": (r.stderr.strip().splitlines() or ["child failed"])[-1]}
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": line["tokens"] / line["seconds"], "unit": UNIT, "cores": 1,
+            "sample": f"1 request: {line['tokens']} draft tokens in {line['seconds']:.1f} s (BLAS on 1 thread)"}
+
+
+def run_oracle_one_request(args):
+    from workloads import zipf_offsets
+    d, v, s = step_configs(args.workload)
+    di = draft_inputs(d)
+    vi = verify_inputs(v, B=1)
+    si = schedule_inputs(s, B=1)
+    T = np.full(d.B, WORKLOAD_TEMPERATURE[args.workload], np.float32)
+    zipf_of = (lambda rows: zipf_offsets(d, rows)) if d.zipf > 0 else None
+    t0 = time.perf_counter()
+    n = oracle_step((d, v, s, di, vi, si, T, zipf_of), np.array([0]))
+    print(json.dumps({"tokens": n, "seconds": time.perf_counter() - t0}))
+
+
 def cpu_baseline(name, budget_s, inputs):
+    """The oracle, as it stands, on a bounded sample of the workload's requests: all BLAS threads
+    (about budget_s seconds), then one request on one thread.  The sampled requests are compared
+    with the GPU step's outputs (teacher-forced sampler, verification on the GPU's tokens), and
+    the full scheduling pool is scheduled by the oracle and compared bit for bit."""
+    import oracle
     d = inputs[0]
+    gpu = inputs[8]
+    si = inputs[5]
+    parity = {"markov_compared": 0, "markov_near_tie": 0, "markov_mismatch": 0,
+              "verify_compared": 0, "verify_mismatch": 0}
     t0 = time.perf_counter()
     tokens = 0
     b = 0
+    stride = max(1, d.B // 8 + 1) if d.B > 1 else 1
     while True:
-        tokens += oracle_step(name, inputs, np.array([b % d.B]))
+        req = np.array([(b * stride) % d.B])
+        tokens += oracle_step(inputs, req, gpu, parity)
         b += 1
-        if time.perf_counter() - t0 >= budget_s or b >= 64:
+        if time.perf_counter() - t0 >= budget_s or b >= d.B:
             break
     el = time.perf_counter() - t0
+    one = oracle_single_thread(name)
+    rs = oracle.schedule(si["cond_accept"], si["sps"], -1)
+    sched_ok = (rs["K"] == gpu["K"] and np.array_equal(rs["lengths"], gpu["lens"])
+                and np.array_equal(rs["selected"], gpu["sel"]) and np.array_equal(rs["survival"], gpu["surv"]))
+    parity["schedule_pool"] = int(si["cond_accept"].size)
+    parity["schedule_bit_exact"] = bool(sched_ok)
+    parity["note"] = ("sampled requests: the oracle's tokens teacher-forced on the GPU step's tokens (a token "
+                      "may differ only at an oracle top-2 gap < 5e-2: near_tie; mismatch counts the rest), "
+                      "verification of the GPU's tokens compared bit for bit per request; the whole "
+                      "scheduling pool compared bit for bit")
     return {"value": tokens / el, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{b} request(s) of {d.name} through the whole path on the CPU oracle "
-                      f"(fp64 numpy): {tokens} draft tokens in {el:.1f} s"}
+                      f"(fp64 numpy): {tokens} draft tokens in {el:.1f} s",
+            "single_thread": one,
+            "parity": parity}
 
 
 def run_reference(args):
@@ -627,17 +722,22 @@ def run_reference(args):
     if rank != 0:
         return
     d, v, s, di, vi, si, T = host_inputs(args.workload)
-    inputs = (d, v, s, di, vi, si, T)
+    zipf_of = None
+    if d.zipf > 0:
+        from workloads import zipf_offsets
+        zipf_host = zipf_offsets(d)
+        zipf_of = zipf_host.__getitem__
+    inputs = (d, v, s, di, vi, si, T, zipf_of)
     per_step_budget = max(1.0, args.cpu_seconds / max(1, args.steps))
     for _ in range(args.warmup):
-        oracle_step(args.workload, inputs, np.array([0]))
+        oracle_step(inputs, np.array([0]))
     times, toks = [], 0
     for k in range(args.steps):
         t0 = time.perf_counter()
         n = 0
         b = k
         while True:
-            n += oracle_step(args.workload, inputs, np.array([b % d.B]))
+            n += oracle_step(inputs, np.array([b % d.B]))
             b += args.steps
             if time.perf_counter() - t0 >= per_step_budget or n >= d.B * d.N:
                 break
@@ -658,7 +758,9 @@ def run_reference(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.oracle_one_request:
+        run_oracle_one_request(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

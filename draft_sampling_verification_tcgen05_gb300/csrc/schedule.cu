@@ -714,9 +714,11 @@ dspark_status launch_schedule(const float* cond_accept, const double* sps, int S
 // never block (cudaMalloc and cudaFree can synchronise with work already queued
 // on the device), or a host whose device memory is entirely reserved by another
 // allocator (a framework's memory pool), where a fresh allocation would fail.
-// For them the scratch that dspark_schedule takes from its workspace (a status
-// header and two radix-sort key buffers) lives here instead, in one fixed array
-// that every GPU loading the library holds until the process exits.
+// For them the scratch that dspark_schedule takes from its workspace lives here
+// instead, in one fixed array that every GPU loading the library holds until the
+// process exits.  Pools of up to kSmemMaxCandidates candidates sort in shared
+// memory, so the only global scratch they use is the workspace header (status
+// word and wait bookkeeping); the array is exactly that header.
 // ---------------------------------------------------------------------------
 #include <mutex>
 
@@ -724,31 +726,81 @@ namespace dspark {
 namespace {
 
 constexpr int kNoAllocMaxCandidates = 16384;                 // B * N limit
-constexpr size_t kNoAllocScratchBytes =
-    sizeof(WsHeader) + 2 * sizeof(unsigned long long) * static_cast<size_t>(kNoAllocMaxCandidates);
+static_assert(kNoAllocMaxCandidates <= kSmemMaxCandidates,
+              "allocation-free pools must stay on the shared-memory kernels (no global key buffers)");
+constexpr size_t kNoAllocScratchBytes = sizeof(WsHeader);
 
 static __device__ __align__(256) unsigned char g_schedule_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {};
+// The array's device address, looked up once per CUDA context.  A context is named by the
+// driver's context id (unique for the life of the process), so a device reset, or another
+// context made current on the same device, gets a lookup of its own rather than a stale address.
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of g_schedule_scratch on the current device, looked up once per device.
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* addr;
+};
+
+constexpr int kScratchEntries = 64;
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch_cache[kScratchEntries] = {};
+int g_scratch_used = 0, g_scratch_next = 0;
+PfnCtxGetCurrent g_ctx_get_current = nullptr;
+PfnCtxGetId g_ctx_get_id = nullptr;
+
+template <typename F>
+bool driver_fn(const char* name, F* out) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        set_error("driver entry point %s unavailable", name);
+        return false;
+    }
+    *out = reinterpret_cast<F>(fn);
+    return true;
+}
+
+// Device address of g_schedule_scratch in the current context.
 dspark_status schedule_scratch(void** out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) {
-        set_error("device index %d out of range", dev);
-        return DSPARK_ERR_UNSUPPORTED;
-    }
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_schedule_scratch);
-        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(schedule scratch)");
-        g_scratch_addr[dev] = p;
+    if (g_ctx_get_current == nullptr && !driver_fn("cuCtxGetCurrent", &g_ctx_get_current))
+        return DSPARK_ERR_UNSUPPORTED;
+    if (g_ctx_get_id == nullptr && !driver_fn("cuCtxGetId", &g_ctx_get_id)) return DSPARK_ERR_UNSUPPORTED;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) {
+        set_error("cuCtxGetCurrent failed");
+        return DSPARK_ERR_CUDA;
     }
-    *out = g_scratch_addr[dev];
+    void* p = nullptr;
+    if (ctx == nullptr) {
+        // no context yet: the runtime makes the device's primary context current on this lookup
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_schedule_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(schedule scratch)");
+        if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+            set_error("no current CUDA context");
+            return DSPARK_ERR_CUDA;
+        }
+    }
+    unsigned long long id = 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) {
+        set_error("cuCtxGetId failed");
+        return DSPARK_ERR_CUDA;
+    }
+    for (int k = 0; k < g_scratch_used; ++k)
+        if (g_scratch_cache[k].ctx_id == id) {
+            *out = g_scratch_cache[k].addr;
+            return DSPARK_OK;
+        }
+    if (p == nullptr) {
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_schedule_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(schedule scratch)");
+    }
+    const int slot = g_scratch_used < kScratchEntries ? g_scratch_used++ : (g_scratch_next++ % kScratchEntries);
+    g_scratch_cache[slot] = ScratchEntry{id, p};
+    *out = p;
     return DSPARK_OK;
 }
 

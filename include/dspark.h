@@ -126,8 +126,20 @@ DSPARK_API dspark_status dspark_draft_logits(const void* hidden, const void* lm_
  *     z[v]    = (base_logits[b, i, v] + bias[v]) / T_b          (T_b > 0)
  *     x       = argmax_v (z[v] + g[v])   ties to the lowest v
  *     draft_tokens[b, i] = x;  prev = x
- * with g the stream-0 Gumbel noise of counter (v >> 2, b, i, offset), word
- * v & 3.  T_b = 0 means greedy: x = argmax_v (base + bias), no noise.
+ * with g a standard Gumbel variate per (b, i, v) from the Philox generator
+ * (counter words (c0, c1, c2, c3) = (j, b, (stream << 16) | i, offset), key
+ * (lo32 seed, hi32 seed), uniform u = ((w >> 9) + 1/2) * 2^-23), drawn in
+ * groups of 16 entries (G = v >> 4, k = v & 15):
+ *     W     = word G & 3 of the stream-0 counter j = G >> 2 (the group word)
+ *     p     = W & 15, the position of the group's largest variate
+ *     E_min = -log(u(W)) / 16, the group's smallest exponential
+ *     E_k   = E_min                                 for k == p
+ *           = E_min - log(u(w_k))                    otherwise, w_k = word
+ *             k & 3 of the stream-3 counter j = (G << 2) | (k >> 2)
+ *     g     = -log(E_k)
+ * (the 16 E_k are independent Exp(1), so every g is a standard Gumbel, and
+ * -log(E_min) bounds the whole group).  T_b = 0 means greedy:
+ * x = argmax_v (base + bias), no noise.
  * The [B, V] row of z is never written to device memory.
  *
  *   base_logits  [B, N, V] fp32, device (row (b, i) contiguous over v)
@@ -423,12 +435,15 @@ DSPARK_API dspark_status dspark_schedule(const float* cond_accept, const double*
  * must never block (cudaMalloc/cudaFree can synchronise with work already
  * queued on the device), or a host whose device memory is wholly reserved by
  * another allocator, so that a new allocation would fail.  The scratch lives in
- * one fixed array inside the library (262,400 bytes, held on every GPU that
- * loads the library until the process exits); the call allocates nothing.
+ * one fixed array inside the library (256 bytes: the status header, since pools
+ * this size sort in shared memory; held on every GPU that loads the library
+ * until the process exits); the call allocates nothing.
  *   - B*N must be at most 16384; larger pools return DSPARK_ERR_INVALID_ARG
  *     (use dspark_schedule with a workspace).
- *   - The first call on each device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - The first call in each CUDA context looks up the array's device address
+ *     (with that context current); make that first call before any stream
+ *     capture.  A device reset or another context on the same device gets a
+ *     fresh lookup on its first call.
  *   - All calls share the array and each call clears its status header first.
  *     Calls that overlap on the GPU (different streams, or several threads)
  *     race on it and must be serialised by the caller.

@@ -50,11 +50,18 @@ def markov_bias(prev: np.ndarray, w1: np.ndarray, w2: np.ndarray) -> np.ndarray:
     return emb @ np.asarray(w2, dtype=np.float64).T                             # [b, V]
 
 
-def markov_sample_given_noise(base_logits, anchor, w1, w2, temperature, gumbel):
+def markov_sample_given_noise(base_logits, anchor, w1, w2, temperature, gumbel, forced_tokens=None):
     """The sequential loop with the Gumbel noise supplied.
 
     gumbel(i, rows) -> [len(rows), V] float64 noise of step i for the local
     request rows `rows` (only rows with T > 0 are asked for).
+
+    forced_tokens [Bs, N] (optional): teacher forcing.  Step i + 1 then embeds
+    forced_tokens[:, i] as its previous token instead of this loop's own token
+    of step i.  Each step is still the step of §2.2 (bias of the previous
+    token, add, temperature, Gumbel-max); only the history it conditions on is
+    supplied, so that another implementation's token sequence can be checked
+    position by position without one near tie changing every later step.
 
     Returns (tokens [Bs, N] int64, gap [Bs, N] float64, lse [Bs, N] float64):
       gap = (largest - second largest) of the perturbed values at each step,
@@ -82,12 +89,15 @@ def markov_sample_given_noise(base_logits, anchor, w1, w2, temperature, gumbel):
         m = z.max(axis=1)
         lse[:, i] = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
         tokens[:, i] = x
-        prev = x                                                   # feeds the next step
+        if forced_tokens is None:
+            prev = x                                               # feeds the next step
+        else:
+            prev = np.asarray(forced_tokens, dtype=np.int64)[:, i].copy()
     return tokens, gap, lse
 
 
 def markov_sample(base_logits, anchor, w1, w2, temperature, seed: int, offset: int,
-                  req_ids=None):
+                  req_ids=None, forced_tokens=None):
     """Sequential Markov-biased Gumbel-max sampling of N draft tokens per request.
 
     "DSpark implementation and evaluation" §2.2 (the sequential loop) and §3.
@@ -95,9 +105,13 @@ def markov_sample(base_logits, anchor, w1, w2, temperature, seed: int, offset: i
     base_logits [Bs, N, V]: base logits of the requests req_ids (default 0..Bs-1);
     req_ids give the request index b used in the random-number counter, so a
     subset of a large batch can be checked alone.  anchor, temperature: [Bs].
-    The Gumbel noise of step i, request b, token v is the variate of the
-    split draft word of ``philox.draft_word`` (high half from stream 0, low half
-    from stream 3, counter (v >> 3, b, i, offset)).
+    The Gumbel noise of step i, request b, token v is ``philox.draft_gumbel``:
+    entries in groups of 16 (G = v >> 4, k = v & 15); the group word is word
+    G & 3 of the stream-0 counter (G >> 2, b, i, offset) and gives the position
+    of the group's largest variate and the group's smallest exponential; every
+    other entry adds its own exponential from word k & 3 of the stream-3 counter
+    ((G << 2) | (k >> 2), b, i, offset); g = -log(E).
+    forced_tokens: teacher forcing, as in ``markov_sample_given_noise``.
     """
     L = np.asarray(base_logits)
     req = np.arange(L.shape[0]) if req_ids is None else np.asarray(req_ids)
@@ -106,4 +120,4 @@ def markov_sample(base_logits, anchor, w1, w2, temperature, seed: int, offset: i
     def gumbel(i, rows):
         return draft_gumbel(seed, offset, req[rows], i, V)
 
-    return markov_sample_given_noise(base_logits, anchor, w1, w2, temperature, gumbel)
+    return markov_sample_given_noise(base_logits, anchor, w1, w2, temperature, gumbel, forced_tokens)

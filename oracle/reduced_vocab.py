@@ -40,8 +40,10 @@ def map_to_target(draft_ids: np.ndarray, d2t: np.ndarray, mode: int, V_target: i
 
 
 def markov_sample_reduced(base_logits, anchor, w1, w2, temperature, seed: int, offset: int,
-                          d2t, mode: int, V_target: int, req_ids=None):
+                          d2t, mode: int, V_target: int, req_ids=None, forced_draft_tokens=None):
     """Returns (target tokens [Bs, N], draft tokens [Bs, N], gap, lse) -- gap and lse as in
-    ``markov_sample`` (computed on the draft vocabulary)."""
-    draft, gap, lse = markov_sample(base_logits, anchor, w1, w2, temperature, seed, offset, req_ids)
+    ``markov_sample`` (computed on the draft vocabulary).  forced_draft_tokens: teacher
+    forcing with a sequence of draft ids (``markov_sample``'s forced_tokens)."""
+    draft, gap, lse = markov_sample(base_logits, anchor, w1, w2, temperature, seed, offset, req_ids,
+                                    forced_tokens=forced_draft_tokens)
     return map_to_target(draft, d2t, mode, V_target), draft, gap, lse

@@ -26,3 +26,16 @@ def cuda_lib():
 def golden_dir():
     import pathlib
     return pathlib.Path(ROOT) / "tests" / "golden"
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Totals of the GPU parity comparisons (compared positions and near-tie divergences per kind),
+    printed at the end of the run and, when DSPARK_PARITY_RECORD names a file, written there."""
+    from tests._helpers import PARITY_RECORD, parity_summary_lines, write_parity_record
+    if not PARITY_RECORD:
+        return
+    for line in parity_summary_lines():
+        terminalreporter.write_line(line)
+    path = os.environ.get("DSPARK_PARITY_RECORD")
+    if path:
+        write_parity_record(path)

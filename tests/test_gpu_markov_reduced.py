@@ -1,6 +1,7 @@
 """GPU parity: Markov sampling on a reduced draft vocabulary, tokens returned as target ids.
 
-Compared with the oracle (same near-tie rule as the plain sampler), on the CUDA-core path
+Compared with the oracle at every position on the GPU's own prefix (teacher forcing; same
+near-tie rule and bound as the plain sampler), on the CUDA-core path
 (one request, EAGLE-3-sized 32000-entry draft vocabulary in a 151936-entry target vocabulary)
 and on the tensor-core path; both table conventions; identity tables reproduce the plain
 sampler exactly; unmappable ids come back as -1 with a flag."""
@@ -9,7 +10,7 @@ import pytest
 
 import oracle
 from oracle.reduced_vocab import MODE_INDEX, MODE_OFFSET
-from tests._helpers import compare_markov_tokens, to_dev
+from tests._helpers import check_tie_share, compare_teacher_forced, record_parity, to_dev
 from workloads import DraftConfig, markov_logits, normal_rows, to_bf16_values
 
 pytestmark = pytest.mark.gpu
@@ -35,10 +36,14 @@ def test_matches_oracle(cuda_lib, B, N, Vd, r, T, mode):
     Ts = np.full(B, T, np.float32)
     tok = cuda_lib.dspark_markov_sample_reduced(to_dev(L), to_dev(anchor), to_dev(tw1), to_dev(tw2), to_dev(Ts),
                                                 6, 2, to_dev(d2t), mode, V_TARGET).cpu().numpy()
-    ref_t, ref_d, gap, _ = oracle.markov_sample_reduced(L, anchor, w1, w2, Ts, 6, 2, d2t, mode, V_TARGET)
-    n, ties = compare_markov_tokens(tok, ref_t, gap)
-    print(f"B={B} mode={mode}: compared {n}, near-tie divergences {ties}")
     assert np.all(np.isin(tok, table))
+    draft_ids = np.searchsorted(table, tok)             # the table is strictly increasing
+    ref_t, ref_d, gap, _ = oracle.markov_sample_reduced(L, anchor, w1, w2, Ts, 6, 2, d2t, mode, V_TARGET,
+                                                        forced_draft_tokens=draft_ids)
+    n, ties = compare_teacher_forced(draft_ids, ref_d, gap)
+    check_tie_share(n, ties, f"reduced B={B} mode={mode}")
+    record_parity("markov reduced vocabulary", f"B={B} N={N} mode={mode}", n, ties)
+    np.testing.assert_array_equal(tok[draft_ids == ref_d], ref_t[draft_ids == ref_d])
 
 
 def test_identity_table_reproduces_the_plain_sampler(cuda_lib):

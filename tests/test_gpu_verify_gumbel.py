@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests._helpers import to_dev
+from tests._helpers import record_parity, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -42,6 +42,7 @@ def _check(ds, t, T, x, seed, offset, lengths=None, workspace=None):
     for b in np.nonzero(close)[0]:                       # near ties: well formed only
         n = nacc[b]
         assert 0 <= n <= g and np.all(out[b, :n] == x[b, :n]) and 0 <= out[b, n] < t.shape[2]
+    record_parity("verify with draft noise (requests)", f"B={x.shape[0]} V={t.shape[2]}", x.shape[0], int(close.sum()))
     return ref_nacc, int(close.sum())
 
 

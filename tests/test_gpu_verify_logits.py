@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests._helpers import to_dev
+from tests._helpers import record_parity, to_dev
 from workloads import VERIFY_LOGITS_CONFIGS, VerifyLogitsConfig, verify_logits_inputs
 
 pytestmark = pytest.mark.gpu
@@ -66,6 +66,7 @@ def _compare(out, nacc, x, ref, V, gap_tol, rows=None):
             continue
         assert out[b, n] == ref_out[i, n], (
             f"request {b}: gpu token {out[b, n]}, oracle {ref_out[i, n]} (gap {gap[i]:.3g})")
+    record_parity("verify from logits (requests)", f"B={len(rows)} V={V}", len(rows), near)
     return near
 
 

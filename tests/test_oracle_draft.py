@@ -162,6 +162,43 @@ def test_req_ids_select_the_counter_of_each_request():
     np.testing.assert_array_equal(part, full[sub])
 
 
+def test_teacher_forced_greedy_steps_are_argmax_on_the_forced_history():
+    """Teacher forcing at T = 0: step i is numpy's argmax of base + w2 w1[p_i] with p_0 the anchor
+    and p_i the FORCED token of step i - 1 (not the loop's own), written out directly."""
+    rng = np.random.default_rng(12)
+    B, N, V, r = 4, 5, 40, 3
+    L = rng.standard_normal((B, N, V))
+    w1, w2 = rng.standard_normal((V, r)) * 2.0, rng.standard_normal((V, r))
+    anchor = rng.integers(0, V, B)
+    forced = rng.integers(0, V, (B, N))
+    tok, gap, lse = oracle.markov_sample(L, anchor, w1, w2, np.zeros(B), 0, 0, forced_tokens=forced)
+    for b in range(B):
+        for i in range(N):
+            p = anchor[b] if i == 0 else forced[b, i - 1]
+            logits = L[b, i] + w2 @ w1[p]
+            assert tok[b, i] == int(np.argmax(logits))
+            srt = np.sort(logits)
+            np.testing.assert_allclose(gap[b, i], srt[-1] - srt[-2], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b, i], special.logsumexp(logits), rtol=1e-13)
+    # the forced history is used: forcing other tokens changes some step's result
+    free, _, _ = oracle.markov_sample(L, anchor, w1, w2, np.zeros(B), 0, 0)
+    assert np.any(free[:, 1:] != tok[:, 1:])
+
+
+def test_teacher_forced_with_zero_markov_head_ignores_the_history():
+    """w1 = 0: no step depends on the previous token, so any forced history gives the
+    free-running tokens (independent Gumbel-max per position)."""
+    rng = np.random.default_rng(13)
+    B, N, V, r = 3, 6, 100, 4
+    L = rng.standard_normal((B, N, V))
+    w1, w2 = np.zeros((V, r)), rng.standard_normal((V, r))
+    anchor = rng.integers(0, V, B)
+    T = np.array([0.7, 1.0, 1.4])
+    free, _, _ = oracle.markov_sample(L, anchor, w1, w2, T, 5, 2)
+    forced, _, _ = oracle.markov_sample(L, anchor, w1, w2, T, 5, 2, forced_tokens=rng.integers(0, V, (B, N)))
+    np.testing.assert_array_equal(forced, free)
+
+
 def test_tiny_workload_runs_and_param_count_of_markov_head():
     cfg = DRAFT_CONFIGS["tiny"]
     inp = draft_inputs(cfg)

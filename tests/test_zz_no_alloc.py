@@ -4,11 +4,12 @@ workspace one.
 dspark_schedule_noalloc serves callers that cannot hand the library device
 scratch memory -- a serving loop that must never block on a cudaMalloc, or a
 host whose device memory is wholly reserved by another allocator.  Its scratch
-is one fixed array inside the library that every call reuses, so this test
-calls it twice in a row on different pools (the second call starts from the
-first call's leftovers) and checks each result against dspark_schedule with a
-workspace of its own, bit for bit, as the other scheduling tests do.  It also
-checks that a pool beyond the array's capacity is refused before any launch.
+is one fixed array inside the library (the status header) that every call
+reuses, so this test calls it twice in a row on different pools (the second
+call finds the first call's status header and must clear it) and checks each
+result against dspark_schedule with a workspace of its own, bit for bit, as the
+other scheduling tests do.  It also checks that a pool beyond the entry point's
+limit is refused before any launch.
 """
 import ctypes
 

@@ -38,7 +38,7 @@ __all__ = [
     "DraftConfig", "VerifyConfig", "ScheduleConfig", "DRAFT_CONFIGS",
     "VERIFY_CONFIGS", "SCHEDULE_CONFIGS", "VerifyLogitsConfig", "VERIFY_LOGITS_CONFIGS",
     "verify_logits_inputs", "normal_rows", "draft_inputs",
-    "markov_logits", "verify_inputs", "schedule_inputs", "sps_table",
+    "markov_logits", "zipf_offsets", "verify_inputs", "schedule_inputs", "sps_table",
     "to_bf16_values",
 ]
 
@@ -224,23 +224,34 @@ def draft_inputs(cfg: DraftConfig, rows: slice | None = None):
 def markov_logits(cfg: DraftConfig, scale: float = 1.0) -> np.ndarray:
     """Synthetic base logits [B, N, V] float32 for the Markov sampler alone.
 
-    N(0, scale^2) per element, plus (if cfg.zipf > 0) a per-(b, i) Zipf offset
-    -zipf * ln(rank), where rank in 1..V comes from a seeded random permutation
-    of the vocabulary for that row.
+    N(0, scale^2) per element, plus (if cfg.zipf > 0) the per-(b, i) Zipf offset of
+    ``zipf_offsets``.
     """
     B, N, V = cfg.B, cfg.N, cfg.V
     L = normal_rows(B * N, V, scale, cfg.data_seed, "base").reshape(B, N, V)
     if cfg.zipf > 0:
-        off = (-cfg.zipf * np.log(np.arange(1, V + 1, dtype=np.float64))).astype(np.float32)
-
-        def work(row):
-            rng = np.random.default_rng((cfg.data_seed, _TAG["zipf_perm"], row))
-            perm = rng.permutation(V)
-            L.reshape(B * N, V)[row, perm] += off
-
-        with ThreadPoolExecutor(_threads()) as ex:
-            list(ex.map(work, range(B * N)))
+        L.reshape(B * N, V)[:] += zipf_offsets(cfg)
     return L
+
+
+def zipf_offsets(cfg: DraftConfig, rows=None) -> np.ndarray:
+    """Per-row Zipf rank offsets [len(rows), V] float32 (rows of the [B*N, V] logits, default all):
+    entry v of row m is -zipf * ln(rank_m(v)), rank_m a seeded random permutation of 1..V for
+    that row (row m's permutation depends only on (data_seed, m)), so that a few tokens of every
+    row dominate as they do in real LM logits."""
+    V = cfg.V
+    rows = np.arange(cfg.B * cfg.N) if rows is None else np.asarray(rows)
+    off = (-cfg.zipf * np.log(np.arange(1, V + 1, dtype=np.float64))).astype(np.float32)
+    out = np.empty((len(rows), V), dtype=np.float32)
+
+    def work(j):
+        rng = np.random.default_rng((cfg.data_seed, _TAG["zipf_perm"], int(rows[j])))
+        perm = rng.permutation(V)
+        out[j, perm] = off
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(work, range(len(rows))))
+    return out
 
 
 def temperatures(cfg: DraftConfig, T: float) -> np.ndarray:
