@@ -1,7 +1,8 @@
 """Benchmark of the DSpark draft/verify hot path on GB300.
 
 One step = one pass of the whole hot path over one synthetic batch:
-    dspark_draft_logits -> dspark_markov_sample -> dspark_verify -> dspark_schedule
+    dspark_draft_logits -> dspark_markov_sample_conf (the sampler with the calibrated confidence
+    head inside it) -> dspark_verify -> dspark_schedule (on the head's confidences)
 Metric: draft tokens per second (B*N drafted tokens per step), plus the roofline
 fraction of the dominant kernel and of the Markov sampler.
 
@@ -91,6 +92,16 @@ def step_configs(name: str):
                        beta_mix=((9, 1), (5, 2), (2, 3)), sps_len=d.B * d.N,
                        data_seed=d.data_seed + 5)
     return d, v, s
+
+
+def head_weights(d):
+    """Synthetic weights of the calibrated confidence head: w_h ~ N(0, 1/H), w_e ~ N(0, 1/r), beta 0.5,
+    a calibration temperature per position uniform in [0.7, 1.6]."""
+    hrng = np.random.default_rng(d.data_seed + 7)
+    w_h = (hrng.standard_normal(d.H) / np.sqrt(d.H)).astype(np.float32)
+    w_e = (hrng.standard_normal(d.r) / np.sqrt(d.r)).astype(np.float32)
+    tau = hrng.uniform(0.7, 1.6, d.N).astype(np.float32)
+    return w_h, w_e, 0.5, tau
 
 
 def host_inputs(name: str):
@@ -231,17 +242,20 @@ def measure(name, args, dev, dist, world, rank, full):
     w1 = di["w1"].to(dev)
     w2 = di["w2"].to(dev)
     h_in = {"X": di["hidden"], "anchor": torch.from_numpy(di["anchor"]), "temp": torch.from_numpy(T),
-            "p_t": torch.from_numpy(vi["p_t"]), "p_d": torch.from_numpy(vi["p_d"]),
-            "conf": torch.from_numpy(si["cond_accept"]), "sps": torch.from_numpy(si["sps"])}
+            "p_t": torch.from_numpy(vi["p_t"]), "p_d": torch.from_numpy(vi["p_d"]), "sps": torch.from_numpy(si["sps"])}
     in_specs = [(k, tuple(t.shape), t.dtype) for k, t in h_in.items()]
     out_specs = [("tok", (B, N), torch.int32), ("out", (B, N + 1), torch.int32), ("nacc", (B,), torch.int32),
                  ("K_out", (1,), torch.int32), ("lens", (B,), torch.int32), ("sel", (B * N,), torch.int32),
-                 ("surv", (B, N), torch.float32)]
+                 ("surv", (B, N), torch.float32), ("conf", (B, N), torch.float32)]
     d_in, d_out = Arena(in_specs, device=dev), Arena(out_specs, device=dev)
     for k, t in h_in.items():
         d_in.view(k).copy_(t)
-    X, anchor, temp, p_t, p_d, conf, sps = (d_in.view(k) for k in ("X", "anchor", "temp", "p_t", "p_d", "conf", "sps"))
-    tok, out, nacc, K_out, lens, sel, surv = (d_out.view(k) for k in ("tok", "out", "nacc", "K_out", "lens", "sel", "surv"))
+    X, anchor, temp, p_t, p_d, sps = (d_in.view(k) for k in ("X", "anchor", "temp", "p_t", "p_d", "sps"))
+    tok, out, nacc, K_out, lens, sel, surv, conf = (d_out.view(k) for k in ("tok", "out", "nacc", "K_out", "lens", "sel",
+                                                                            "surv", "conf"))
+    # the calibrated confidence head's weights (synthetic): w_h ~ N(0, 1/H), w_e ~ N(0, 1/r), tau per position
+    w_h, w_e, beta, tau = head_weights(d)
+    w_h, w_e, tau = (torch.from_numpy(x).to(dev) for x in (w_h, w_e, tau))
     L = torch.empty(M, V, dtype=torch.float32, device=dev)
     ws_g = ds.Workspace(ds.OP_DRAFT_LOGITS, device=dev)
     ws_m = ds.Workspace(ds.OP_MARKOV_SAMPLE, B, N, V, r, device=dev)
@@ -283,9 +297,9 @@ def measure(name, args, dev, dist, world, rank, full):
         with _nvtx("dspark_draft_logits"):
             ds.dspark_draft_logits(X, W, logits=L, workspace=ws_g)
         if e: e[1].record(stream)
-        with _nvtx("dspark_markov_sample"):
-            ds.dspark_markov_sample(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, draft_tokens=tok,
-                                    workspace=ws_m)
+        with _nvtx("dspark_markov_sample_conf"):
+            ds.dspark_markov_sample_conf(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, X, w_h, w_e, beta,
+                                         tau, draft_tokens=tok, conf=conf, workspace=ws_m)
         if e: e[2].record(stream)
         with _nvtx("dspark_verify"):
             ds.dspark_verify(p_t, p_d, tok, None, seed_verify, 0, out_tokens=out, num_accepted=nacc, workspace=ws_v)
@@ -411,7 +425,7 @@ def measure(name, args, dev, dist, world, rank, full):
                       "verify": kernel_ms[2], "schedule": kernel_ms[3]},
         "roofline": roof,
         "markov_roofline": markov_roof,
-        "gpu_launches": 4 * args.steps,           # GEMM, Markov sampler, verify, schedule
+        "gpu_launches": 4 * args.steps,           # GEMM, Markov sampler with the confidence head, verify, schedule
         "step_launch": "one CUDA graph replay per step" if graph is not None else "four eager calls per step",
         "kernel_ms_note": "per-kernel CUDA-event times from an eager pass over the same K steps",
         "clocks": clk.summary(),
@@ -423,7 +437,7 @@ def measure(name, args, dev, dist, world, rank, full):
     # the step's outputs, read once for the oracle leg and the acceptance figures
     gpu_step = {"tok": tok.cpu().numpy(), "out": out.cpu().numpy(), "nacc": nacc.cpu().numpy(),
                 "K": int(K_out.item()), "lens": lens.cpu().numpy(), "sel": sel.cpu().numpy(),
-                "surv": surv.cpu().numpy()}
+                "surv": surv.cpu().numpy(), "conf": conf.cpu().numpy()}
     tested = gpu_step["nacc"] + (gpu_step["nacc"] < N)
     res["step_verify"] = {"accepted_mean": float(gpu_step["nacc"].mean()),
                           "acceptance_rate": float(gpu_step["nacc"].sum() / max(1, tested.sum())),
@@ -466,14 +480,10 @@ def measure(name, args, dev, dist, world, rank, full):
     g_nacc = torch.empty(B, dtype=torch.int32, device=dev)
     greedy_ms = _timed_calls(lambda: ds.dspark_verify_greedy(p_t, tok, None, out_tokens=g_out, num_accepted=g_nacc,
                                                              workspace=ws_g2), flush_l2, stream)
-    # calibrated confidence head on the step's hidden rows and draft tokens (synthetic head weights)
-    hrng = np.random.default_rng(d.data_seed + 7)
-    w_h = torch.from_numpy((hrng.standard_normal(H) / np.sqrt(H)).astype(np.float32)).to(dev)
-    w_e = torch.from_numpy((hrng.standard_normal(r) / np.sqrt(r)).astype(np.float32)).to(dev)
-    tau = torch.from_numpy(hrng.uniform(0.7, 1.6, N).astype(np.float32)).to(dev)
+    # the calibrated confidence head as its own launch (the step evaluates it inside the sampler)
     ws_c = ds.Workspace(ds.OP_CONFIDENCE, B, N, V, r, device=dev)
     conf_out = torch.empty(B, N, dtype=torch.float32, device=dev)
-    conf_ms = _timed_calls(lambda: ds.dspark_confidence(X, w1, anchor, tok, w_h, w_e, 0.5, tau, conf=conf_out,
+    conf_ms = _timed_calls(lambda: ds.dspark_confidence(X, w1, anchor, tok, w_h, w_e, beta, tau, conf=conf_out,
                                                         workspace=ws_c), flush_l2, stream)
     conf_bytes = M * H * X.element_size() + M * r * w1.element_size() + (H + r + N) * 4 + M * 4
     # the sampler on an EAGLE-3-sized reduced draft vocabulary (first 32000 entries of the step's
@@ -536,8 +546,9 @@ def measure(name, args, dev, dist, world, rank, full):
 
     res["markov_sample_reduced_vocab"] = {"ms": red_ms, "draft_vocab": Vd, "target_vocab": V,
                                           "note": "median of 20 launches, L2 flushed, outside the step"}
-    res["confidence"] = hbm_entry(conf_ms, conf_bytes, "median of 20 launches, L2 flushed, outside the step "
-                                                       "(latency-bound at these sizes)")
+    res["confidence_standalone"] = hbm_entry(conf_ms, conf_bytes, "dspark_confidence as its own launch: median of 20 "
+                                             "launches, L2 flushed, outside the step (the step evaluates the head "
+                                             "inside dspark_markov_sample_conf)")
     res["verify_logits"] = hbm_entry(vlog_ms, vlog_bytes,
                                      "median of 20 calls (2 kernels), L2 flushed, outside the step; bytes = "
                                      "target rows k <= k* plus row k* again, from the measured k*",
@@ -637,8 +648,10 @@ def oracle_step(inputs, req, gpu=None, parity=None):
     tok, gap, _ = oracle.markov_sample(Lr, di["anchor"][req], di["w1_f32"], di["w2_f32"], T[req], 0, 0,
                                        req_ids=req, forced_tokens=forced)
     x = tok if gpu is None else forced
+    w_h, w_e, beta, tau = head_weights(d)
+    c = oracle.confidence(di["hidden_f32"][rows], di["w1_f32"], di["anchor"][req], x, w_h, w_e, beta, tau)
     out, nacc, _, _ = oracle.verify(vi["p_t"][req], vi["p_d"][req], x, None, 2, 0, req_ids=req)
-    oracle.schedule(si["cond_accept"][req], si["sps"][: len(req) * d.N], -1)
+    oracle.schedule(c.astype(np.float32), si["sps"][: len(req) * d.N], -1)
     if parity is not None and gpu is not None:
         diff = tok != forced
         parity["markov_compared"] += int(tok.size)
@@ -646,6 +659,8 @@ def oracle_step(inputs, req, gpu=None, parity=None):
         parity["markov_mismatch"] += int((diff & (gap >= 5e-2)).sum())
         parity["verify_compared"] += len(req)
         parity["verify_mismatch"] += int(np.sum(np.any(out != gpu["out"][req], axis=1) | (nacc != gpu["nacc"][req])))
+        parity["confidence_max_abs_diff"] = max(parity.get("confidence_max_abs_diff", 0.0),
+                                                float(np.abs(c - gpu["conf"][req]).max()))
     return len(req) * d.N
 
 
@@ -701,15 +716,16 @@ def cpu_baseline(name, budget_s, inputs):
             break
     el = time.perf_counter() - t0
     one = oracle_single_thread(name)
-    rs = oracle.schedule(si["cond_accept"], si["sps"], -1)
+    rs = oracle.schedule(gpu["conf"], si["sps"], -1)          # the head's float32 confidences, as the GPU's input
     sched_ok = (rs["K"] == gpu["K"] and np.array_equal(rs["lengths"], gpu["lens"])
                 and np.array_equal(rs["selected"], gpu["sel"]) and np.array_equal(rs["survival"], gpu["surv"]))
     parity["schedule_pool"] = int(si["cond_accept"].size)
     parity["schedule_bit_exact"] = bool(sched_ok)
     parity["note"] = ("sampled requests: the oracle's tokens teacher-forced on the GPU step's tokens (a token "
                       "may differ only at an oracle top-2 gap < 5e-2: near_tie; mismatch counts the rest), "
-                      "verification of the GPU's tokens compared bit for bit per request; the whole "
-                      "scheduling pool compared bit for bit")
+                      "the confidence head on the GPU's tokens (tolerance 2e-5), verification of the GPU's "
+                      "tokens compared bit for bit per request; the whole scheduling pool (the head's float32 "
+                      "confidences) compared bit for bit")
     return {"value": tokens / el, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{b} request(s) of {d.name} through the whole path on the CPU oracle "
                       f"(fp64 numpy): {tokens} draft tokens in {el:.1f} s",

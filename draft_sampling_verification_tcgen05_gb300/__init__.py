@@ -17,7 +17,7 @@ __all__ = [
     "OP_SCHEDULE", "OP_VERIFY_GREEDY", "OP_CONFIDENCE", "OP_VERIFY_LOGITS", "OP_VERIFY_GUMBEL",
     "dspark_workspace_size", "dspark_verify_gumbel",
     "dspark_verify_greedy", "dspark_verify_logits",
-    "dspark_confidence", "dspark_markov_sample_reduced", "D2T_INDEX", "D2T_OFFSET", "dspark_draft_logits", "dspark_markov_sample",
+    "dspark_confidence", "dspark_markov_sample_reduced", "dspark_markov_sample_conf", "D2T_INDEX", "D2T_OFFSET", "dspark_draft_logits", "dspark_markov_sample",
     "dspark_verify", "dspark_schedule", "dspark_read_status", "dspark_status_string",
     "dspark_selftest_wait_timeout", "STATUS_TIMEOUT", "STATUS_NUMERIC", "STATUS_INPUT_RANGE",
     "STATUS_INTERNAL",
@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
     L.dspark_draft_logits.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
     L.dspark_markov_sample.argtypes = [vp, vp, vp, vp, i32, vp, u64, u64, i32, i32, i32, i32,
                                        vp, vp, vp, sz, vp]
+    L.dspark_markov_sample_conf.argtypes = [vp, vp, vp, vp, i32, vp, u64, u64, i32, i32, i32, i32,
+                                            vp, i32, i32, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]
     L.dspark_markov_sample_reduced.argtypes = [vp, vp, vp, vp, i32, vp, u64, u64, i32, i32, i32, i32,
                                                vp, i32, i32, vp, vp, vp, sz, vp]
     L.dspark_verify.argtypes = [vp, vp, vp, vp, u64, u64, i32, i32, i32, vp, vp, vp, sz, vp]
@@ -191,6 +193,45 @@ def dspark_markov_sample(base_logits, anchor, w1, w2, temperature, seed: int, of
                                       _ptr(draft_tokens), _ptr(lse), ws.ptr, ws.nbytes,
                                       _stream(stream)), "dspark_markov_sample")
     return draft_tokens
+
+
+def dspark_markov_sample_conf(base_logits, anchor, w1, w2, temperature, seed: int, offset: int, hidden, w_h, w_e,
+                              beta: float, tau, draft_tokens=None, conf=None, lse=None, workspace=None, stream=None):
+    """dspark_markov_sample with the calibrated confidence head evaluated at every step; returns
+    (draft_tokens [B, N] int32, conf [B, N] fp32).  hidden [B*N, H] (bf16 or fp32), w_h [H], w_e [r],
+    tau [N] fp32; conf[b, i] is the conditional acceptance probability of draft token (b, i)."""
+    torch = _torch()
+    _need(base_logits, "base_logits", (torch.float32,), 3)
+    _need(anchor, "anchor", (torch.int32,), 1)
+    _need(w1, "w1", (torch.bfloat16, torch.float32), 2)
+    _need(w2, "w2", (w1.dtype,), 2)
+    _need(temperature, "temperature", (torch.float32,), 1)
+    _need(hidden, "hidden", (torch.bfloat16, torch.float32), 2)
+    _need(w_h, "w_h", (torch.float32,), 1)
+    _need(w_e, "w_e", (torch.float32,), 1)
+    _need(tau, "tau", (torch.float32,), 1)
+    B, N, V = base_logits.shape
+    r = w1.shape[1]
+    H = hidden.shape[1]
+    if tuple(w2.shape) != (V, r) or w1.shape[0] != V:
+        raise ValueError("w1 and w2 must both be [V, r]")
+    if hidden.shape[0] != B * N or w_h.shape[0] != H or w_e.shape[0] != r or tau.shape[0] != N:
+        raise ValueError("shapes: hidden [B*N, H], w_h [H], w_e [r], tau [N]")
+    if draft_tokens is None:
+        draft_tokens = torch.empty(B, N, dtype=torch.int32, device=base_logits.device)
+    if conf is None:
+        conf = torch.empty(B, N, dtype=torch.float32, device=base_logits.device)
+    _need(draft_tokens, "draft_tokens", (torch.int32,))
+    _need(conf, "conf", (torch.float32,))
+    if lse is not None:
+        _need(lse, "lse", (torch.float32,))
+    ws = _ws(workspace, OP_MARKOV_SAMPLE, B, N, V, r, base_logits.device)
+    _check(lib().dspark_markov_sample_conf(_ptr(base_logits), _ptr(anchor), _ptr(w1), _ptr(w2), _dt(w1),
+                                           _ptr(temperature), seed, offset, B, N, V, r, _ptr(hidden), _dt(hidden), H,
+                                           _ptr(w_h), _ptr(w_e), float(beta), _ptr(tau), _ptr(draft_tokens),
+                                           _ptr(conf), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream)),
+           "dspark_markov_sample_conf")
+    return draft_tokens, conf
 
 
 def dspark_markov_sample_reduced(base_logits, anchor, w1, w2, temperature, seed: int, offset: int, d2t,

@@ -1,6 +1,7 @@
 // C ABI of the DSpark hot path: argument validation, device facts, tensor-map
 // encoding and the status word.  Compute happens only in the kernels of the
 // other files; nothing here runs on the host in place of a kernel.
+#include "confidence_common.cuh"
 #include "device_common.cuh"
 #include "host_common.h"
 
@@ -226,7 +227,43 @@ dspark_status dspark_markov_sample(const float* base_logits, const int32_t* anch
     DeviceInfo dev;
     if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
     return launch_markov_sample(base_logits, anchor, w1, w2, wdtype, temperature, seed,
-                                static_cast<uint32_t>(offset), B, N, V, r, draft_tokens, lse, nullptr, 0, V,
+                                static_cast<uint32_t>(offset), B, N, V, r, draft_tokens, lse, nullptr, 0, V, nullptr,
+                                workspace, static_cast<cudaStream_t>(stream), dev);
+}
+
+dspark_status dspark_markov_sample_conf(const float* base_logits, const int32_t* anchor, const void* w1,
+                                        const void* w2, dspark_dtype wdtype, const float* temperature,
+                                        uint64_t seed, uint64_t offset, int B, int N, int V, int r,
+                                        const void* hidden, dspark_dtype hdtype, int H, const float* w_h,
+                                        const float* w_e, float beta, const float* tau, int32_t* draft_tokens,
+                                        float* conf, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+    g_error[0] = '\0';
+    DSPARK_REQUIRE(base_logits && anchor && w1 && w2 && temperature && draft_tokens,
+                   "markov_sample_conf: null pointer");
+    DSPARK_REQUIRE(hidden && w_h && w_e && tau && conf, "markov_sample_conf: null confidence-head pointer");
+    DSPARK_REQUIRE(wdtype == DSPARK_F32 || wdtype == DSPARK_BF16, "markov_sample_conf: unknown dtype %d", (int)wdtype);
+    DSPARK_REQUIRE(hdtype == DSPARK_F32 || hdtype == DSPARK_BF16, "markov_sample_conf: unknown hidden dtype %d",
+                   (int)hdtype);
+    DSPARK_REQUIRE(B >= 1 && N >= 1 && N <= 65535 && V >= 2 && r >= 1 && r <= 1024 && H >= 1,
+                   "markov_sample_conf: bad sizes (B=%d N=%d V=%d r=%d H=%d)", B, N, V, r, H);
+    DSPARK_REQUIRE(offset < (1ull << 32), "markov_sample_conf: offset must be below 2^32");
+    DSPARK_REQUIRE(aligned(base_logits, 4) && aligned(w1, 16) && aligned(w2, 16),
+                   "markov_sample_conf: w1/w2 must be 16-byte aligned");
+    if (bad_ws(workspace, ws_bytes, dspark_workspace_size(DSPARK_OP_MARKOV_SAMPLE, B, N, V, r)))
+        return DSPARK_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
+    ConfHead head;
+    head.hidden = hidden;
+    head.hidden_bf16 = hdtype == DSPARK_BF16 ? 1 : 0;
+    head.H = H;
+    head.w_h = w_h;
+    head.w_e = w_e;
+    head.tau = tau;
+    head.beta = beta;
+    head.conf = conf;
+    return launch_markov_sample(base_logits, anchor, w1, w2, wdtype, temperature, seed,
+                                static_cast<uint32_t>(offset), B, N, V, r, draft_tokens, lse, nullptr, 0, V, &head,
                                 workspace, static_cast<cudaStream_t>(stream), dev);
 }
 
@@ -255,7 +292,7 @@ dspark_status dspark_markov_sample_reduced(const float* base_logits, const int32
     if (!current_device(&dev)) return DSPARK_ERR_UNSUPPORTED;
     return launch_markov_sample(base_logits, anchor, w1, w2, wdtype, temperature, seed,
                                 static_cast<uint32_t>(offset), B, N, V, r, draft_tokens, lse, d2t,
-                                d2t_mode == DSPARK_D2T_OFFSET ? 1 : 0, V_target, workspace,
+                                d2t_mode == DSPARK_D2T_OFFSET ? 1 : 0, V_target, nullptr, workspace,
                                 static_cast<cudaStream_t>(stream), dev);
 }
 

@@ -10,8 +10,10 @@
 //
 // One warp per (request, position): 16-byte loads of the hidden row (the LM
 // head's input row) and of w_h, eight in flight per lane, the r Markov
-// features, a shuffle reduction, fp32 throughout.  The output feeds
-// dspark_schedule's cond_accept directly.
+// features, a shuffle reduction, fp32 throughout (csrc/confidence_common.cuh,
+// shared with the samplers that evaluate the head step by step).  The output
+// feeds dspark_schedule's cond_accept directly.
+#include "confidence_common.cuh"
 #include "device_common.cuh"
 #include "host_common.h"
 
@@ -36,38 +38,6 @@ struct ConfArgs {
     int B, N, H, V, r;
 };
 
-template <typename T> __device__ __forceinline__ float as_f(T x);
-template <> __device__ __forceinline__ float as_f<float>(float x) { return x; }
-template <> __device__ __forceinline__ float as_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-// Partial dot product of one lane over a row of n elements of type T against fp32 weights:
-// 16-byte pieces where the row allows it, then the tail element by element.
-template <typename T>
-__device__ __forceinline__ float lane_dot(const T* row, const float* w, int n, uint32_t lane) {
-    constexpr int kPer = 16 / static_cast<int>(sizeof(T));          // elements per 16-byte piece
-    float acc0 = 0.f, acc1 = 0.f;
-    int done = 0;
-    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && (reinterpret_cast<uintptr_t>(w) & 15) == 0) {
-        const int pieces = n / kPer;
-#pragma unroll 8
-        for (int p = static_cast<int>(lane); p < pieces; p += 32) {
-            const uint4 q = *reinterpret_cast<const uint4*>(row + p * kPer);
-            const T* e = reinterpret_cast<const T*>(&q);
-#pragma unroll
-            for (int k = 0; k < kPer; k += 4) {
-                const float4 wv = *reinterpret_cast<const float4*>(w + p * kPer + k);
-                acc0 = fmaf(as_f<T>(e[k + 0]), wv.x, acc0);
-                acc1 = fmaf(as_f<T>(e[k + 1]), wv.y, acc1);
-                acc0 = fmaf(as_f<T>(e[k + 2]), wv.z, acc0);
-                acc1 = fmaf(as_f<T>(e[k + 3]), wv.w, acc1);
-            }
-        }
-        done = pieces * kPer;
-    }
-    for (int k = done + static_cast<int>(lane); k < n; k += 32) acc0 = fmaf(as_f<T>(row[k]), w[k], acc0);
-    return acc0 + acc1;
-}
-
 template <typename HT, typename WT>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) confidence_kernel(ConfArgs a) {
     const int pair = static_cast<int>(blockIdx.x) * kWarpsPerBlock + static_cast<int>(warp_id());
@@ -79,22 +49,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) confidence_kernel(ConfArg
         if (lane == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
         prev = 0;
     }
-    float s = lane_dot<HT>(static_cast<const HT*>(a.hidden) + static_cast<size_t>(pair) * a.H, a.w_h, a.H, lane) +
-              lane_dot<WT>(static_cast<const WT*>(a.w1) + static_cast<size_t>(prev) * a.r, a.w_e, a.r, lane);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    if (lane == 0) {
-        const float tau = a.tau[i];
-        float c = 0.f;
-        if (tau > 0.f && tau < INFINITY) {
-            const float z = __fdiv_rn(__fadd_rn(s, a.beta), tau);
-            c = 1.f / (1.f + expf(-z));
-        } else {
-            set_status(a.ws, DSPARK_STATUS_NUMERIC);     // calibration temperatures must be positive
-        }
-        if (c != c) set_status(a.ws, DSPARK_STATUS_NUMERIC);
-        a.conf[pair] = c;
-    }
+    const float s = conf_logit_sum<HT, WT>(static_cast<const HT*>(a.hidden) + static_cast<size_t>(pair) * a.H, a.w_h,
+                                           a.H, static_cast<const WT*>(a.w1) + static_cast<size_t>(prev) * a.r, a.w_e,
+                                           a.r, lane);
+    if (lane == 0) a.conf[pair] = conf_probability(s, a.beta, a.tau[i], a.ws);
 }
 
 }  // namespace

@@ -49,7 +49,8 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
                                    const void* w2, dspark_dtype wdtype, const float* temperature,
                                    uint64_t seed, uint32_t offset, int B, int N, int V, int r,
                                    int32_t* draft_tokens, float* lse, const int32_t* d2t, int d2t_offset,
-                                   int V_target, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+                                   int V_target, const struct ConfHead* head, void* ws, cudaStream_t stream,
+                                   const DeviceInfo& dev);
 
 size_t verify_workspace_bytes(int B, int V);
 size_t verify_greedy_workspace_bytes(int B, int gamma);

@@ -3,6 +3,7 @@
 // slots and the log-sum-exp partials.
 #pragma once
 
+#include "confidence_common.cuh"
 #include "device_common.cuh"
 #include "host_common.h"
 
@@ -12,13 +13,15 @@ namespace markov {
 constexpr int kMaxGrid = 1024;                         // workspace is sized for this many blocks
 constexpr uint32_t kWaitStep = 0x200;                  // + step index (grid barrier)
 constexpr int kExchangeMaxBN = 64;                     // B * N limit of the candidate exchange
+constexpr int kPubStride = 16;                         // publication counters per step (one per request chunk)
 
 struct MarkovLayout {
     unsigned long long* slots;   // [N][B] argmax keys
     uint32_t* lb;                // [N][B] order bits of the published lower bound
-    uint32_t* pub;               // [N] blocks that have published their bounds (tensor path)
+    uint32_t* pub;               // [N][kPubStride] blocks that have published a chunk's bounds (tensor path)
     unsigned long long* cand;    // [N][grid][B] per-block candidates (exchange; B * N <= kExchangeMaxBN)
     float2* lse_part;            // [2][kMaxGrid][B] (max, sum) partials
+    float* conf_h;               // [B][N] w_h . hidden row of each pair (confidence head, CUDA-core path)
 };
 
 __host__ __device__ inline size_t markov_cand_entries(int B, int N) {
@@ -34,11 +37,13 @@ __host__ __device__ inline MarkovLayout markov_layout(void* ws, int B, int N) {
     L.lb = reinterpret_cast<uint32_t*>(p);
     p += sizeof(uint32_t) * static_cast<size_t>(N) * B;
     L.pub = reinterpret_cast<uint32_t*>(p);
-    p += sizeof(uint32_t) * static_cast<size_t>(N);
+    p += sizeof(uint32_t) * static_cast<size_t>(N) * kPubStride;
     p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~static_cast<uintptr_t>(15));
     L.cand = reinterpret_cast<unsigned long long*>(p);
     p += sizeof(unsigned long long) * markov_cand_entries(B, N);
     L.lse_part = reinterpret_cast<float2*>(p);
+    p += sizeof(float2) * 2 * static_cast<size_t>(kMaxGrid) * B;
+    L.conf_h = reinterpret_cast<float*>(p);
     return L;
 }
 
@@ -66,6 +71,7 @@ struct MarkovArgs {
     const int32_t* d2t;         // [V] draft-to-target table, or null (tokens are draft ids)
     int d2t_offset;             // 0: target = d2t[d]; 1: target = d + d2t[d]
     int V_target;               // range of the mapped ids
+    ConfHead head;              // calibrated confidence head evaluated at every step (head.hidden null: none)
     long long timeout_ns;
 };
 

@@ -369,6 +369,25 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
     }
     if (a.exchange)
         for (int b = tid; b < a.B; b += kThreads) s_win[b] = 0ull;
+    if (a.head.hidden != nullptr) {
+        // the calibrated confidence head of "Speculative decoding: from zero to DSpark" §6: the
+        // hidden-state half of its logit does not depend on any token, so each block computes it
+        // now for the (request, position) pairs it owns (pair p belongs to block p mod grid); the
+        // embedding half is added at each step from the E row the block holds then
+        const long long pairs = static_cast<long long>(a.B) * a.N;
+        const uint32_t lane = lane_id();
+        for (long long pr = blockIdx.x + static_cast<long long>(warp_id()) * gridDim.x; pr < pairs;
+             pr += static_cast<long long>(kWarps) * gridDim.x) {
+            float hs = a.head.hidden_bf16
+                           ? conf_lane_dot<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(a.head.hidden) + pr * a.head.H,
+                                                          a.head.w_h, a.head.H, lane)
+                           : conf_lane_dot<float>(static_cast<const float*>(a.head.hidden) + pr * a.head.H, a.head.w_h,
+                                                  a.head.H, lane);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) hs += __shfl_xor_sync(0xFFFFFFFFu, hs, o);
+            if (lane == 0) a.lay.conf_h[pr] = hs;
+        }
+    }
     bool alive = true;
     int tc_fail = 0;                                  // tensor path: an MMA wait timed out
     for (int i = 0; i < a.N && alive; ++i) {
@@ -417,6 +436,17 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             tc_fence_after();
             const uint32_t w = warp_id();
             const uint32_t lanes = (32u * (w & 3u)) << 16;
+            if (a.head.hidden != nullptr && w == 1) {
+                // one request: E = w1[prev] in bf16 is row 0 of the B operand (unswizzled for row 0)
+                const long long pr = static_cast<long long>(i);
+                if (pr % gridDim.x == blockIdx.x) {
+                    const uint32_t ln = lane_id();
+                    float es = conf_lane_dot<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(bop), a.head.w_e, a.r, ln);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) es += __shfl_xor_sync(0xFFFFFFFFu, es, o);
+                    if (ln == 0) a.head.conf[pr] = conf_probability(a.lay.conf_h[pr] + es, a.head.beta, a.head.tau[i], a.ws);
+                }
+            }
             tb0 = __uint_as_float(tmem_ld1(tmem + lanes + static_cast<uint32_t>(kTcN * (w >> 2))));
             tb1 = __uint_as_float(tmem_ld1(tmem + lanes + static_cast<uint32_t>(kTcN * ((w >> 2) + 4))));
             tmem_wait_ld();
@@ -428,6 +458,18 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             }
             if (i == 0 && a.w2_cached) asm volatile("cp.async.wait_all;" ::: "memory");
             __syncthreads();
+            if (a.head.hidden != nullptr) {
+                // the embedding half of each owned pair's confidence logit, from E (fp32 in shared memory)
+                const uint32_t w = warp_id(), ln = lane_id();
+                for (int b = static_cast<int>(w); b < a.B; b += kWarps) {
+                    const long long pr = static_cast<long long>(b) * a.N + i;
+                    if (pr % gridDim.x != blockIdx.x) continue;
+                    float es = conf_lane_dot<float>(E + static_cast<size_t>(b) * a.r, a.head.w_e, a.r, ln);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) es += __shfl_xor_sync(0xFFFFFFFFu, es, o);
+                    if (ln == 0) a.head.conf[pr] = conf_probability(a.lay.conf_h[pr] + es, a.head.beta, a.head.tau[i], a.ws);
+                }
+            }
         }
 
         unsigned long long* slot = a.lay.slots + static_cast<size_t>(i) * a.B;
@@ -729,10 +771,11 @@ dspark_status run_generic(MarkovArgs& a, cudaStream_t stream, const DeviceInfo& 
 size_t markov_workspace_bytes(int B, int N) {
     const size_t nb = static_cast<size_t>(B) * N;
     size_t bytes = sizeof(WsHeader) + nb * sizeof(unsigned long long) + nb * sizeof(uint32_t) +
-                   sizeof(uint32_t) * static_cast<size_t>(N);
+                   sizeof(uint32_t) * static_cast<size_t>(N) * kPubStride;
     bytes = (bytes + 15) & ~static_cast<size_t>(15);
     bytes += sizeof(unsigned long long) * markov_cand_entries(B, N);
     bytes += 2 * static_cast<size_t>(kMaxGrid) * B * sizeof(float2);
+    bytes += nb * sizeof(float);                      // confidence head: hidden-row dot per pair
     return bytes;
 }
 
@@ -740,7 +783,8 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
                                    const void* w2, dspark_dtype wdtype, const float* temperature,
                                    uint64_t seed, uint32_t offset, int B, int N, int V, int r,
                                    int32_t* draft_tokens, float* lse, const int32_t* d2t, int d2t_offset,
-                                   int V_target, void* ws, cudaStream_t stream, const DeviceInfo& dev) {
+                                   int V_target, const ConfHead* head, void* ws, cudaStream_t stream,
+                                   const DeviceInfo& dev) {
     // clear header, slots, bounds, publication counters and the candidate entries a grid of
     // at most one block per SM uses (the lse partials need no clearing)
     const MarkovLayout lay = markov_layout(ws, B, N);
@@ -768,6 +812,7 @@ dspark_status launch_markov_sample(const float* base_logits, const int32_t* anch
     a.d2t = d2t;
     a.d2t_offset = d2t_offset;
     a.V_target = V_target;
+    if (head != nullptr) a.head = *head;
     a.timeout_ns = kDefaultTimeoutNs;
     if (markov_tc_eligible(B, N, V, r, wdtype, base_logits, lse, dev.sm_count))
         return launch_markov_tc(a, stream, dev);

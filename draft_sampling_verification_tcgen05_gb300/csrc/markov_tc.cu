@@ -31,8 +31,11 @@
 //                          with an lse output, also the block's sum of
 //                          exp(z - block max z) per request, merged over the
 //                          blocks at the start of the next step
-//   then a grid barrier among warps 1..9; the producer keeps streaming.
+//   last warp     (aux) evaluates the calibrated confidence head of the (request, step) pairs
+//                 the block owns, from the previous tokens the step's bias uses
+//   then a grid barrier among the step's warps; the producers keep streaming.
 // No [B, V] row is written to device memory.
+#include "confidence_common.cuh"
 #include "device_common.cuh"
 #include "host_common.h"
 #include "markov_common.cuh"
@@ -46,9 +49,10 @@ using namespace markov;
 
 constexpr int kGroups = 4;
 constexpr int kEpiWarps = 4 * kGroups;
-constexpr int kLProdWarp = 2 + kEpiWarps;                    // last warp: base-logit producer
-constexpr int kThreadsTC = 32 * (3 + kEpiWarps);
-constexpr uint32_t kStepThreads = 32 * (1 + kEpiWarps);
+constexpr int kLProdWarp = 2 + kEpiWarps;                    // base-logit producer
+constexpr int kAuxWarp = 3 + kEpiWarps;                      // last warp: the confidence head
+constexpr int kThreadsTC = 32 * (4 + kEpiWarps);
+constexpr uint32_t kStepThreads = 32 * (2 + kEpiWarps);      // warps 1 .. 1 + kEpiWarps and the aux warp
 constexpr int kW2Stages = 6;                    // upper bound of the w2 ring (the stream from L2 is bound by bytes in flight)
 constexpr int kLStages = 3;                      // upper bound per epilogue group; the launcher picks 2 or 3
 constexpr int kTileV = 128;
@@ -135,8 +139,8 @@ __device__ __forceinline__ void transpose_half(float* zt, const uint32_t (&r)[16
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
-markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmL,
-                 MarkovArgs a, TcArgs t) {
+markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW2k,
+                 const __grid_constant__ CUtensorMap tmL, MarkovArgs a, TcArgs t) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -185,6 +189,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
         for (int i = 0; i < kMaxLocalTiles; ++i) mbar_init(&bar_tile[i], 1);
         fence_mbarrier_init();
         prefetch_tensormap(&tmW2);
+        prefetch_tensormap(&tmW2k);
         prefetch_tensormap(&tmL);
     }
     bool bad_t = false;
@@ -243,9 +248,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                                 break;
                             }
                             mbar_arrive_expect_tx(&bar_w2_full[ws], static_cast<uint32_t>(nkb) * kW2BoxBytes);
-                            for (int j = 0; j < nkb; ++j)
-                                tma_load_2d(w2s + ws * kW2StageBytes + j * kW2BoxBytes, &tmW2, (ks * kKbPerStage + j) * 64,
-                                            (tile_lo + t0 + u) * kTileV, &bar_w2_full[ws], pol_keep);
+                            if (nkb == kKbPerStage) {
+                                // one copy of the stage's k-blocks (slabs of 16 KB): a TMA-issuing thread
+                                // pays a large fixed cost per copy, so fewer, larger copies stream faster
+                                tma_load_3d(w2s + ws * kW2StageBytes, &tmW2k, 0, (tile_lo + t0 + u) * kTileV,
+                                            ks * kKbPerStage, &bar_w2_full[ws], pol_keep);
+                            } else {
+                                for (int j = 0; j < nkb; ++j)
+                                    tma_load_2d(w2s + ws * kW2StageBytes + j * kW2BoxBytes, &tmW2, (ks * kKbPerStage + j) * 64,
+                                                (tile_lo + t0 + u) * kTileV, &bar_w2_full[ws], pol_keep);
+                            }
                             if (++ws == t.w2_stages) { ws = 0; wph ^= 1u; }
                         }
                     }
@@ -301,8 +313,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
             }
         }
     } else {
-        // ---------------- MMA warp + epilogue warps: the N sequential steps ----------------
-        const int stid = static_cast<int>(threadIdx.x) - 32;
+        // ---------------- MMA warp, epilogue warps, aux warp: the N sequential steps ----------------
+        const bool is_aux = warp == static_cast<uint32_t>(kAuxWarp);
+        const int stid = is_aux ? static_cast<int>(32 * (1 + kEpiWarps) + lane) : static_cast<int>(threadIdx.x) - 32;
         const bool is_mma = warp == 1;
         const int epi = static_cast<int>(warp) - 2;
         const int grp = epi >= 0 ? epi / 4 : 0;
@@ -346,7 +359,25 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
             fence_proxy_async_smem();
             named_bar_sync(kBarStep, kStepThreads);
 
-            if (is_mma) {
+            if (is_aux) {
+                // ---- calibrated confidence head of the (request, step) pairs this block owns: the
+                //      hidden row and the embedding of the previous token this step's bias uses ----
+                if (a.head.hidden != nullptr) {
+                    for (int b0 = 0; b0 < a.B; b0 += 32) {
+                        const int bl = b0 + static_cast<int>(lane);
+                        const bool mine = bl < a.B && (static_cast<long long>(bl) * a.N + i) % gridDim.x == blockIdx.x;
+                        uint32_t m = __ballot_sync(0xFFFFFFFFu, mine);
+                        while (m != 0u) {
+                            const int b = b0 + __ffs(m) - 1;
+                            m &= m - 1u;
+                            conf_eval_warp<__nv_bfloat16>(a.head, a.ws, static_cast<size_t>(b) * a.N + i, i,
+                                                          static_cast<const __nv_bfloat16*>(a.w1) +
+                                                              static_cast<size_t>(s_prev[b]) * a.r,
+                                                          a.r, lane);
+                        }
+                    }
+                }
+            } else if (is_mma) {
                 // ---- bias for every local tile: D[tile] = w2_tile (128 x r) . E^T (r x Bp) ----
                 if (lane == 0 && !dead) {
                     tc_fence_after();
@@ -456,7 +487,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 // ---- wait (bounded) until every block has published its bounds for this step ----
                 named_bar_sync(kBarEpi, 32 * kEpiWarps);
                 if (epi == 0 && lane == 0) {
-                    uint32_t* pub = a.lay.pub + i;
+                    uint32_t* pub = a.lay.pub + static_cast<size_t>(i) * kPubStride;
                     __threadfence();
                     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(pub) : "memory");
                     const long long t0 = global_ns();
@@ -663,12 +694,22 @@ dspark_status launch_markov_tc(const MarkovArgs& a, cudaStream_t stream, const D
     while (cols < static_cast<uint32_t>(max_local * t.B_pad)) cols *= 2;
     t.tmem_cols = cols;
 
-    CUtensorMap tmW2, tmL;
+    CUtensorMap tmW2, tmW2k, tmL;
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(a.r), static_cast<uint64_t>(a.V)};
         const uint64_t strides[1] = {static_cast<uint64_t>(a.r) * 2};
         const uint32_t box[2] = {64, static_cast<uint32_t>(kTileV)};
         if (!make_tensor_map(&tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.w2, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+            return DSPARK_ERR_UNSUPPORTED;
+    }
+    {
+        // w2 seen as (64 elements of a k-block, row, k-block): a box of (64, 128, kKbPerStage) is one
+        // ring stage, landing as kKbPerStage slabs of 128 rows x 128 bytes in the swizzled layout
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(a.V), static_cast<uint64_t>(a.r / 64)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(a.r) * 2, 128};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(kTileV), static_cast<uint32_t>(std::min(kKbPerStage, a.r / 64))};
+        if (!make_tensor_map(&tmW2k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.w2, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_128B))
             return DSPARK_ERR_UNSUPPORTED;
     }
@@ -705,7 +746,7 @@ dspark_status launch_markov_tc(const MarkovArgs& a, cudaStream_t stream, const D
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, markov_tc_kernel, tmW2, tmL, a, t);
+    e = cudaLaunchKernelEx(&cfg, markov_tc_kernel, tmW2, tmW2k, tmL, a, t);
     if (e != cudaSuccess) return cuda_error(e, "launch(markov_tc)");
     return DSPARK_OK;
 }

@@ -164,6 +164,37 @@ DSPARK_API dspark_status dspark_markov_sample(const float* base_logits, const in
                                    int32_t* draft_tokens, float* lse,
                                    void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * dspark_markov_sample with the calibrated confidence head of every draft token
+ * evaluated inside the sampler, step by step.
+ *
+ * "Speculative decoding: from zero to DSpark" §6: a linear projection of the
+ * backbone's hidden state together with the Markov embedding predicts each draft
+ * position's conditional acceptance probability, calibrated per position by
+ * temperature scaling; the scheduler chains these into survival probabilities:
+ *   conf[b, i] = 1 / (1 + exp(-(w_h . hidden[b*N+i] + w_e . w1[prev] + beta) / tau[i]))
+ * with prev the token whose embedding step i's Markov bias uses (anchor[b] for
+ * i = 0, draft token i-1 after).  The sampler already holds that embedding at
+ * step i, so no second pass over the tokens and no separate launch are needed;
+ * conf is dspark_schedule's cond_accept.  The result equals dspark_confidence
+ * on the tokens this call draws.
+ *
+ *   hidden  [B*N, H] hdtype (bf16 or fp32), device: the LM head's input rows
+ *   w_h [H], w_e [r] fp32, device; beta: host value; tau [N] fp32 > 0, device
+ *   conf    [B, N] fp32 output
+ * Everything else (arguments, requirements, workspace, device-side status) as
+ * dspark_markov_sample; a temperature tau[i] that is not positive and finite
+ * gives conf 0 and sets NUMERIC.
+ */
+DSPARK_API dspark_status dspark_markov_sample_conf(const float* base_logits, const int32_t* anchor,
+                                        const void* w1, const void* w2, dspark_dtype wdtype,
+                                        const float* temperature, uint64_t seed, uint64_t offset,
+                                        int B, int N, int V, int r,
+                                        const void* hidden, dspark_dtype hdtype, int H,
+                                        const float* w_h, const float* w_e, float beta,
+                                        const float* tau, int32_t* draft_tokens, float* conf,
+                                        float* lse, void* workspace, size_t ws_bytes, void* stream);
+
 /* Draft-to-target id table conventions of dspark_markov_sample_reduced. */
 typedef enum {
     DSPARK_D2T_INDEX = 0,    /* target id = d2t[draft id] (the draft logits scattered into target positions) */

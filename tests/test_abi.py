@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
     for op in ("dspark_draft_logits", "dspark_markov_sample", "dspark_verify", "dspark_schedule",
                "dspark_verify_greedy", "dspark_confidence", "dspark_markov_sample_reduced",
-               "dspark_verify_logits", "dspark_verify_gumbel"):
+               "dspark_verify_logits", "dspark_verify_gumbel", "dspark_markov_sample_conf"):
         assert op in names
 
 
@@ -65,6 +65,15 @@ def test_host_validation_without_gpu(L):
     assert L.dspark_markov_sample(fake, fake, fake, fake, 1, fake, 0, 0, 1, 0, 100, 64,
                                   fake, null, fake, 1 << 20, null) == 1                   # N = 0
     assert L.dspark_verify(fake, fake, fake, null, 0, 0, 1, 0, 10, fake, fake, fake, 256, null) == 1
+    # the sampler with the confidence head: a missing head pointer or an unknown hidden dtype is refused
+    L.dspark_markov_sample_conf.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64,
+                                            ctypes.c_uint64] + [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float] + \
+        [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p]
+    assert L.dspark_markov_sample_conf(fake, fake, fake, fake, 1, fake, 0, 0, 1, 8, 100, 64, fake, 1, 256, fake, null,
+                                       0.5, fake, fake, fake, null, fake, 1 << 20, null) == 1
+    assert L.dspark_markov_sample_conf(fake, fake, fake, fake, 1, fake, 0, 0, 1, 8, 100, 64, fake, 7, 256, fake, fake,
+                                       0.5, fake, fake, fake, null, fake, 1 << 20, null) == 1
     assert L.dspark_markov_sample_reduced(fake, fake, fake, fake, 1, fake, 0, 0, 1, 8, 100, 64, null, 0, 500,
                                           fake, null, fake, 1 << 20, null) == 1                # no table
     assert L.dspark_markov_sample_reduced(fake, fake, fake, fake, 1, fake, 0, 0, 1, 8, 100, 64, fake, 2, 500,
