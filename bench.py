@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import (DRAFT_CONFIGS, VerifyConfig, ScheduleConfig, draft_inputs,  # noqa: E402
+from workloads import (DRAFT_CONFIGS, SCHEDULE_CONFIGS, VerifyConfig, ScheduleConfig, draft_inputs,  # noqa: E402
                        verify_inputs, schedule_inputs)
 
 METRIC = "draft tokens/sec (B·N per draft step) and % of roofline for logits+Markov sampling"
@@ -537,6 +537,29 @@ def measure(name, args, dev, dist, world, rank, full):
                                                              workspace=ws_gu), flush_l2, stream)
     gumbel_bytes = B * (N + 1) * V * 4
     del ws_l, ws_m2, t_logits
+    # confidence-scheduled admission under load: B=1024 requests x N=16 candidates, SPS over batch
+    # sizes 1..16384, K chosen (its own launches, outside the step); cold = L2 flushed before each
+    # call, warm = 20 calls back to back
+    sc = SCHEDULE_CONFIGS["schedule"]
+    sci = schedule_inputs(sc)
+    c_sc = torch.from_numpy(sci["cond_accept"]).to(dev)
+    sps_sc = torch.from_numpy(sci["sps"]).to(dev)
+    ws_sc = ds.Workspace(ds.OP_SCHEDULE, sc.B, sc.N, device=dev)
+    sc_out = (torch.empty(sc.B * sc.N, dtype=torch.float32, device=dev), torch.empty(1, dtype=torch.int32, device=dev),
+              torch.empty(sc.B, dtype=torch.int32, device=dev), torch.empty(sc.B * sc.N, dtype=torch.int32, device=dev))
+
+    def sched_call():
+        ds.dspark_schedule(c_sc, sps_sc, -1, survival=sc_out[0], K_out=sc_out[1], lengths=sc_out[2],
+                           selected=sc_out[3], workspace=ws_sc)
+
+    sched_cold_ms = _timed_calls(sched_call, flush_l2, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(20):
+        sched_call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sched_warm_ms = e0.elapsed_time(e1) / 20
 
     def hbm_entry(ms, nbytes, note, **extra):
         e = {"ms": ms, "bound": "hbm", "algorithmic_bytes": nbytes, "achieved": nbytes / (ms / 1e3) / 1e9,
@@ -560,6 +583,11 @@ def measure(name, args, dev, dist, world, rank, full):
                                      accepted_mean=float(gu_nacc.float().mean().item()))
     res["verify_greedy"] = hbm_entry(greedy_ms, B * (N + 1) * V * 4,
                                      "median of 20 launches, L2 flushed, outside the step")
+    res["schedule_b1024_n16"] = {"ms": sched_cold_ms, "warm_ms": sched_warm_ms, "candidates": sc.B * sc.N,
+                                 "K": int(sc_out[1].item()),
+                                 "note": "dspark_schedule per call (workspace clear + one kernel on a cluster of "
+                                         "16 blocks): ms = median of 20 calls with L2 flushed before each, warm_ms "
+                                         "= mean of 20 calls back to back"}
     res["_oracle_inputs"] = (d, v, s, di, vi, si, T, None if zipf_host is None else zipf_host.__getitem__,
                              gpu_step)
     return res

@@ -1,4 +1,4 @@
-// Confidence-scheduled admission of draft tokens, one block.
+// Confidence-scheduled admission of draft tokens.
 //
 // "Speculative decoding: from zero to DSpark" §6: conditional acceptance
 // probabilities are chained into survival probabilities; all candidates of all
@@ -7,24 +7,29 @@
 // curve is jagged, so every K is evaluated; K may also be fixed ahead of time
 // and only the fill done now.  No token value is read at any point.
 //
-// Pools of up to 16384 candidates (every admission pool of a serving batch) run
-// entirely in shared memory, one block of 1024 threads (256 for pools of at
-// most 256):
-//   1. coalesced load of c; survival chain per request (fp32, round to nearest,
-//      no contraction); sort key (~bits(s)) per candidate, index order
-//   2. stable LSD radix sort of candidate indices by that key: 4 passes of 8
-//      bits; each warp ranks a contiguous run of the current order with warp
-//      match, per-warp digit counters are turned into output positions by one
-//      block scan, then scattered (the index breaks survival ties for free)
+// Every kernel takes the same steps:
+//   1. survival chain per request (fp32, round to nearest, no contraction);
+//      sort key (~bits(s)) per candidate, index order
+//   2. stable sort of the candidates by that key (the index breaks survival
+//      ties): LSD radix passes of 8 bits whose per-key ranks come from warp
+//      ballots, or a bitonic network over (key << 32 | index) for small pools
 //   3. if K is to be chosen: fixed-point masses floor(s * 2^32) from the float
-//      bits, block prefix sum, f(K) = float64(B * 2^32 + prefix) * SPS[K-1]
-//      for every K with the rounding done in integer arithmetic (the FP64 pipe
-//      of this GPU is narrow), block argmax with ties to the smallest K
-//   4. fill: selected in rank order, lengths by counting admitted flags
-// Larger pools (up to 2^20) take the same steps with the keys in the
-// workspace (global memory, L2-resident) instead of shared memory.
+//      bits, prefix sums, f(K) = float64(B * 2^32 + prefix) * SPS[K-1] for
+//      every K with the rounding done in integer arithmetic (the FP64 pipe of
+//      this GPU is narrow), argmax with ties to the smallest K
+//   4. fill: selected in rank order, lengths of the admitted prefixes
+// and differ in where the keys live:
+//   <= 32 candidates        one warp, one candidate per lane
+//   <= 2048                 one block, shared memory (bitonic sort above 256)
+//   <= 16384 (2049 and up)  a cluster of 16 (or 8) blocks, distributed shared memory
+//                           (one block with shared memory where a block's share
+//                           of the requests does not fit)
+//   <= 2^20                 one block, keys in the workspace (global memory, L2)
 #include "device_common.cuh"
 #include "host_common.h"
+
+#include <cooperative_groups.h>
+#include <mutex>
 
 namespace dspark {
 namespace {
@@ -544,6 +549,447 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs
 }
 
 // ---------------------------------------------------------------------------
+// Pools of 2049 .. 16384 candidates on a cluster of C = 16 blocks (one per SM; 8 where the GPU
+// cannot place 16), everything in distributed shared memory.  Block c owns a contiguous range of requests (their survival
+// chains and keys) and, after the sort, sorted positions [c * P, (c + 1) * P), P = ceil(n / C).
+// Blocks exchange small tables by writing them into every block's shared memory, so that reads
+// stay local after each cluster barrier; only the sorted keys themselves cross the cluster.
+//   1. survival chain and the 64-bit key (order key << 32 | flat index) of each candidate
+//   2. stable LSD radix sort over the cluster: survival lies in [+0, 1], so the two top bits of
+//      its order key are always one and 4 passes of 8, 8, 8 and 6 bits cover the rest; per pass
+//      each warp ranks its 64 keys by digit (warp ballots), each block hands its per-digit totals to every block,
+//      orders its keys by digit locally, then writes runs of equal digits to consecutive
+//      positions in the shared memory of the block owning them; two cluster barriers per pass,
+//      split so that local work fills their wait
+//   3. capacity: fixed-point masses of the block's sorted positions, a block scan, the blocks'
+//      totals for the carry, f(K) for the block's K range, the best (f, smallest K) over the
+//      cluster
+//   4. fill: selected for the block's positions; the admitted set is every key up to the one at
+//      sorted position K - 1, so each block counts its own requests' admitted candidates
+//      against that one key
+// ---------------------------------------------------------------------------
+constexpr int kClusterThreads = 1024;
+constexpr int kClusterChunk = 2048;                 // keys a block holds (per-block capacity)
+constexpr int kClusterWarps = kClusterThreads / 32;
+constexpr int kCQuarters = kClusterThreads / kRadix;                 // (digit, quarter) threads
+constexpr int kCWarpsPerQuarter = kClusterWarps / kCQuarters;
+constexpr size_t kClusterKeyBytes = kClusterChunk * sizeof(unsigned long long);
+constexpr size_t kClusterCntBytes = static_cast<size_t>(kClusterWarps) * kRadix * sizeof(uint16_t);
+// keys [2][chunk] | digit-ordered staging [chunk] | per-warp counters | survival [chunk] | SPS [chunk]
+constexpr size_t kClusterSpsOffset = 3 * kClusterKeyBytes + kClusterCntBytes + kClusterChunk * sizeof(float);
+constexpr size_t kClusterSmemBytes = kClusterSpsOffset + kClusterChunk * sizeof(double);
+static_assert(kCQuarters * kRadix == kClusterThreads && kCWarpsPerQuarter * kCQuarters == kClusterWarps,
+              "digit scan layout");
+
+// Requests [lo, hi) of block c when B requests are split into kCtas contiguous ranges.
+template <int kCtas>
+__device__ __forceinline__ void cluster_requests(int B, int c, int& lo, int& hi) {
+    lo = static_cast<int>((static_cast<long long>(c) * B) / kCtas);
+    hi = static_cast<int>((static_cast<long long>(c + 1) * B) / kCtas);
+}
+
+// Lanes of the warp whose digit (nbits bits, nbits <= 8) equals this lane's, among the lanes of
+// `valid`, one ballot per bit.
+__device__ __forceinline__ uint32_t same_digit_lanes_masked(uint32_t d, int nbits, uint32_t valid) {
+    uint32_t peers = valid;
+#pragma unroll
+    for (int bit = 0; bit < 8; ++bit) {
+        if (bit < nbits) {
+            const uint32_t ones = __ballot_sync(0xFFFFFFFFu, (d >> bit) & 1u);
+            peers &= ((d >> bit) & 1u) ? ones : ~ones;
+        }
+    }
+    return peers;
+}
+
+// Split cluster barrier: arrive (release: this thread's shared-memory writes, local and remote,
+// become visible to every thread that waits), then wait (acquire) for every thread of the cluster.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+template <int kClusterCtas>
+__global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(ScheduleArgs a) {
+    static_assert(kClusterCtas <= 32 && kClusterCtas * kRadix / 8 <= kClusterThreads,
+                  "one lane per block in the exchanges, one thread per 16-byte piece of the totals");
+    namespace cg = cooperative_groups;
+    constexpr int kWarps = kClusterWarps;
+    cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(s_dyn);              // [2][kClusterChunk]
+    unsigned long long* stage = keys + 2 * kClusterChunk;                                 // [kClusterChunk]
+    uint16_t* cnt = reinterpret_cast<uint16_t*>(s_dyn + 3 * kClusterKeyBytes);            // [kWarps][kRadix]
+    float* surv = reinterpret_cast<float*>(s_dyn + 3 * kClusterKeyBytes + kClusterCntBytes);   // [swz(j)]
+    double* s_sps = reinterpret_cast<double*>(s_dyn + kClusterSpsOffset);                // this block's K range
+    __shared__ __align__(16) uint16_t s_alltot[kClusterCtas][kRadix];   // every block's per-digit totals
+    __shared__ uint32_t s_q[kCQuarters][kRadix];                // per-quarter digit counts, then offsets
+    __shared__ __align__(16) uint16_t s_tot[kRadix];            // this block's per-digit totals
+    __shared__ uint32_t s_pos[kRadix];                          // start of (digit, this block) in the output
+    __shared__ uint32_t s_lstart[kRadix];                       // start of the digit in this block's keys
+    __shared__ uint32_t s_gsum[kRadix / 32], s_lsum[kRadix / 32];
+    __shared__ unsigned long long s_allpart[kClusterCtas];      // mass of every block's sorted positions
+    __shared__ unsigned long long s_allbest[kClusterCtas];      // every block's best objective key
+    __shared__ int s_allK[kClusterCtas];
+    __shared__ unsigned long long s_allT[kClusterCtas];         // every block's key at its best K - 1
+    __shared__ unsigned long long s_wsum[kWarps];
+    __shared__ unsigned long long s_best[kWarps];
+    __shared__ int s_bestK[kWarps];
+    __shared__ unsigned long long s_T;                          // key at sorted position K - 1
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x;
+    const uint32_t lane = lane_id(), warp = warp_id();
+    const int c = static_cast<int>(cluster.block_rank());
+    const int B = a.B, N = a.N;
+    const int n = B * N;
+    const int P = (n + kClusterCtas - 1) / kClusterCtas;        // sorted positions per block
+    // pos / P as a multiply-high: exact for pos < 2^16 and P <= 2^11 (the error term stays below 1 / P)
+    const uint32_t magicP = static_cast<uint32_t>((0x100000000ull + P - 1) / static_cast<unsigned long long>(P));
+    int r_lo, r_hi;
+    cluster_requests<kClusterCtas>(B, c, r_lo, r_hi);
+    const int Kmax = a.K_in >= 0 ? 0 : (a.S < n ? a.S : n);
+
+    // the SPS entries of this block's K range are read in step 3: copied into shared memory now,
+    // asynchronously (8-byte pieces: the range may start at an odd entry)
+    for (int j = c * P + tid; j < min(Kmax, (c + 1) * P); j += kClusterThreads)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;"
+                     :: "r"(smem_u32(s_sps + (j - c * P))), "l"(a.sps + j) : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
+    // ---- 1. survival chain (one thread per request, in row-permuted slots), keys in flat order ----
+    int m = (r_hi - r_lo) * N;                                   // keys this block holds now
+    const int base = r_lo * N;
+    float cin[kClusterChunk / kClusterThreads];                  // loads in flight while counters clear
+#pragma unroll
+    for (int r = 0; r < kClusterChunk / kClusterThreads; ++r) {
+        const int j = tid + r * kClusterThreads;
+        cin[r] = j < m ? __ldg(a.c + base + j) : 0.f;
+    }
+    if (tid == 0) s_bad = 0;
+    for (int i = tid; i < static_cast<int>(kClusterCntBytes / 16); i += kClusterThreads)
+        reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int r = 0; r < kClusterChunk / kClusterThreads; ++r) {
+        const int j = tid + r * kClusterThreads;
+        if (j < m) surv[swz(j)] = cin[r];
+    }
+    __syncthreads();
+    bool bad = false;
+    for (int b = tid; b < r_hi - r_lo; b += kClusterThreads) {
+        float sv = 1.f;
+        for (int k = 0; k < N; ++k) {
+            const int j = b * N + k;
+            const float cp = clamp_prob(surv[swz(j)], bad);
+            sv = (k == 0) ? cp : __fmul_rn(sv, cp);
+            surv[swz(j)] = sv;
+        }
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (tid == 0 && s_bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+    for (int j = tid; j < m; j += kClusterThreads)
+        keys[j] = (static_cast<unsigned long long>(order_key(surv[swz(j)])) << 32) | static_cast<unsigned long long>(base + j);
+    __syncthreads();
+
+    // ---- 2. stable LSD radix sort over the cluster ----
+    int cur = 0;
+    // the warp's keys: a contiguous run of one or two rounds of 32, so that every warp ranks keys
+    const int rounds = m > 32 * kWarps || (n + kClusterCtas - 1) / kClusterCtas > 32 * kWarps ? 2 : 1;
+    const int w0 = static_cast<int>(warp) * 32 * rounds;
+    uint16_t* mycnt = cnt + warp * kRadix;
+    const int sd = tid & (kRadix - 1), sq = tid / kRadix;        // (digit, quarter) of this thread
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 32 + 8 * pass;
+        const int nbits = pass == 3 ? 6 : 8;                     // key bits 62 and 63 never vary
+        const uint32_t dmask = (1u << nbits) - 1u;
+        uint32_t slot[2];
+        unsigned long long kv[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int j = w0 + r * 32 + static_cast<int>(lane);
+            kv[r] = r < rounds && j < m ? keys[cur * kClusterChunk + j] : 0ull;
+            slot[r] = static_cast<uint32_t>(kv[r] >> shift) & dmask;
+        }
+        // (a) per-warp digit counts; each key keeps (digit << 16 | offset within the warp's digit)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int live = r < rounds ? min(32, max(0, m - (w0 + r * 32))) : 0;   // lanes with a key
+            if (live > 0) {
+                const uint32_t vmask = live == 32 ? 0xFFFFFFFFu : ((1u << live) - 1u);
+                const bool valid = lane < static_cast<uint32_t>(live);
+                const uint32_t d = slot[r];
+                const uint32_t peers = same_digit_lanes_masked(d, nbits, vmask);
+                const uint32_t below = peers & ((1u << lane) - 1u);
+                const uint32_t before = valid ? mycnt[d] : 0u;
+                __syncwarp();
+                if (valid && below == 0u) mycnt[d] = static_cast<uint16_t>(before + __popc(peers));
+                __syncwarp();
+                slot[r] = (d << 16) | (before + __popc(below));
+            }
+        }
+        __syncthreads();
+        // (b) block totals per digit, from four quarters of the warps; handed to every block
+        {
+            uint32_t sum = 0;
+#pragma unroll
+            for (int i = 0; i < kCWarpsPerQuarter; ++i) sum += cnt[(sq * kCWarpsPerQuarter + i) * kRadix + sd];
+            s_q[sq][sd] = sum;
+        }
+        __syncthreads();
+        if (tid < kRadix) {
+            uint32_t tot = 0;
+#pragma unroll
+            for (int q = 0; q < kCQuarters; ++q) {                   // quarters: exclusive prefix in place
+                const uint32_t v = s_q[q][tid];
+                s_q[q][tid] = tot;
+                tot += v;
+            }
+            s_tot[tid] = static_cast<uint16_t>(tot);
+            // 16-byte pieces of 8 totals gathered by shuffles: lane l holds piece l & 3 of its warp's
+            // 32 digits and sends it to the blocks l >> 2, (l >> 2) + 8, ...
+            const uint32_t pair = tot | (__shfl_down_sync(0xFFFFFFFFu, tot, 1) << 16);
+            const int src = static_cast<int>(lane & 3u) * 8;
+            uint4 piece;
+            piece.x = __shfl_sync(0xFFFFFFFFu, pair, src + 0);
+            piece.y = __shfl_sync(0xFFFFFFFFu, pair, src + 2);
+            piece.z = __shfl_sync(0xFFFFFFFFu, pair, src + 4);
+            piece.w = __shfl_sync(0xFFFFFFFFu, pair, src + 6);
+#pragma unroll
+            for (int cc = static_cast<int>(lane >> 2); cc < kClusterCtas; cc += 8)
+                reinterpret_cast<uint4*>(cluster.map_shared_rank(&s_alltot[c][0], cc))[warp * 4 + (lane & 3u)] = piece;
+        }
+        cluster_arrive();
+        __syncthreads();
+        {                                                            // counters: exclusive prefix over warps
+            uint32_t run = s_q[sq][sd];
+#pragma unroll
+            for (int i = 0; i < kCWarpsPerQuarter; ++i) {
+                uint16_t* cp = cnt + (sq * kCWarpsPerQuarter + i) * kRadix + sd;
+                const uint32_t v = *cp;
+                *cp = static_cast<uint16_t>(run);
+                run += v;
+            }
+        }
+        cluster_wait();
+        // (c) per digit: start in the output (smaller digits anywhere, then this digit in the
+        //     blocks before this one) and start in this block's digit order
+        uint32_t all_d = 0, tot_d = 0, incl_g = 0, incl_l = 0;
+        if (tid < kRadix) {
+            uint32_t mine_before = 0;
+#pragma unroll
+            for (int cc = 0; cc < kClusterCtas; ++cc) {
+                const uint32_t v = s_alltot[cc][tid];
+                all_d += v;
+                if (cc < c) mine_before += v;
+            }
+            tot_d = s_tot[tid];
+            incl_g = all_d;
+            incl_l = tot_d;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t yg = __shfl_up_sync(0xFFFFFFFFu, incl_g, o);
+                const uint32_t yl = __shfl_up_sync(0xFFFFFFFFu, incl_l, o);
+                if (lane >= static_cast<uint32_t>(o)) {
+                    incl_g += yg;
+                    incl_l += yl;
+                }
+            }
+            if (lane == 31) {
+                s_gsum[warp] = incl_g;
+                s_lsum[warp] = incl_l;
+            }
+            incl_g += mine_before;
+        }
+        __syncthreads();
+        if (tid < kRadix) {
+            uint32_t g = 0, l = 0;
+            for (int w = 0; w < static_cast<int>(warp); ++w) {
+                g += s_gsum[w];
+                l += s_lsum[w];
+            }
+            s_pos[tid] = g + incl_g - all_d;
+            s_lstart[tid] = l + incl_l - tot_d;
+        }
+        __syncthreads();
+        // (d) this block's keys in digit order (stable), then each run of a digit written to
+        //     consecutive output positions in the block owning them
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int j = w0 + r * 32 + static_cast<int>(lane);
+            if (r < rounds && j < m) {
+                const uint32_t d = slot[r] >> 16;
+                stage[s_lstart[d] + mycnt[d] + (slot[r] & 0xFFFFu)] = kv[r];
+            }
+        }
+        __syncthreads();
+        // Two keys of one digit run that land on an even slot and the next one go as one 16-byte
+        // store (remote stores cost per request, not per byte); the second key's thread skips.
+        unsigned long long* nxt = keys + (cur ^ 1) * kClusterChunk;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int t = tid + r * kClusterThreads;
+            if (t < m) {
+                const unsigned long long key = stage[t];
+                const uint32_t d = static_cast<uint32_t>(key >> shift) & dmask;
+                const uint32_t pos = s_pos[d] + static_cast<uint32_t>(t) - s_lstart[d];
+                const uint32_t owner = __umulhi(pos, magicP);
+                const uint32_t slot_o = pos - owner * static_cast<uint32_t>(P);
+                unsigned long long* dst = cluster.map_shared_rank(nxt, static_cast<int>(owner)) + slot_o;
+                if ((slot_o & 1u) == 0u) {
+                    const bool pair = t + 1 < m && slot_o + 1 < static_cast<uint32_t>(P) &&
+                                      (static_cast<uint32_t>(stage[t + 1] >> shift) & dmask) == d;
+                    if (pair) *reinterpret_cast<ulonglong2*>(dst) = make_ulonglong2(key, stage[t + 1]);
+                    else *dst = key;
+                } else {
+                    const bool second = t > 0 && (static_cast<uint32_t>(stage[t - 1] >> shift) & dmask) == d;
+                    if (!second) *dst = key;
+                }
+            }
+        }
+        cluster_arrive();
+        if (pass < 3)                                            // counters were last read before staging
+            for (int i = tid; i < static_cast<int>(kClusterCntBytes / 16); i += kClusterThreads)
+                reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        cluster_wait();                                          // every key landed
+        cur ^= 1;
+        m = max(0, min(P, n - c * P));
+    }
+    // this block now holds sorted positions [c * P, c * P + m)
+    const unsigned long long* sorted = keys + cur * kClusterChunk;
+
+    // ---- 3. capacity K ----
+    int K;
+    bool have_T = false;
+    if (a.K_in >= 0) {
+        K = a.K_in < n ? a.K_in : n;
+    } else {
+        // kPer consecutive positions per thread (one for 16 blocks, whose share is at most 1024)
+        constexpr int kPer = (kSmemMaxCandidates / kClusterCtas + kClusterThreads - 1) / kClusterThreads;
+        const int j_lo = c * P, j_hi = min(Kmax, c * P + m);        // this block's K - 1 range
+        const int jl0 = kPer * tid;
+        asm volatile("cp.async.wait_all;" ::: "memory");            // this thread's SPS pieces landed
+        unsigned long long q[kPer];
+        unsigned long long sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            q[i] = j_lo + jl0 + i < j_hi ? mass32(key_survival(static_cast<uint32_t>(sorted[jl0 + i] >> 32))) : 0ull;
+            sum += q[i];
+        }
+        unsigned long long incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= static_cast<uint32_t>(o)) incl += y;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();                                              // also: every thread's SPS pieces landed
+        if (warp == 0) {
+            const unsigned long long v = s_wsum[lane];
+            unsigned long long x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= static_cast<uint32_t>(o)) x += y;
+            }
+            s_wsum[lane] = x - v;                                     // exclusive prefix of the warps
+            const unsigned long long total = __shfl_sync(0xFFFFFFFFu, x, 31);
+            if (lane < static_cast<uint32_t>(kClusterCtas))          // the block's total mass, to every block
+                cluster.map_shared_rank(&s_allpart[c], static_cast<int>(lane))[0] = total;
+        }
+        cluster.sync();
+        unsigned long long carry = static_cast<unsigned long long>(a.B) << 32;
+        for (int cc = 0; cc < c; ++cc) carry += s_allpart[cc];
+        carry += s_wsum[warp] + incl - sum;                           // masses before this thread's positions
+        unsigned long long best = 0ull;
+        int bestK = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            carry += q[i];
+            if (j_lo + jl0 + i < j_hi) {
+                const unsigned long long k = objective_key(carry, s_sps[jl0 + i]);
+                if (k > best) { best = k; bestK = j_lo + jl0 + i + 1; }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            const int oK = __shfl_xor_sync(0xFFFFFFFFu, bestK, o);
+            if (ok > best || (ok == best && oK < bestK)) { best = ok; bestK = oK; }
+        }
+        if (lane == 0) { s_best[warp] = best; s_bestK[warp] = bestK; }
+        __syncthreads();
+        if (warp == 0) {
+            best = s_best[lane];
+            bestK = s_bestK[lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                const int oK = __shfl_xor_sync(0xFFFFFFFFu, bestK, o);
+                if (ok > best || (ok == best && oK < bestK)) { best = ok; bestK = oK; }
+            }
+            // the block's best with the key at its position K - 1 (local), to every block
+            const unsigned long long T = bestK != 0x7FFFFFFF ? sorted[bestK - 1 - j_lo] : 0ull;
+            if (lane < static_cast<uint32_t>(kClusterCtas)) {
+                cluster.map_shared_rank(&s_allbest[c], static_cast<int>(lane))[0] = best;
+                cluster.map_shared_rank(&s_allK[c], static_cast<int>(lane))[0] = bestK;
+                cluster.map_shared_rank(&s_allT[c], static_cast<int>(lane))[0] = T;
+            }
+        }
+        cluster.sync();
+        unsigned long long bk = 0ull;
+        int bK = 0x7FFFFFFF, bc = 0;
+#pragma unroll
+        for (int cc = 0; cc < kClusterCtas; ++cc) {
+            const unsigned long long ok = s_allbest[cc];
+            const int oK = s_allK[cc];
+            if (ok > bk || (ok == bk && oK < bK)) { bk = ok; bK = oK; bc = cc; }
+        }
+        if (bK == 0x7FFFFFFF) {                                       // every f was NaN or -inf: K = 1, flagged
+            if (c == 0 && tid == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+            bK = 1;
+        } else if (tid == 0) {
+            s_T = s_allT[bc];
+            have_T = true;
+        }
+        K = bK;
+    }
+
+    // ---- 4. fill ----
+    if (tid == 0 && K > 0 && !have_T) {                              // K fixed, or the flagged K = 1
+        const uint32_t last = static_cast<uint32_t>(K - 1);
+        const uint32_t owner = __umulhi(last, magicP);
+        s_T = cluster.map_shared_rank(keys + cur * kClusterChunk, static_cast<int>(owner))[last - owner * P];
+    }
+    __syncthreads();
+    cluster_arrive();                                                 // no remote access after this point
+    // global stores only from here on: the release fences of the cluster barriers above never wait
+    // for them
+    for (int jl = tid; jl < m; jl += kClusterThreads) {
+        const int j = c * P + jl;
+        a.selected[j] = j < K ? static_cast<int>(sorted[jl] & 0xFFFFFFFFull) : -1;
+    }
+    // Candidate k of a request is admitted iff its key is at most T.  Survival never grows along a
+    // request (each factor is at most one) and equal survivals order by index, so the admitted
+    // candidates of a request are a prefix: the thread of its last admitted candidate (or of its
+    // first candidate, when none is) writes the length.
+    const unsigned long long T = s_T;
+    for (int jj = tid; jj < (r_hi - r_lo) * N; jj += kClusterThreads) {
+        const float sv = surv[swz(jj)];
+        a.survival[base + jj] = sv;
+        const int b = jj / N, k = jj - b * N;
+        const bool adm = K > 0 && ((static_cast<unsigned long long>(order_key(sv)) << 32) |
+                                   static_cast<unsigned long long>(base + jj)) <= T;
+        const bool adm_next = k + 1 < N && K > 0 &&
+                              ((static_cast<unsigned long long>(order_key(surv[swz(jj + 1)])) << 32) |
+                               static_cast<unsigned long long>(base + jj + 1)) <= T;
+        if (adm && !adm_next) a.lengths[r_lo + b] = k + 1;
+        if (k == 0 && !adm) a.lengths[r_lo + b] = 0;
+    }
+    if (c == 0 && tid == 0) a.K_out[0] = K;
+    cluster_wait();                                                   // no block leaves while another reads it
+}
+
+// ---------------------------------------------------------------------------
 // Pools above kSmemMaxCandidates: 64-bit keys (order key << 32 | index) in the workspace.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024, 1) schedule_global_kernel(ScheduleArgs a) {
@@ -660,6 +1106,61 @@ __global__ void __launch_bounds__(1024, 1) schedule_global_kernel(ScheduleArgs a
 
 }  // namespace
 
+template <int kCtas>
+cudaLaunchConfig_t cluster_config(cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCtas, 1, 1);
+    cfg.blockDim = dim3(kClusterThreads, 1, 1);
+    cfg.dynamicSmemBytes = kClusterSmemBytes;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int kCtas>
+cudaError_t prepare_cluster_kernel() {
+    cudaError_t e = cudaFuncSetAttribute(schedule_cluster_kernel<kCtas>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kClusterSmemBytes));
+    if (e == cudaSuccess && kCtas > 8)
+        e = cudaFuncSetAttribute(schedule_cluster_kernel<kCtas>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+template <int kCtas>
+cudaError_t launch_cluster(const ScheduleArgs& a, cudaStream_t stream) {
+    const cudaError_t e = prepare_cluster_kernel<kCtas>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = cluster_config<kCtas>(stream, attr);
+    return cudaLaunchKernelEx(&cfg, schedule_cluster_kernel<kCtas>, a);
+}
+
+// Whether the device can place a cluster of 16 of these blocks (16 SMs of one GPU processing
+// cluster, each with the block's shared memory), asked once per device.
+bool cluster16_fits(int device) {
+    static std::mutex mu;
+    static int known[64] = {};                                    // 0 unknown, 1 fits, 2 does not
+    if (device < 0 || device >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (known[device] == 0) {
+        int clusters = 0;
+        cudaError_t e = prepare_cluster_kernel<16>();
+        if (e == cudaSuccess) {
+            cudaLaunchAttribute attr[1];
+            const cudaLaunchConfig_t cfg = cluster_config<16>(nullptr, attr);
+            e = cudaOccupancyMaxActiveClusters(&clusters, schedule_cluster_kernel<16>, &cfg);
+        }
+        if (e != cudaSuccess) (void)cudaGetLastError();           // not sticky: fall back to 8
+        known[device] = (e == cudaSuccess && clusters >= 1) ? 1 : 2;
+    }
+    return known[device] == 1;
+}
+
 size_t schedule_workspace_bytes(int B, int N) {
     return sizeof(WsHeader) + 2 * sizeof(unsigned long long) * static_cast<size_t>(B) * N;
 }
@@ -690,6 +1191,12 @@ dspark_status launch_schedule(const float* cond_accept, const double* sps, int S
         schedule_warp_kernel<<<1, 32, 0, stream>>>(a);
     } else if (n <= 256) {                    // one block: 256 threads are plenty for small pools
         schedule_smem_kernel<256><<<1, 256, smem_schedule_bytes(static_cast<int>(n), 8), stream>>>(a);
+    } else if (n > kBitonicMax && n <= kSmemMaxCandidates &&
+               ((B + 7) / 8) * static_cast<long long>(N) <= kClusterChunk) {
+        // every block's requests and every block's share of the sorted order fit its key buffers
+        const bool wide = ((B + 15) / 16) * static_cast<long long>(N) <= kClusterChunk && cluster16_fits(dev.device);
+        const cudaError_t e = wide ? launch_cluster<16>(a, stream) : launch_cluster<8>(a, stream);
+        if (e != cudaSuccess) return cuda_error(e, "launch(schedule cluster)");
     } else if (n <= kSmemMaxCandidates) {
         const size_t smem = smem_schedule_bytes(static_cast<int>(n), 32);
         const cudaError_t e = cudaFuncSetAttribute(schedule_smem_kernel<1024>,
@@ -720,7 +1227,6 @@ dspark_status launch_schedule(const float* cond_accept, const double* sps, int S
 // memory, so the only global scratch they use is the workspace header (status
 // word and wait bookkeeping); the array is exactly that header.
 // ---------------------------------------------------------------------------
-#include <mutex>
 
 namespace dspark {
 namespace {

@@ -123,3 +123,42 @@ def test_pools_of_at_most_32_candidates(cuda_lib, B, N, K_in):
         sps[rng.random(sps.size) < 0.2] = np.nan
         sps[rng.random(sps.size) < 0.1] = 0.0
     _check(cuda_lib, c, sps, K_in)
+
+
+@pytest.mark.parametrize("B,N,case", [(1024, 16, "ties"), (1023, 16, "fixed"), (3, 700, "short_S"), (130, 16, "nan_sps"),
+                                      (2049, 1, "clamp"), (300, 10, "fixed0"), (8, 2048, "ties"), (1000, 13, "short_S"),
+                                      (517, 31, "negzero")])
+def test_pools_sorted_across_a_cluster(cuda_lib, B, N, case):
+    """Pools of 2049 .. 16384 candidates whose requests split into eight blocks of at most 2048
+    keys are sorted across a thread-block cluster: ragged and empty blocks (B not a multiple of
+    eight, B < 8), heavy survival ties across block boundaries, K fixed (0, inside, past the
+    pool), S ending inside a block, special SPS entries, clamped and negative-zero inputs."""
+    rng = np.random.default_rng(B * 31 + N)
+    c = rng.beta(4, 1.5, size=(B, N)).astype(np.float32)
+    n = B * N
+    sps, K_in = sps_table(n), -1
+    if case == "ties":
+        c[rng.random((B, N)) < 0.4] = 1.0
+        c[rng.random((B, N)) < 0.1] = 0.0
+    elif case == "fixed":
+        for K_in in (0, 1, n // 3, n, n + 5):
+            _check(cuda_lib, c, None, K_in)
+        return
+    elif case == "fixed0":
+        sps, K_in = None, 0
+    elif case == "short_S":
+        sps = sps_table(n // 2 + 7)
+    elif case == "nan_sps":
+        sps[rng.random(n) < 0.3] = np.nan
+        sps[rng.random(n) < 0.1] = -np.inf
+    elif case == "clamp":
+        c[rng.random((B, N)) < 0.01] = 1.5
+        c[rng.random((B, N)) < 0.01] = np.nan
+    elif case == "negzero":
+        c[rng.random((B, N)) < 0.2] = -0.0
+        c[rng.random((B, N)) < 0.2] = 0.0
+    ref, st, bits = _check(cuda_lib, c, sps, K_in)
+    if case == "clamp":
+        assert bits & cuda_lib.STATUS_INPUT_RANGE
+    else:
+        assert st == 0
