@@ -20,10 +20,12 @@ __all__ = [
     "dspark_confidence", "dspark_markov_sample_reduced", "dspark_markov_sample_conf", "D2T_INDEX", "D2T_OFFSET", "dspark_draft_logits", "dspark_markov_sample",
     "dspark_verify", "dspark_schedule", "dspark_read_status", "dspark_status_string",
     "dspark_selftest_wait_timeout", "STATUS_TIMEOUT", "STATUS_NUMERIC", "STATUS_INPUT_RANGE",
-    "STATUS_INTERNAL",
+    "STATUS_INTERNAL", "STATUS_INDEX",
 ]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdspark.so")
+# The library this binding loads: the in-tree build, or the file DSPARK_LIBRARY names (another
+# build of the same sources, e.g. one compiled with -DDSPARK_CHECKED).
+LIB_PATH = os.environ.get("DSPARK_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdspark.so")
 
 OP_DRAFT_LOGITS, OP_MARKOV_SAMPLE, OP_VERIFY, OP_SCHEDULE, OP_VERIFY_GREEDY, OP_CONFIDENCE = 0, 1, 2, 3, 4, 5
 OP_VERIFY_LOGITS = 6
@@ -31,7 +33,7 @@ OP_VERIFY_GUMBEL = 7
 F32, BF16 = 0, 1
 D2T_INDEX, D2T_OFFSET = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NUMERIC, ERR_INPUT_RANGE = range(7)
-STATUS_TIMEOUT, STATUS_NUMERIC, STATUS_INPUT_RANGE, STATUS_INTERNAL = 0x1, 0x2, 0x4, 0x8
+STATUS_TIMEOUT, STATUS_NUMERIC, STATUS_INPUT_RANGE, STATUS_INTERNAL, STATUS_INDEX = 0x1, 0x2, 0x4, 0x8, 0x10
 
 _lib = None
 

@@ -427,7 +427,7 @@ dspark_status dspark_read_status(const void* workspace, uint32_t* bits, void* st
     if (w & DSPARK_STATUS_TIMEOUT) return DSPARK_ERR_TIMEOUT;
     if (w & DSPARK_STATUS_NUMERIC) return DSPARK_ERR_NUMERIC;
     if (w & DSPARK_STATUS_INPUT_RANGE) return DSPARK_ERR_INPUT_RANGE;
-    if (w & DSPARK_STATUS_INTERNAL) return DSPARK_ERR_CUDA;
+    if (w & (DSPARK_STATUS_INTERNAL | DSPARK_STATUS_INDEX)) return DSPARK_ERR_CUDA;   // the library's own state
     return DSPARK_OK;
 }
 

@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) confidence_kernel(ConfArg
     const int b = pair / a.N, i = pair % a.N;
     int prev = i == 0 ? a.anchor[b] : a.tokens[static_cast<size_t>(b) * a.N + i - 1];
     if (prev < 0 || prev >= a.V) {                       // read as token 0, flagged
-        if (lane == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+        if (lane == 0) flag_input_index(a.ws);
         prev = 0;
     }
     const float s = conf_logit_sum<HT, WT>(static_cast<const HT*>(a.hidden) + static_cast<size_t>(pair) * a.H, a.w_h,

@@ -36,6 +36,28 @@ __device__ __forceinline__ void set_status(WsHeader* ws, uint32_t bits) {
     atomicOr(&ws->status, bits);
 }
 
+// Index checks at gather sites.  An index taken from the caller (an anchor, a draft token, a
+// length, a table entry) is always checked: out of range it sets INPUT_RANGE (and INDEX in a
+// checked build) and the kernel substitutes a safe value.  An index the library computed itself
+// (a token read back from a step slot, a sorted candidate, a request from a work list) is checked
+// only in a library built with -DDSPARK_CHECKED: out of range it sets INDEX and the access is
+// skipped.  Neither kind ever traps.
+#ifdef DSPARK_CHECKED
+constexpr bool kCheckedBuild = true;
+#else
+constexpr bool kCheckedBuild = false;
+#endif
+
+__device__ __forceinline__ void flag_input_index(WsHeader* ws) {
+    set_status(ws, DSPARK_STATUS_INPUT_RANGE | (kCheckedBuild ? DSPARK_STATUS_INDEX : 0u));
+}
+
+__device__ __forceinline__ bool own_index_ok(long long i, long long n, WsHeader* ws) {
+    if (!kCheckedBuild || (i >= 0 && i < n)) return true;
+    set_status(ws, DSPARK_STATUS_INDEX);
+    return false;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -82,7 +82,7 @@ __device__ __forceinline__ int32_t output_token(const MarkovArgs& a, int d) {
     if (a.d2t == nullptr) return d;
     const long long t = a.d2t_offset ? static_cast<long long>(d) + a.d2t[d] : static_cast<long long>(a.d2t[d]);
     if (t < 0 || t >= a.V_target) {
-        set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+        flag_input_index(a.ws);
         return -1;
     }
     return static_cast<int32_t>(t);
@@ -106,7 +106,8 @@ __device__ __forceinline__ int slot_token(const MarkovArgs& a, int i, int b) {
         set_status(a.ws, DSPARK_STATUS_NUMERIC);
         return 0;
     }
-    return static_cast<int>(key_index(k));
+    const int x = static_cast<int>(key_index(k));
+    return own_index_ok(x, a.V, a.ws) ? x : 0;
 }
 
 // Combine the lse partials of step i: one warp per request, the lanes over the blocks' partials,

@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
             if (i == 0) {
                 p = b == tid ? anchor_first : a.anchor[b];
                 if (p < 0 || p >= a.V) {
-                    set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+                    flag_input_index(a.ws);
                     p = 0;
                 }
             } else {
@@ -647,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 if (k > 1ull) {
                     const unsigned long long old = atomicMax(&s_win[e % a.B], k);
                     if constexpr (kTC) {
-                        if (k > old) {
+                        if (k > old && own_index_ok(key_index(k), a.V, a.ws)) {
                             const uint4* src = reinterpret_cast<const uint4*>(
                                 static_cast<const uint8_t*>(a.w1) + static_cast<size_t>(key_index(k)) * (2 * kTcR));
 #pragma unroll
@@ -672,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) markov_generic_kernel(MarkovArgs 
                 const unsigned long long k = s_win[b];
                 int x = 0;
                 if (k == 0ull) set_status(a.ws, DSPARK_STATUS_NUMERIC);    // no finite candidate at all
-                else x = static_cast<int>(key_index(k));
+                else if (own_index_ok(key_index(k), a.V, a.ws)) x = static_cast<int>(key_index(k));
                 s_tok[i * a.B + b] = x;
                 if constexpr (!kTC) s_win[b] = 0ull;
             }

@@ -339,7 +339,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 if (i == 0) {
                     p = a.anchor[b];
                     if (p < 0 || p >= a.V) {
-                        set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+                        flag_input_index(a.ws);
                         p = 0;
                     }
                 } else {

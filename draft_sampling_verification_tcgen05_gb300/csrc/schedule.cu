@@ -512,7 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs
                 const int j = w0 + r * 32 + static_cast<int>(lane);
                 if (j < w1) {
                     const uint32_t d = slot[r] >> 16;
-                    dst[mycnt[d] + (slot[r] & 0xFFFFu)] = src[j];
+                    const int pos = mycnt[d] + static_cast<int>(slot[r] & 0xFFFFu);
+                    if (own_index_ok(pos, n, a.ws)) dst[pos] = src[j];
                 }
             }
         }
@@ -537,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs
     for (int j = tid; j < n; j += kThreads) {
         const int idx = src[j];
         a.selected[j] = j < K ? idx : -1;
-        key[swz(idx)] = j < K ? 1u : 0u;
+        if (own_index_ok(idx, n, a.ws)) key[swz(idx)] = j < K ? 1u : 0u;
     }
     __syncthreads();
     for (int b = tid; b < B; b += kThreads) {
@@ -833,6 +834,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
                 const uint32_t pos = s_pos[d] + static_cast<uint32_t>(t) - s_lstart[d];
                 const uint32_t owner = __umulhi(pos, magicP);
                 const uint32_t slot_o = pos - owner * static_cast<uint32_t>(P);
+                if (!own_index_ok(owner, kClusterCtas, a.ws) || !own_index_ok(slot_o, P, a.ws)) continue;
                 unsigned long long* dst = cluster.map_shared_rank(nxt, static_cast<int>(owner)) + slot_o;
                 if ((slot_o & 1u) == 0u) {
                     const bool pair = t + 1 < m && slot_o + 1 < static_cast<uint32_t>(P) &&
@@ -1096,7 +1098,7 @@ __global__ void __launch_bounds__(1024, 1) schedule_global_kernel(ScheduleArgs a
         const int idx = static_cast<int>(src[j] & 0xFFFFFFFFull);
         if (j < K) {
             a.selected[j] = idx;
-            atomicAdd(a.lengths + idx / N, 1);
+            if (own_index_ok(idx, n, a.ws)) atomicAdd(a.lengths + idx / N, 1);
         } else {
             a.selected[j] = -1;
         }

@@ -171,7 +171,7 @@ __device__ int decide_request(const VerifyArgs& a, int b) {
     }
     bad = __any_sync(0xFFFFFFFFu, bad);
     kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-    if (bad && lane == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+    if (bad && lane == 0) flag_input_index(a.ws);
     return bad ? -1 : ((kmin << 1) | (kmin < Lb ? 1 : 0));
 }
 

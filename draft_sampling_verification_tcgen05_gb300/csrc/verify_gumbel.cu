@@ -234,7 +234,7 @@ __device__ void decide(const GumbelArgs& a, int b) {
         if (m != 0u && kstar == Lb) kstar = min(kstar, k0 + __ffs(m) - 1);
     }
     if (bad) {
-        if (lane == 0) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
+        if (lane == 0) flag_input_index(a.ws);
         for (int k = static_cast<int>(lane); k <= g; k += 32) out[k] = -1;
         if (lane == 0) a.n_acc[b] = 0;
         return;

@@ -223,8 +223,8 @@ __device__ __forceinline__ int read_decision(const VLArgs& a, int b) {
 
 __device__ void write_bad(const VLArgs& a, int b, int bad) {
     if (lane_id() == 0) {
-        set_status(a.ws, ((bad & kBadNumeric) ? DSPARK_STATUS_NUMERIC : 0u) |
-                             ((bad & kBadRange) ? DSPARK_STATUS_INPUT_RANGE : 0u));
+        if (bad & kBadNumeric) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+        if (bad & kBadRange) flag_input_index(a.ws);
         a.decision[b] = -1 + 2;
     }
 }
@@ -351,6 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1) vl_rounds_kernel(VLArgs a) {
             const int li = static_cast<int>(f / per_req);
             const int b = j == 0 ? li : __ldcg(list + li);
             const long long req_end = min(static_cast<long long>(li + 1) * per_req, f1);
+            if (!own_index_ok(b, a.B, a.ws)) {                      // a work-list entry out of range
+                f = req_end;
+                continue;
+            }
             const uint32_t count = static_cast<uint32_t>(req_end - f);
             const int Lb = a.lengths != nullptr ? a.lengths[b] : a.g;
             const bool ok = j > 0 || (request_ok(a, b) && Lb > 0);

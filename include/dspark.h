@@ -75,11 +75,26 @@ typedef enum {
     DSPARK_OP_VERIFY_GUMBEL = 7
 } dspark_op;
 
-/* Device status-word bits (OR-ed by kernels; read with dspark_read_status). */
+/*
+ * Device status-word bits (OR-ed by kernels; read with dspark_read_status).
+ *   INPUT_RANGE  a value from the caller is out of its range (an anchor or draft
+ *                token outside [0, V), a length outside [0, gamma], a mapped
+ *                draft-to-target id outside the target vocabulary, a confidence
+ *                outside [0, 1], ...); the kernel substitutes a safe value and
+ *                never reads memory at the bad index.
+ *   INDEX        set only by a library built with -DDSPARK_CHECKED (a debugging
+ *                build with no counterpart on the pages, in which every gather
+ *                site checks its index): an index at a gather site was out of
+ *                range.  Beside INPUT_RANGE it marks a caller's index; alone it
+ *                marks an index the library computed itself (a token read back
+ *                from a step slot, a sorted candidate, a work-list entry), and
+ *                the access was skipped instead of made.
+ */
 #define DSPARK_STATUS_TIMEOUT      0x1u
 #define DSPARK_STATUS_NUMERIC      0x2u
 #define DSPARK_STATUS_INPUT_RANGE  0x4u
 #define DSPARK_STATUS_INTERNAL     0x8u
+#define DSPARK_STATUS_INDEX        0x10u
 
 /*
  * Bytes of workspace an operation needs.  op is a dspark_op; arguments an op
