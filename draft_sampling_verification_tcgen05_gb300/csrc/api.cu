@@ -6,6 +6,7 @@
 #include "host_common.h"
 
 #include <cudaTypedefs.h>
+#include <algorithm>
 #include <mutex>
 #include <stdarg.h>
 #include <stdio.h>
@@ -99,9 +100,28 @@ bool make_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
     return true;
 }
 
+namespace {
+
+// Zeroes the first bytes of a workspace (16-byte stores, then the tail byte by byte).  A kernel
+// rather than cudaMemsetAsync: in a CUDA graph a memset node ahead of each call's kernel measured
+// about 4 us of dependency latency, a small kernel node well under 1 us.
+__global__ void __launch_bounds__(256) clear_workspace_kernel(uint4* p, size_t n16, uint8_t* tail, size_t ntail) {
+    const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t i = i0; i < n16; i += stride) p[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (i0 < ntail) tail[i0] = 0;
+}
+
+}  // namespace
+
 dspark_status clear_workspace(void* ws, size_t bytes, cudaStream_t stream) {
-    const cudaError_t e = cudaMemsetAsync(ws, 0, bytes, stream);
-    if (e != cudaSuccess) return cuda_error(e, "cudaMemsetAsync(workspace)");
+    if (bytes == 0) return DSPARK_OK;
+    const size_t n16 = bytes / 16, ntail = bytes % 16;
+    const size_t blocks = std::min<size_t>(std::max<size_t>((n16 + 1023) / 1024, 1), 608);
+    clear_workspace_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<uint4*>(ws), n16, static_cast<uint8_t*>(ws) + n16 * 16, ntail);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "launch(clear workspace)");
     return DSPARK_OK;
 }
 

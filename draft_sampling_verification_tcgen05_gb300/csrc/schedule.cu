@@ -236,6 +236,7 @@ __device__ int choose_capacity(const ScheduleArgs& a, int n, SortedKey sorted, u
 __global__ void __launch_bounds__(32) schedule_warp_kernel(ScheduleArgs a) {
     __shared__ int s_at_rank[32];
     const int lane = static_cast<int>(threadIdx.x);
+    if (lane == 0) a.ws->status = 0u;            // this call's status word; only lane 0 sets bits
     const int B = a.B, N = a.N, n = B * N;
     const bool valid = lane < n;
     const int k = lane % N;
@@ -368,7 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs
     }
 
     // ---- 1. coalesced load of c, survival chain (one thread per request), keys ----
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) {
+        s_bad = 0;
+        a.ws->status = 0u;                       // this call's status word; only thread 0 sets bits
+    }
     for (int j = tid; j < n; j += kThreads) {
         key[swz(j)] = __float_as_uint(__ldg(a.c + j));
         idxA[j] = static_cast<uint16_t>(j);
@@ -666,6 +670,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
         cin[r] = j < m ? __ldg(a.c + base + j) : 0.f;
     }
     if (tid == 0) s_bad = 0;
+    // this call's status word: cleared by block 0 before the first cluster barrier; every bit is
+    // set after it
+    if (c == 0 && tid == 0) a.ws->status = 0u;
     for (int i = tid; i < static_cast<int>(kClusterCntBytes / 16); i += kClusterThreads)
         reinterpret_cast<uint4*>(cnt)[i] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -686,7 +693,6 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
     }
     if (bad) s_bad = 1;
     __syncthreads();
-    if (tid == 0 && s_bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
     for (int j = tid; j < m; j += kClusterThreads)
         keys[j] = (static_cast<unsigned long long>(order_key(surv[swz(j)])) << 32) | static_cast<unsigned long long>(base + j);
     __syncthreads();
@@ -771,6 +777,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
             }
         }
         cluster_wait();
+        if (pass == 0 && tid == 0 && s_bad) set_status(a.ws, DSPARK_STATUS_INPUT_RANGE);
         // (c) per digit: start in the output (smaller digits anywhere, then this digit in the
         //     blocks before this one) and start in this block's digit order
         uint32_t all_d = 0, tot_d = 0, incl_g = 0, incl_l = 0;
@@ -1011,6 +1018,8 @@ __global__ void __launch_bounds__(1024, 1) schedule_global_kernel(ScheduleArgs a
     const int n = B * N;
 
     // ---- 1. survival chain and keys ----
+    if (tid == 0) a.ws->status = 0u;             // this call's status word, cleared before any bit is set
+    __syncthreads();
     bool bad = false;
     for (int b = tid; b < B; b += kThreads) {
         float s = 1.f;
@@ -1170,9 +1179,7 @@ size_t schedule_workspace_bytes(int B, int N) {
 dspark_status launch_schedule(const float* cond_accept, const double* sps, int S, int B, int N,
                               int K_in, float* survival, int32_t* K_out, int32_t* lengths,
                               int32_t* selected, void* ws, cudaStream_t stream, const DeviceInfo& dev) {
-    (void)dev;
-    dspark_status st = clear_workspace(ws, sizeof(WsHeader), stream);
-    if (st != DSPARK_OK) return st;
+    // no separate clear: every schedule kernel zeroes its status word itself before setting a bit
     ScheduleArgs a;
     a.c = cond_accept;
     a.sps = sps;
