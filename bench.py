@@ -425,7 +425,9 @@ def measure(name, args, dev, dist, world, rank, full):
                       "verify": kernel_ms[2], "schedule": kernel_ms[3]},
         "roofline": roof,
         "markov_roofline": markov_roof,
-        "gpu_launches": 4 * args.steps,           # GEMM, Markov sampler with the confidence head, verify, schedule
+        # per step: GEMM, Markov sampler with the confidence head and verify, each after its
+        # workspace-clear kernel, then the scheduler (which clears its own status word)
+        "gpu_launches": 7 * args.steps,
         "step_launch": "one CUDA graph replay per step" if graph is not None else "four eager calls per step",
         "kernel_ms_note": "per-kernel CUDA-event times from an eager pass over the same K steps",
         "clocks": clk.summary(),
