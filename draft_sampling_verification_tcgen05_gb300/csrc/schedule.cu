@@ -586,6 +586,27 @@ constexpr size_t kClusterSmemBytes = kClusterSpsOffset + kClusterChunk * sizeof(
 static_assert(kCQuarters * kRadix == kClusterThreads && kCWarpsPerQuarter * kCQuarters == kClusterWarps,
               "digit scan layout");
 
+// Warp reductions by the hardware's 32-bit reduce instructions rather than shuffle rounds (on this
+// GPU a shuffle or a vote costs about as much SM time as a hundred cycles of simple arithmetic):
+// the sum of a u64 below 2^63 in three 21-bit parts, whose 32-lane sums cannot overflow.
+__device__ __forceinline__ unsigned long long warp_sum_u63(unsigned long long x) {
+    const uint32_t s0 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x & 0x1FFFFFull));
+    const uint32_t s1 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>((x >> 21) & 0x1FFFFFull));
+    const uint32_t s2 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x >> 42));
+    return static_cast<unsigned long long>(s0) + (static_cast<unsigned long long>(s1) << 21) +
+           (static_cast<unsigned long long>(s2) << 42);
+}
+
+// The warp's largest key and, among the lanes holding it, the smallest K (to every lane).
+__device__ __forceinline__ void warp_best_key(unsigned long long& key, int& K) {
+    const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
+    const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, hi == mhi ? lo : 0u);
+    const bool top = hi == mhi && lo == mlo;
+    K = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, top ? static_cast<uint32_t>(K) : 0xFFFFFFFFu));
+    key = (static_cast<unsigned long long>(mhi) << 32) | mlo;
+}
+
 // Requests [lo, hi) of block c when B requests are split into kCtas contiguous ranges.
 template <int kCtas>
 __device__ __forceinline__ void cluster_requests(int B, int c, int& lo, int& hi) {
@@ -639,6 +660,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
     __shared__ unsigned long long s_best[kWarps];
     __shared__ int s_bestK[kWarps];
     __shared__ unsigned long long s_T;                          // key at sorted position K - 1
+    __shared__ int s_Kfill;                                     // K, for every thread of the fill
     __shared__ int s_bad;
 
     const int tid = threadIdx.x;
@@ -684,11 +706,21 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
     bool bad = false;
     for (int b = tid; b < r_hi - r_lo; b += kClusterThreads) {
         float sv = 1.f;
-        for (int k = 0; k < N; ++k) {
-            const int j = b * N + k;
-            const float cp = clamp_prob(surv[swz(j)], bad);
-            sv = (k == 0) ? cp : __fmul_rn(sv, cp);
-            surv[swz(j)] = sv;
+        for (int k0 = 0; k0 < N; k0 += 8) {                      // eight loads in flight, then the chain
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = k0 + u < N ? surv[swz(b * N + k0 + u)] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (k0 + u < N) {
+                    const float cp = clamp_prob(v[u], bad);
+                    sv = (k0 + u == 0) ? cp : __fmul_rn(sv, cp);
+                    v[u] = sv;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (k0 + u < N) surv[swz(b * N + k0 + u)] = v[u];
         }
     }
     if (bad) s_bad = 1;
@@ -906,8 +938,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
                 cluster.map_shared_rank(&s_allpart[c], static_cast<int>(lane))[0] = total;
         }
         cluster.sync();
-        unsigned long long carry = static_cast<unsigned long long>(a.B) << 32;
-        for (int cc = 0; cc < c; ++cc) carry += s_allpart[cc];
+        // masses of the blocks before this one: one entry per lane and a warp sum in every warp
+        // (a loop over the entries in every thread costs more: 32 warps of broadcast loads)
+        const unsigned long long before = warp_sum_u63(lane < static_cast<uint32_t>(c) ? s_allpart[lane] : 0ull);
+        unsigned long long carry = (static_cast<unsigned long long>(a.B) << 32) + before;
         carry += s_wsum[warp] + incl - sum;                           // masses before this thread's positions
         unsigned long long best = 0ull;
         int bestK = 0x7FFFFFFF;
@@ -919,23 +953,13 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
                 if (k > best) { best = k; bestK = j_lo + jl0 + i + 1; }
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            const int oK = __shfl_xor_sync(0xFFFFFFFFu, bestK, o);
-            if (ok > best || (ok == best && oK < bestK)) { best = ok; bestK = oK; }
-        }
+        warp_best_key(best, bestK);
         if (lane == 0) { s_best[warp] = best; s_bestK[warp] = bestK; }
         __syncthreads();
         if (warp == 0) {
             best = s_best[lane];
             bestK = s_bestK[lane];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-                const int oK = __shfl_xor_sync(0xFFFFFFFFu, bestK, o);
-                if (ok > best || (ok == best && oK < bestK)) { best = ok; bestK = oK; }
-            }
+            warp_best_key(best, bestK);
             // the block's best with the key at its position K - 1 (local), to every block
             const unsigned long long T = bestK != 0x7FFFFFFF ? sorted[bestK - 1 - j_lo] : 0ull;
             if (lane < static_cast<uint32_t>(kClusterCtas)) {
@@ -945,31 +969,37 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
             }
         }
         cluster.sync();
-        unsigned long long bk = 0ull;
-        int bK = 0x7FFFFFFF, bc = 0;
-#pragma unroll
-        for (int cc = 0; cc < kClusterCtas; ++cc) {
-            const unsigned long long ok = s_allbest[cc];
-            const int oK = s_allK[cc];
-            if (ok > bk || (ok == bk && oK < bK)) { bk = ok; bK = oK; bc = cc; }
+        // the best over the blocks (one entry per lane) by warp 0; the fill reads K from shared memory
+        K = 0;
+        if (warp == 0) {
+            const unsigned long long mine = lane < static_cast<uint32_t>(kClusterCtas) ? s_allbest[lane] : 0ull;
+            const int mineK = lane < static_cast<uint32_t>(kClusterCtas) ? s_allK[lane] : 0x7FFFFFFF;
+            unsigned long long bk = mine;
+            int bK = mineK;
+            warp_best_key(bk, bK);
+            const uint32_t holder = __ballot_sync(0xFFFFFFFFu, mine == bk && mineK == bK);
+            if (bK == 0x7FFFFFFF) {                                   // every f was NaN or -inf: K = 1, flagged
+                if (c == 0 && lane == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
+                bK = 1;
+            } else if (lane == 0) {
+                s_T = s_allT[__ffs(holder) - 1];
+                have_T = true;
+            }
+            K = bK;
         }
-        if (bK == 0x7FFFFFFF) {                                       // every f was NaN or -inf: K = 1, flagged
-            if (c == 0 && tid == 0) set_status(a.ws, DSPARK_STATUS_NUMERIC);
-            bK = 1;
-        } else if (tid == 0) {
-            s_T = s_allT[bc];
-            have_T = true;
-        }
-        K = bK;
     }
 
     // ---- 4. fill ----
-    if (tid == 0 && K > 0 && !have_T) {                              // K fixed, or the flagged K = 1
-        const uint32_t last = static_cast<uint32_t>(K - 1);
-        const uint32_t owner = __umulhi(last, magicP);
-        s_T = cluster.map_shared_rank(keys + cur * kClusterChunk, static_cast<int>(owner))[last - owner * P];
+    if (tid == 0) {
+        s_Kfill = K;
+        if (K > 0 && !have_T) {                                       // K fixed, or the flagged K = 1
+            const uint32_t last = static_cast<uint32_t>(K - 1);
+            const uint32_t owner = __umulhi(last, magicP);
+            s_T = cluster.map_shared_rank(keys + cur * kClusterChunk, static_cast<int>(owner))[last - owner * P];
+        }
     }
     __syncthreads();
+    K = s_Kfill;
     cluster_arrive();                                                 // no remote access after this point
     // global stores only from here on: the release fences of the cluster barriers above never wait
     // for them
