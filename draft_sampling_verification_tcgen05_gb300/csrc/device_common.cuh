@@ -345,13 +345,14 @@ __device__ __forceinline__ uint32_t key_index(unsigned long long key) {
     return 0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull);
 }
 
+// Two hardware reduces (the high words, then the low words of the lanes holding the largest high
+// word) instead of five shuffle rounds of two words each: a shuffle occupies its SM sub-partition
+// for several issue cycles.
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, k, o);
-        k = other > k ? other : k;
-    }
-    return k;
+    const uint32_t hi = static_cast<uint32_t>(k >> 32), lo = static_cast<uint32_t>(k);
+    const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, hi == mhi ? lo : 0u);
+    return (static_cast<unsigned long long>(mhi) << 32) | mlo;
 }
 
 // ---------------------------------------------------------------------------

@@ -430,7 +430,9 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                         bool okw = !dead;
                         if (okw) okw = mbar_wait(&bar_tile[tl], static_cast<uint32_t>(i & 1), a.ws, a.timeout_ns, kWaitEpi);
                         if (okw) okw = mbar_wait(&bar_L_full[grp][lsg], lphg, a.ws, a.timeout_ns, kWaitEpi);
-                        dead = !__all_sync(0xFFFFFFFFu, okw);
+                        // lane 0's outcome decides for the warp (a shuffle, not a vote): when it saw
+                        // both phases complete the data is there for every lane
+                        dead = __shfl_sync(0xFFFFFFFFu, okw ? 0 : 1, 0) != 0;
                         if (!dead) {
                             tc_fence_after();
                             const uint32_t taddr = tmem + ((quad * 32u) << 16) + static_cast<uint32_t>(tl * Bp + c * kChunk);
@@ -581,9 +583,11 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                             // the table bounds the group's largest variate by the top byte of its word
                             const bool T0 = lb0 < INFINITY && __fadd_rn(gm0, gtab[W0 >> 24]) >= lb0;
                             const bool T1 = lb1 < INFINITY && __fadd_rn(gm1, gtab[W1 >> 24]) >= lb1;
-                            // the even lane of each pair reports its group; the warp draws them one by one
-                            uint32_t m0 = __ballot_sync(0xFFFFFFFFu, T0 && (q & 1) == 0);
-                            uint32_t m1 = __ballot_sync(0xFFFFFFFFu, T1 && (q & 1) == 0);
+                            // both lanes of a pair know both groups: the even lane reports the first,
+                            // the odd lane the second, in one vote; the warp draws them one by one
+                            const uint32_t mm = __ballot_sync(0xFFFFFFFFu, (q & 1) ? T1 : T0);
+                            uint32_t m0 = mm & 0x55555555u;
+                            uint32_t m1 = (mm & 0xAAAAAAAAu) >> 1;
                             const int row0 = (tile_lo + tl) * kTileV + static_cast<int>(quad * 32);
                             while ((m0 | m1) != 0u) {
                                 const bool second = m0 == 0u;
