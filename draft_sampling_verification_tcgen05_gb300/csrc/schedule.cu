@@ -145,10 +145,32 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
     return x;
 }
 
+// Warp reductions by the hardware's 32-bit reduce instructions rather than shuffle rounds (on this
+// GPU a shuffle occupies its sub-partition for about seven issue cycles, a vote about fourteen):
+// the sum of a u64 below 2^63 in three 21-bit parts, whose 32-lane sums cannot overflow.
+__device__ __forceinline__ unsigned long long warp_sum_u63(unsigned long long x) {
+    const uint32_t s0 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x & 0x1FFFFFull));
+    const uint32_t s1 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>((x >> 21) & 0x1FFFFFull));
+    const uint32_t s2 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x >> 42));
+    return static_cast<unsigned long long>(s0) + (static_cast<unsigned long long>(s1) << 21) +
+           (static_cast<unsigned long long>(s2) << 42);
+}
+
+// The warp's largest key and, among the lanes holding it, the smallest K (to every lane).
+__device__ __forceinline__ void warp_best_key(unsigned long long& key, int& K) {
+    const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
+    const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, hi == mhi ? lo : 0u);
+    const bool top = hi == mhi && lo == mlo;
+    K = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, top ? static_cast<uint32_t>(K) : 0xFFFFFFFFu));
+    key = (static_cast<unsigned long long>(mhi) << 32) | mlo;
+}
+
 // Capacity K* over the sorted order (sorted(j) = the sort key of the j-th candidate), shared by
-// both kernels.  Warp w owns a contiguous run of ranks and walks it 32 at a time: a first
-// walk sums its masses, a block scan of the warp sums gives each run's starting prefix, a
-// second walk forms every E(K) with an inclusive warp scan and keeps the best f(K).
+// the one-block kernels.  Thread t owns the contiguous K range [t per, (t + 1) per): it sums its
+// masses, one block scan of the thread sums gives each range its starting prefix, and a second
+// walk forms every E(K) and keeps the best f(K) (ascending K, so a strict comparison keeps the
+// smallest K).  The reductions over the block use the hardware's 32-bit reduce instructions.
 // Returns K* to every thread.
 template <int kThreads, typename SortedKey>
 __device__ int choose_capacity(const ScheduleArgs& a, int n, SortedKey sorted, unsigned long long* s_wsum,
@@ -157,73 +179,58 @@ __device__ int choose_capacity(const ScheduleArgs& a, int n, SortedKey sorted, u
     const int tid = threadIdx.x;
     const uint32_t lane = lane_id(), warp = warp_id();
     const int Kmax = a.S < n ? a.S : n;
-    const int run = (((Kmax + kWarps - 1) / kWarps) + 31) & ~31;
-    const int j0 = static_cast<int>(warp) * run, j1 = min(Kmax, j0 + run);
+    const int per = (Kmax + kThreads - 1) / kThreads;
+    const int j0 = min(Kmax, tid * per), j1 = min(Kmax, j0 + per);
     unsigned long long part = 0;
-    for (int j = j0 + static_cast<int>(lane); j < j1; j += 32) part += mass32(key_survival(sorted(j)));
-    part = warp_sum_u64(part);
-    if (lane == 0) s_wsum[warp] = part;
+    for (int j = j0; j < j1; ++j) part += mass32(key_survival(sorted(j)));
+    // block exclusive scan of the thread sums
+    unsigned long long incl = part;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= static_cast<uint32_t>(o)) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
     __syncthreads();
-    unsigned long long carry = static_cast<unsigned long long>(a.B) << 32;
-    for (int w = 0; w < static_cast<int>(warp); ++w) carry += s_wsum[w];
+    if (warp == 0) {
+        const unsigned long long v = lane < static_cast<uint32_t>(kWarps) ? s_wsum[lane] : 0ull;
+        unsigned long long x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= static_cast<uint32_t>(o)) x += y;
+        }
+        if (lane < static_cast<uint32_t>(kWarps)) s_wsum[lane] = x - v;
+    }
+    __syncthreads();
+    unsigned long long E = (static_cast<unsigned long long>(a.B) << 32) + s_wsum[warp] + incl - part;
     unsigned long long best_key = 0ull;                   // below every f > -inf
     int best_K = 0x7FFFFFFF;
-    for (int jg = j0; jg < j1; jg += 4 * 32) {
-        double sps4[4];                                    // four rounds of SPS loads in flight
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = jg + i * 32 + static_cast<int>(lane);
-            sps4[i] = j < j1 ? __ldg(a.sps + j) : 0.0;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = jg + i * 32 + static_cast<int>(lane);
-            const bool valid = j < j1;
-            const unsigned long long q = valid ? mass32(key_survival(sorted(j))) : 0ull;
-            unsigned long long incl = q;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= static_cast<uint32_t>(o)) incl += y;
-            }
-            if (valid) {
-                const unsigned long long k = objective_key(carry + incl, sps4[i]);
-                if (k > best_key) {                        // ascending K per lane: strict keeps the smallest
-                    best_key = k;
-                    best_K = j + 1;
-                }
-            }
-            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    for (int j = j0; j < j1; ++j) {
+        E += mass32(key_survival(sorted(j)));
+        const unsigned long long k = objective_key(E, __ldg(a.sps + j));
+        if (k > best_key) {
+            best_key = k;
+            best_K = j + 1;
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long ok = __shfl_xor_sync(0xFFFFFFFFu, best_key, o);
-        const int oK = __shfl_xor_sync(0xFFFFFFFFu, best_K, o);
-        if (ok > best_key || (ok == best_key && oK < best_K)) {
-            best_key = ok;
-            best_K = oK;
-        }
-    }
+    warp_best_key(best_key, best_K);
     if (lane == 0) {
         s_bk[warp] = best_key;
         s_bK[warp] = best_K;
     }
     __syncthreads();
-    if (tid == 0) {
-        unsigned long long bkey = 0ull;
-        int bK = 0x7FFFFFFF;
-        for (int w = 0; w < kWarps; ++w) {
-            if (s_bk[w] > bkey || (s_bk[w] == bkey && s_bK[w] < bK)) {
-                bkey = s_bk[w];
-                bK = s_bK[w];
+    if (warp == 0) {
+        unsigned long long bkey = lane < static_cast<uint32_t>(kWarps) ? s_bk[lane] : 0ull;
+        int bK = lane < static_cast<uint32_t>(kWarps) ? s_bK[lane] : 0x7FFFFFFF;
+        warp_best_key(bkey, bK);
+        if (lane == 0) {
+            if (bK == 0x7FFFFFFF) {             // every f was NaN or -inf: K = 1, flagged
+                set_status(a.ws, DSPARK_STATUS_NUMERIC);
+                bK = 1;
             }
+            *s_K = bK;
         }
-        if (bK == 0x7FFFFFFF) {             // every f was NaN or -inf: K = 1, flagged
-            set_status(a.ws, DSPARK_STATUS_NUMERIC);
-            bK = 1;
-        }
-        *s_K = bK;
     }
     __syncthreads();
     return *s_K;
@@ -381,12 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_smem_kernel(ScheduleArgs
     bool bad = false;
     for (int b = tid; b < B; b += kThreads) {
         float s = 1.f;
-        for (int k = 0; k < N; ++k) {
-            const int id = b * N + k;
-            const float c = clamp_prob(__uint_as_float(key[swz(id)]), bad);
-            s = (k == 0) ? c : __fmul_rn(s, c);
-            a.survival[id] = s;
-            key[swz(id)] = order_key(s);
+        for (int k0 = 0; k0 < N; k0 += 8) {                      // eight loads in flight, then the chain
+            uint32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = k0 + u < N ? key[swz(b * N + k0 + u)] : 0u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (k0 + u < N) {
+                    const float c = clamp_prob(__uint_as_float(v[u]), bad);
+                    s = (k0 + u == 0) ? c : __fmul_rn(s, c);
+                    a.survival[b * N + k0 + u] = s;
+                    v[u] = order_key(s);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (k0 + u < N) key[swz(b * N + k0 + u)] = v[u];
         }
     }
     if (bad) s_bad = 1;
@@ -585,27 +602,6 @@ constexpr size_t kClusterSpsOffset = 3 * kClusterKeyBytes + kClusterCntBytes + k
 constexpr size_t kClusterSmemBytes = kClusterSpsOffset + kClusterChunk * sizeof(double);
 static_assert(kCQuarters * kRadix == kClusterThreads && kCWarpsPerQuarter * kCQuarters == kClusterWarps,
               "digit scan layout");
-
-// Warp reductions by the hardware's 32-bit reduce instructions rather than shuffle rounds (on this
-// GPU a shuffle occupies its sub-partition for about seven issue cycles, a vote about fourteen):
-// the sum of a u64 below 2^63 in three 21-bit parts, whose 32-lane sums cannot overflow.
-__device__ __forceinline__ unsigned long long warp_sum_u63(unsigned long long x) {
-    const uint32_t s0 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x & 0x1FFFFFull));
-    const uint32_t s1 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>((x >> 21) & 0x1FFFFFull));
-    const uint32_t s2 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x >> 42));
-    return static_cast<unsigned long long>(s0) + (static_cast<unsigned long long>(s1) << 21) +
-           (static_cast<unsigned long long>(s2) << 42);
-}
-
-// The warp's largest key and, among the lanes holding it, the smallest K (to every lane).
-__device__ __forceinline__ void warp_best_key(unsigned long long& key, int& K) {
-    const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
-    const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
-    const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, hi == mhi ? lo : 0u);
-    const bool top = hi == mhi && lo == mlo;
-    K = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, top ? static_cast<uint32_t>(K) : 0xFFFFFFFFu));
-    key = (static_cast<unsigned long long>(mhi) << 32) | mlo;
-}
 
 // Requests [lo, hi) of block c when B requests are split into kCtas contiguous ranges.
 template <int kCtas>
