@@ -355,6 +355,16 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k)
     return (static_cast<unsigned long long>(mhi) << 32) | mlo;
 }
 
+// Sum over the warp, modulo 2^64 like a shuffle-tree sum, by three hardware reduces: the value in
+// parts of 21, 21 and 22 bits, whose 32-lane sums cannot overflow 32 bits.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
+    const uint32_t s0 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x & 0x1FFFFFull));
+    const uint32_t s1 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>((x >> 21) & 0x1FFFFFull));
+    const uint32_t s2 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x >> 42));
+    return static_cast<unsigned long long>(s0) + (static_cast<unsigned long long>(s1) << 21) +
+           (static_cast<unsigned long long>(s2) << 42);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarrier and TMA.
 // ---------------------------------------------------------------------------

@@ -139,24 +139,9 @@ __device__ __forceinline__ unsigned long long objective_key(unsigned long long E
     return (fb >> 63) ? ~fb : (fb | 0x8000000000000000ull);
 }
 
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-    return x;
-}
-
-// Warp reductions by the hardware's 32-bit reduce instructions rather than shuffle rounds (on this
-// GPU a shuffle occupies its sub-partition for about seven issue cycles, a vote about fourteen):
-// the sum of a u64 below 2^63 in three 21-bit parts, whose 32-lane sums cannot overflow.
-__device__ __forceinline__ unsigned long long warp_sum_u63(unsigned long long x) {
-    const uint32_t s0 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x & 0x1FFFFFull));
-    const uint32_t s1 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>((x >> 21) & 0x1FFFFFull));
-    const uint32_t s2 = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(x >> 42));
-    return static_cast<unsigned long long>(s0) + (static_cast<unsigned long long>(s1) << 21) +
-           (static_cast<unsigned long long>(s2) << 42);
-}
-
-// The warp's largest key and, among the lanes holding it, the smallest K (to every lane).
+// The warp's largest key and, among the lanes holding it, the smallest K (to every lane), by the
+// hardware's 32-bit reduce instructions rather than shuffle rounds (on this GPU a shuffle occupies
+// its sub-partition for about seven issue cycles, a vote about fourteen).
 __device__ __forceinline__ void warp_best_key(unsigned long long& key, int& K) {
     const uint32_t hi = static_cast<uint32_t>(key >> 32), lo = static_cast<uint32_t>(key);
     const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
@@ -936,7 +921,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) schedule_cluster_kernel(Sc
         cluster.sync();
         // masses of the blocks before this one: one entry per lane and a warp sum in every warp
         // (a loop over the entries in every thread costs more: 32 warps of broadcast loads)
-        const unsigned long long before = warp_sum_u63(lane < static_cast<uint32_t>(c) ? s_allpart[lane] : 0ull);
+        const unsigned long long before = warp_sum_u64(lane < static_cast<uint32_t>(c) ? s_allpart[lane] : 0ull);
         unsigned long long carry = (static_cast<unsigned long long>(a.B) << 32) + before;
         carry += s_wsum[warp] + incl - sum;                           // masses before this thread's positions
         unsigned long long best = 0ull;

@@ -92,12 +92,6 @@ __device__ __forceinline__ void masses4(const float* rt, const float* rd, int e,
     }
 }
 
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-    return x;
-}
-
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long x) {
     const uint32_t lane = lane_id();
 #pragma unroll
