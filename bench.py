@@ -291,8 +291,14 @@ def measure(name, args, dev, dist, world, rank, full):
     # each replica serves its own requests: independent noise streams per rank
     seed_draft, seed_verify = replica_seed(0, rank), replica_seed(2, rank)
 
+    # Verification reads the draft tokens and scheduling the head's confidences: neither needs
+    # the other, so the step runs them on two streams (fork after the sampler, join at the end).
+    # The eager pass that times each kernel runs them one after the other.
+    sched_stream = torch.cuda.Stream(dev)
+
     def step(k=None):
         e = ev[k] if k is not None else None
+        cur = torch.cuda.current_stream()
         if e: e[0].record(stream)
         with _nvtx("dspark_draft_logits"):
             ds.dspark_draft_logits(X, W, logits=L, workspace=ws_g)
@@ -301,13 +307,21 @@ def measure(name, args, dev, dist, world, rank, full):
             ds.dspark_markov_sample_conf(L_markov.view(B, N, V), anchor, w1, w2, temp, seed_draft, 0, X, w_h, w_e, beta,
                                          tau, draft_tokens=tok, conf=conf, workspace=ws_m)
         if e: e[2].record(stream)
+        if e is None:
+            sched_stream.wait_stream(cur)
+            with torch.cuda.stream(sched_stream), _nvtx("dspark_schedule"):
+                ds.dspark_schedule(conf, sps, -1, survival=surv, K_out=K_out, lengths=lens, selected=sel,
+                                   workspace=ws_s)
         with _nvtx("dspark_verify"):
             ds.dspark_verify(p_t, p_d, tok, None, seed_verify, 0, out_tokens=out, num_accepted=nacc, workspace=ws_v)
         if e: e[3].record(stream)
-        with _nvtx("dspark_schedule"):
-            ds.dspark_schedule(conf, sps, -1, survival=surv, K_out=K_out, lengths=lens, selected=sel,
-                               workspace=ws_s)
-        if e: e[4].record(stream)
+        if e is None:
+            cur.wait_stream(sched_stream)
+        else:
+            with _nvtx("dspark_schedule"):
+                ds.dspark_schedule(conf, sps, -1, survival=surv, K_out=K_out, lengths=lens, selected=sel,
+                                   workspace=ws_s)
+            e[4].record(stream)
 
     for _ in range(args.warmup):
         flush_l2(1)
@@ -428,7 +442,8 @@ def measure(name, args, dev, dist, world, rank, full):
         # per step: GEMM, Markov sampler with the confidence head and verify, each after its
         # workspace-clear kernel, then the scheduler (which clears its own status word)
         "gpu_launches": 7 * args.steps,
-        "step_launch": "one CUDA graph replay per step" if graph is not None else "four eager calls per step",
+        "step_launch": ("one CUDA graph replay per step (verify and schedule on two streams after the sampler)"
+                        if graph is not None else "four eager calls per step"),
         "kernel_ms_note": "per-kernel CUDA-event times from an eager pass over the same K steps",
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
