@@ -46,8 +46,8 @@ WORKLOAD_TEMPERATURE = {"qwen3_8b_single": 1.0, "batched_draft": 0.8, "tiny": 1.
 # each workload, from one ncu capture of that kernel on that workload, with a digest of the
 # kernel's sources at capture time: once the sources change the figure is reported as null.
 GEMM_TRAFFIC = {
-    "qwen3_8b_single": {"bytes": 1244770560 + 5357568, "src_digest": "eeb3fed5834d"},
-    "batched_draft": {"bytes": 1276655872 + 593545728, "src_digest": "eeb3fed5834d"},
+    "qwen3_8b_single": {"bytes": 1244833280 + 5136640, "src_digest": "fb8ff20f07fe"},
+    "batched_draft": {"bytes": 1272637696 + 593294592, "src_digest": "fb8ff20f07fe"},
 }
 GEMM_SOURCES = ("draft_sampling_verification_tcgen05_gb300/csrc/draft_logits.cu",
                 "draft_sampling_verification_tcgen05_gb300/csrc/device_common.cuh")
