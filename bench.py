@@ -602,9 +602,9 @@ def measure(name, args, dev, dist, world, rank, full):
                                      "median of 20 launches, L2 flushed, outside the step")
     res["schedule_b1024_n16"] = {"ms": sched_cold_ms, "warm_ms": sched_warm_ms, "candidates": sc.B * sc.N,
                                  "K": int(sc_out[1].item()),
-                                 "note": "dspark_schedule per call (workspace clear + one kernel on a cluster of "
-                                         "16 blocks): ms = median of 20 calls with L2 flushed before each, warm_ms "
-                                         "= mean of 20 calls back to back"}
+                                 "note": "dspark_schedule per call (one kernel on a cluster of 16 blocks; it clears "
+                                         "its own status word): ms = median of 20 calls with L2 flushed before "
+                                         "each, warm_ms = mean of 20 calls back to back"}
     res["_oracle_inputs"] = (d, v, s, di, vi, si, T, None if zipf_host is None else zipf_host.__getitem__,
                              gpu_step)
     return res
