@@ -107,9 +107,9 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* ws, uint32_t phase, long 
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
+        // release on arrival, acquire on the poll; the block barriers carry both to every thread
         int ok = 1;
         const uint32_t target = (phase + 1u) * gridDim.x;
-        __threadfence();
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(&ws->barrier) : "memory");
         long long t0 = global_ns();
         uint32_t spins = 0;
@@ -125,7 +125,6 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* ws, uint32_t phase, long 
             }
             __nanosleep(64);
         }
-        __threadfence();
         s_ok = ok;
     }
     __syncthreads();
@@ -136,10 +135,8 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* ws, uint32_t phase, long 
 // on the other blocks between arriving and waiting.
 __device__ __forceinline__ void grid_arrive(WsHeader* ws) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
+    if (threadIdx.x == 0)                        // release: covers the block's writes before the barrier
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(&ws->barrier) : "memory");
-    }
 }
 
 __device__ __forceinline__ bool grid_wait(WsHeader* ws, uint32_t phase, long long timeout_ns, uint32_t where) {
@@ -161,8 +158,7 @@ __device__ __forceinline__ bool grid_wait(WsHeader* ws, uint32_t phase, long lon
             }
             __nanosleep(32);
         }
-        __threadfence();
-        s_ok2 = ok;
+        s_ok2 = ok;                              // the acquire above orders the block's later reads
     }
     __syncthreads();
     return s_ok2 != 0;
@@ -180,9 +176,10 @@ __device__ __forceinline__ bool grid_barrier_named(WsHeader* ws, uint32_t phase,
                                                    bool leader, volatile int* s_ok) {
     named_bar_sync(bar_id, nthreads);
     if (leader) {
+        // the release of the arrival covers every write the block's threads made before the named
+        // barrier, and the acquire of the poll every read after it: no separate fences
         int ok = 1;
         const uint32_t target = (phase + 1u) * gridDim.x;
-        __threadfence();
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(&ws->barrier) : "memory");
         const long long t0 = global_ns();
         uint32_t spins = 0;
@@ -198,7 +195,6 @@ __device__ __forceinline__ bool grid_barrier_named(WsHeader* ws, uint32_t phase,
             }
             __nanosleep(32);
         }
-        __threadfence();
         *s_ok = ok;
     }
     named_bar_sync(bar_id, nthreads);

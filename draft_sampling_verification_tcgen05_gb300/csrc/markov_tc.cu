@@ -490,7 +490,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 named_bar_sync(kBarEpi, 32 * kEpiWarps);
                 if (epi == 0 && lane == 0) {
                     uint32_t* pub = a.lay.pub + static_cast<size_t>(i) * kPubStride;
-                    __threadfence();
+                    // release: covers the bounds the group leads published before the named barrier
                     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(pub) : "memory");
                     const long long t0 = global_ns();
                     while (ld_acquire_u32(pub) < gridDim.x && !aborted(a.ws) &&
