@@ -86,6 +86,15 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
+// Counter increment with release (every write the thread, or its block or warp through a barrier
+// before it, made is visible first) and acquire (the caller's later reads see what the other
+// incrementers released): the "last one to finish" pattern without separate fences.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
     return *reinterpret_cast<const volatile uint32_t*>(p);
 }

@@ -335,15 +335,13 @@ __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(VerifyArgs a
             const float* rd = (dec & 1) ? a.p_d + (static_cast<size_t>(b) * g + kstar) * V : nullptr;
             segment_sums(rt, rd, V, vec, s0, s1, a.seg + static_cast<size_t>(b) * n_seg);
         }
-        __threadfence();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0) {                                   // release the block's sums, acquire the others'
             const uint32_t cnt = static_cast<uint32_t>(s1 - s0);
-            s_last = atomicAdd(a.done + b, cnt) + cnt == static_cast<uint32_t>(n_seg);
+            s_last = atom_add_acq_rel(a.done + b, cnt) + cnt == static_cast<uint32_t>(n_seg);
         }
         __syncthreads();
         if (s_last) {
-            __threadfence();
             finish_request(a, b, dec, s_seg, s_red, s_scan, &s_pick, &s_tloc);
             __syncthreads();                              // shared scratch is reused by the next request
         }

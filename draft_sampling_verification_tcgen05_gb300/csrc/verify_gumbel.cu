@@ -307,12 +307,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm) verify_gumbel_kernel(G
         }
         // count this warp's chunks of request b; the warp completing the count decides it
         uint32_t last = 0;
-        if (lane == 0) {
-            __threadfence();
-            last = atomicAdd(a.done + b, count) + count == static_cast<uint32_t>(per_req) ? 1u : 0u;
-        }
+        if (lane == 0)                                   // release this warp's keys, acquire the others'
+            last = atom_add_acq_rel(a.done + b, count) + count == static_cast<uint32_t>(per_req) ? 1u : 0u;
+        __syncwarp();                                    // the other lanes read after lane 0's acquire
         if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-            __threadfence();
             decide(a, b);
         }
     }

@@ -375,24 +375,20 @@ __global__ void __launch_bounds__(kThreads, 1) vl_rounds_kernel(VLArgs a) {
                 }
                 if (live) {
                     uint32_t last = 0;
-                    if (lane == 0) {
-                        __threadfence();
-                        last = atomicAdd(a.rowcnt + static_cast<size_t>(b) * a.g + k, rcount) + rcount ==
+                    if (lane == 0)                       // release this warp's partials, acquire the others'
+                        last = atom_add_acq_rel(a.rowcnt + static_cast<size_t>(b) * a.g + k, rcount) + rcount ==
                                        static_cast<uint32_t>(a.n_chunk) ? 1u : 0u;
-                    }
+                    __syncwarp();
                     if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-                        __threadfence();
                         decide_row(a, b, k, k0);
                     }
                 }
             }
             uint32_t last = 0;
-            if (lane == 0) {
-                __threadfence();
-                last = atomicAdd(a.done + b, count) + count == static_cast<uint32_t>((j + 1) * per_req) ? 1u : 0u;
-            }
+            if (lane == 0)
+                last = atom_add_acq_rel(a.done + b, count) + count == static_cast<uint32_t>((j + 1) * per_req) ? 1u : 0u;
+            __syncwarp();
             if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-                __threadfence();
                 decide_request(a, b, j, next_base);
             }
         }
@@ -685,12 +681,10 @@ __global__ void __launch_bounds__(kDrawThreads, 2) vl_draw_kernel(VLArgs a) {
         }
         f = req_end;
         uint32_t last = 0;
-        if (lane == 0) {
-            __threadfence();
-            last = atomicAdd(a.done3 + b, count) + count == static_cast<uint32_t>(a.n_chunk3) ? 1u : 0u;
-        }
+        if (lane == 0)
+            last = atom_add_acq_rel(a.done3 + b, count) + count == static_cast<uint32_t>(a.n_chunk3) ? 1u : 0u;
+        __syncwarp();
         if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-            __threadfence();
             finish(a, b, dec);
         }
     }
