@@ -7,6 +7,8 @@
 // Design (sm_103a): a persistent, warp-specialised tcgen05 GEMM.
 //   warp 0      one thread issues TMA loads of 128-byte K slices of both
 //               operands (128-byte swizzle) into a ring of shared-memory stages
+//               (one slice per stage; four or two adjacent slices per stage in
+//               the decode shapes)
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
 //               (M = 128, N = BN, K = 16 for bf16 / 8 for tf32) into one of two
 //               fp32 accumulators in TMEM and commits each stage back to the
@@ -43,17 +45,27 @@ struct GemmArgs {
     long long timeout_ns;
 };
 
+// A stage holds kSlices adjacent 128-byte K slices of both operands, the A slices copied back to
+// back, so the memory-bound decode shapes read each lm_head row in runs of kSlices x 128 bytes.
+// Measured on the decode GEMM (M = 8 and M = 24, H = 4096, V = 151936): four slices in three
+// 72 KB stages (BN = 16) and two in five 40 KB stages (BN = 32) run about 2 us (1 %) faster than
+// one slice in ten or nine stages; four slices at BN = 32 leave two stages and run slower.
+template <int BN>
+constexpr int slices_for() { return BN <= 16 ? 4 : BN <= 32 ? 2 : 1; }
+
 template <int BN>
 struct GemmCfg {
-    static constexpr uint32_t kStageBytes = (kTileA + BN) * kRowBytes;
-    static constexpr int kStages = std::min<int>(12, (192 * 1024) / kStageBytes);
+    static constexpr int kSlices = slices_for<BN>();
+    static constexpr uint32_t kSliceBytes = (kTileA + BN) * kRowBytes;
+    static constexpr uint32_t kStageBytes = kSlices * kSliceBytes;
+    static constexpr int kStages = std::min<int>(12, (kSlices == 1 ? 192 * 1024 : 216 * 1024) / kStageBytes);
     static constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
 };
 
 template <int BN>
 struct GemmSmem {
-    alignas(1024) uint8_t a[GemmCfg<BN>::kStages][kTileA * kRowBytes];
-    alignas(1024) uint8_t b[GemmCfg<BN>::kStages][BN * kRowBytes];
+    alignas(1024) uint8_t a[GemmCfg<BN>::kStages][GemmCfg<BN>::kSlices][kTileA * kRowBytes];
+    alignas(1024) uint8_t b[GemmCfg<BN>::kStages][GemmCfg<BN>::kSlices][BN * kRowBytes];
     uint64_t full[GemmCfg<BN>::kStages];
     uint64_t empty[GemmCfg<BN>::kStages];
     uint64_t tmem_full[2];
@@ -69,9 +81,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     using Cfg = GemmCfg<BN>;
     using Smem = GemmSmem<BN>;
     constexpr int kStages = Cfg::kStages;
-    constexpr int kKElems = kTF32 ? 32 : 64;                 // K elements per stage
+    constexpr int kSlices = Cfg::kSlices;
+    constexpr int kKElems = kTF32 ? 32 : 64;                 // K elements per slice
     constexpr int kMmaK = kTF32 ? 8 : 16;                    // K per MMA instruction
-    constexpr int kMmaPerStage = kKElems / kMmaK;            // 4
+    constexpr int kMmaPerSlice = kKElems / kMmaK;            // 4
     constexpr uint32_t kIdesc = mma_idesc(kTileA, BN, kTF32);
 
     extern __shared__ uint8_t smem_raw[];
@@ -119,14 +132,17 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
                 const int a_tile = t % p.tiles_a, b_tile = t / p.tiles_a;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = 0; kb < p.k_blocks; kb += kSlices) {
                     if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.ws, p.timeout_ns, kWaitProducer)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&s.full[stage], Cfg::kStageBytes);
-                    tma_load_2d(s.a[stage], &tmA, kb * kKElems, a_tile * kTileA, &s.full[stage], pol_a);
-                    tma_load_2d(s.b[stage], &tmB, kb * kKElems, b_tile * BN, &s.full[stage], pol_b);
+                    const int ns = p.k_blocks - kb < kSlices ? p.k_blocks - kb : kSlices;
+                    mbar_arrive_expect_tx(&s.full[stage], static_cast<uint32_t>(ns) * Cfg::kSliceBytes);
+                    for (int j = 0; j < ns; ++j)
+                        tma_load_2d(s.a[stage][j], &tmA, (kb + j) * kKElems, a_tile * kTileA, &s.full[stage], pol_a);
+                    for (int j = 0; j < ns; ++j)
+                        tma_load_2d(s.b[stage][j], &tmB, (kb + j) * kKElems, b_tile * BN, &s.full[stage], pol_b);
                     issued[stage] = true;
                     issued_parity[stage] = phase;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -156,19 +172,22 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = 0; kb < p.k_blocks; kb += kSlices) {
                     if (!mbar_wait(&s.full[stage], phase, p.ws, p.timeout_ns, kWaitMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(s.a[stage]);
-                    const uint32_t b_addr = smem_u32(s.b[stage]);
+                    const int ns = p.k_blocks - kb < kSlices ? p.k_blocks - kb : kSlices;
+                    for (int j = 0; j < ns; ++j) {
+                        const uint32_t a_addr = smem_u32(s.a[stage][j]);
+                        const uint32_t b_addr = smem_u32(s.b[stage][j]);
 #pragma unroll
-                    for (int k = 0; k < kMmaPerStage; ++k) {
-                        const uint64_t adesc = sw128_kmajor_desc(a_addr + k * 32);
-                        const uint64_t bdesc = sw128_kmajor_desc(b_addr + k * 32);
-                        mma_issue<kTF32>(d_tmem, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < kMmaPerSlice; ++k) {
+                            const uint64_t adesc = sw128_kmajor_desc(a_addr + k * 32);
+                            const uint64_t bdesc = sw128_kmajor_desc(b_addr + k * 32);
+                            mma_issue<kTF32>(d_tmem, adesc, bdesc, kIdesc, (kb | j | k) != 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&s.empty[stage]);          // stage reusable once these MMAs finish
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }

@@ -32,10 +32,15 @@ def test_tiny_fp32_tf32_full(cuda_lib):
 @pytest.mark.parametrize("M,H,V", [(1, 64, 1), (3, 136, 100), (8, 256, 1000), (17, 200, 4097),
                                    (100, 64, 333), (129, 128, 520), (256, 64, 300),
                                    (300, 192, 777), (513, 72, 1031), (384, 128, 129),
-                                   (640, 256, 2000), (1024, 64, 256)])
+                                   (640, 256, 2000), (1024, 64, 256), (5, 1096, 3000), (24, 1352, 2100),
+                                   (300, 128, 11900), (1024, 64, 5000), (520, 96, 13000)])
 def test_ragged_shapes(cuda_lib, dtype, M, H, V):
     """Several tiles with ragged tails in M, V and K, in both tile shapes (swap for M <= 256; above,
-    CTA-pair 256 x 256 tiles for bf16, including pairs whose second half lies wholly past M or V)."""
+    CTA-pair 256 x 256 tiles for bf16, including pairs whose second half lies wholly past M or V).
+    The decode tiles put four (M <= 16) or two (M <= 32) K slices in a stage: H = 1096 and 1352
+    wrap their rings several times per tile and end on a stage with fewer slices.  94, 80 and 153
+    pair tiles take the persistent pairs more than one round, ending on a partial round, with V
+    ending 124, 136 and 200 entries into the last tile."""
     if dtype == "f32" and H % 4:
         pytest.skip("fp32 rows must be 16-byte multiples")
     X = normal_rows(M, H, 1.0, 77, "hidden")
