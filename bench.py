@@ -250,7 +250,9 @@ def measure(name, args, dev, dist, world, rank, full):
     d_in, d_out = Arena(in_specs, device=dev), Arena(out_specs, device=dev)
     for k, t in h_in.items():
         d_in.view(k).copy_(t)
-    X, anchor, temp, p_t, p_d, sps = (d_in.view(k) for k in ("X", "anchor", "temp", "p_t", "p_d", "sps"))
+    in_names = ("X", "anchor", "temp", "p_t", "p_d", "sps")
+    step_inputs = tuple(d_in.view(k) for k in in_names)
+    X, anchor, temp, p_t, p_d, sps = step_inputs
     tok, out, nacc, K_out, lens, sel, surv, conf = (d_out.view(k) for k in ("tok", "out", "nacc", "K_out", "lens", "sel",
                                                                             "surv", "conf"))
     # the calibrated confidence head's weights (synthetic): w_h ~ N(0, 1/H), w_e ~ N(0, 1/r), tau per position
@@ -296,7 +298,9 @@ def measure(name, args, dev, dist, world, rank, full):
     # The eager pass that times each kernel runs them one after the other.
     sched_stream = torch.cuda.Stream(dev)
 
-    def step(k=None):
+    def step(k=None, inp=None):
+        # inp: (hidden, anchor, temperature, p_t, p_d, sps) views of another input arena
+        X, anchor, temp, p_t, p_d, sps = inp if inp is not None else step_inputs
         e = ev[k] if k is not None else None
         cur = torch.cuda.current_stream()
         if e: e[0].record(stream)
@@ -464,29 +468,52 @@ def measure(name, args, dev, dist, world, rank, full):
     # ---------------- end to end through host buffers ----------------
     e2e = None
     if not args.skip_e2e:
-        # the step's inputs in one pinned host arena laid out like the device one (copied whole),
-        # and the results read back whole from the device output arena
+        # The step's inputs sit in one pinned host arena laid out like the device one and are
+        # copied whole every step; the results are read back whole after every step.  Two device
+        # input arenas: step k+1's inputs cross on a copy stream while step k runs from the other
+        # arena (an event keeps a copy out of an arena until the step reading it is done).  The
+        # timed region runs from the first step's copy to the last step's read-back; every
+        # step's inputs (1.29 GB on the batched draft) are larger than L2, so no flush is added.
         hin, hout = Arena(in_specs, pin=True), Arena(out_specs, pin=True)
         for k, t in h_in.items():
             hin.view(k).copy_(t)
         h2d, d2h = hin.nbytes, hout.nbytes
-        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        for k in range(args.warmup + args.steps):
-            timed = k >= args.warmup
-            flush_l2(k)
-            if timed:
-                e0[k - args.warmup].record(stream)
-            d_in.buf.copy_(hin.buf, non_blocking=True)
-            step()
-            hout.buf.copy_(d_out.buf, non_blocking=True)
-            if timed:
-                e1[k - args.warmup].record(stream)
-            stream.synchronize()
-        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(e0, e1)]))
-        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+        d_in2 = Arena(in_specs, device=dev)
+        arenas = (d_in, d_in2)
+        views = tuple(tuple(a.view(k) for k in in_names) for a in arenas)
+        copy_stream = torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event() for _ in arenas]
+        consumed = [torch.cuda.Event() for _ in arenas]
+
+        def copy_in(j):
+            copy_stream.wait_event(consumed[j])
+            with torch.cuda.stream(copy_stream):
+                arenas[j].buf.copy_(hin.buf, non_blocking=True)
+            copied[j].record(copy_stream)
+
+        def run(n):
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(copy_stream)
+            copy_in(0)
+            for k in range(n):
+                j = k % 2
+                if k + 1 < n:
+                    copy_in(1 - j)
+                stream.wait_event(copied[j])
+                step(inp=views[j])
+                hout.buf.copy_(d_out.buf, non_blocking=True)
+                consumed[j].record(stream)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / n
+
+        run(args.warmup)
+        e2e_ms = max_over_ranks(run(args.steps), dist, dev)
         e2e = {"value": job_throughput(M, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+               "note": "every step copies its inputs from pinned host memory and reads its results back; "
+                       "step k+1's copy overlaps step k on a second stream (two device input arenas)"}
     res["e2e"] = e2e
 
     # ---------------- the library's other entry points, timed on their own ----------------
