@@ -157,6 +157,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
     __shared__ int s_prev[256];
     __shared__ float s_invT[256];
     __shared__ float s_lb[kGroups][kChunk];
+    __shared__ uint32_t s_lbv[256];                                    // the step's bounds, as read by the wait
     __shared__ unsigned long long s_part[kGroups][4][kChunk];
     __shared__ unsigned long long s_best[kGroups][kChunk];
     __shared__ float s_zmax[256];                                      // block max of z per request
@@ -486,17 +487,35 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                     named_bar_sync(kBarGroup0 + grp, 128);
                 }
 
-                // ---- wait (bounded) until every block has published its bounds for this step ----
+                // ---- wait (bounded) until every block has published its bounds for this step.  The
+                //      bounds are read in the same polls as the count, so pass 2 starts without
+                //      another round trip: every published bound is a value some element reaches, so
+                //      a read that missed a late bound (or a wait that ran out) only weakens the
+                //      pruning, and the result stays exact ----
                 named_bar_sync(kBarEpi, 32 * kEpiWarps);
-                if (epi == 0 && lane == 0) {
+                if (epi == 0) {
                     uint32_t* pub = a.lay.pub + static_cast<size_t>(i) * kPubStride;
                     // release: covers the bounds the group leads published before the named barrier
-                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(pub) : "memory");
+                    if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(pub) : "memory");
+                    __syncwarp();
                     const long long t0 = global_ns();
-                    while (ld_acquire_u32(pub) < gridDim.x && !aborted(a.ws) &&
-                           global_ns() - t0 < a.timeout_ns)
+                    uint32_t lbv[8];
+                    while (true) {
+                        const uint32_t cnt = ld_volatile_u32(pub);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int b = static_cast<int>(lane) + 32 * j;
+                            lbv[j] = b < a.B ? ld_volatile_u32(lbs + b) : 0u;
+                        }
+                        const bool stop = cnt >= gridDim.x || aborted(a.ws) || global_ns() - t0 >= a.timeout_ns;
+                        if (__any_sync(0xFFFFFFFFu, stop)) break;
                         __nanosleep(32);
-                    // running out only weakens the bound; the result stays exact
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int b = static_cast<int>(lane) + 32 * j;
+                        if (b < a.B) s_lbv[b] = lbv[j];
+                    }
                 }
                 named_bar_sync(kBarEpi, 32 * kEpiWarps);
 
@@ -509,8 +528,7 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                     if (c >= n_chunks) continue;
                     if (grp_lead && lane < kChunk) {
                         const int b = c * kChunk + static_cast<int>(lane);
-                        s_lb[grp][lane] = (b < a.B && s_invT[b] > 0.f) ? float_from_order_bits(__ldcg(lbs + b))
-                                                                        : INFINITY;
+                        s_lb[grp][lane] = (b < a.B && s_invT[b] > 0.f) ? float_from_order_bits(s_lbv[b]) : INFINITY;
                         s_best[grp][lane] = 0ull;
                     }
                     named_bar_sync(kBarGroup0 + grp, 128);
