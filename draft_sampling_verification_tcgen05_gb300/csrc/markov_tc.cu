@@ -349,14 +349,16 @@ markov_tc_kernel(const __grid_constant__ CUtensorMap tmW2, const __grid_constant
                 s_prev[b] = p;
             }
             named_bar_sync(kBarStep, kStepThreads);
+            // 16-byte cp.async copies: all of a thread's pieces are in flight at once and none
+            // passes through registers
             for (int idx = stid; idx < a.B * chunks16; idx += kStepThreads) {
                 const int b = idx / chunks16, c16 = idx % chunks16;
                 const int kb = c16 >> 3, cc = c16 & 7;
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                    static_cast<const uint8_t*>(a.w1) + (static_cast<size_t>(s_prev[b]) * a.r + c16 * 8) * 2));
                 uint8_t* dst = Es + kb * e_kb_bytes + (b >> 3) * 1024 + (b & 7) * 128 + ((cc ^ (b & 7)) << 4);
-                *reinterpret_cast<uint4*>(dst) = v;
+                const uint8_t* src = static_cast<const uint8_t*>(a.w1) + (static_cast<size_t>(s_prev[b]) * a.r + c16 * 8) * 2;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
             }
+            asm volatile("cp.async.wait_all;" ::: "memory");
             fence_proxy_async_smem();
             named_bar_sync(kBarStep, kStepThreads);
 
