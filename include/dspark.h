@@ -2,8 +2,9 @@
  * dspark.h -- C ABI of the DSpark draft-sampling / verification hot path on one
  * GB300 (sm_103a).
  *
- * Four operations, each one kernel launch on the caller's stream (after a
- * memset of the workspace header):
+ * Four operations, each one kernel launch on the caller's stream (after a small
+ * kernel that clears the workspace header; the scheduler's kernels clear their
+ * own status word):
  *
  *   dspark_draft_logits   base logits of the draft LM head (tcgen05 GEMM)
  *   dspark_markov_sample  N-step Markov-biased Gumbel-max sampling (one
